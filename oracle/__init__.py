@@ -1,0 +1,207 @@
+"""CPU oracle for the SwiGLU MLP block -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never uses it and it
+never uses the CUDA library: the two share no code.  Inputs are bf16 bit
+patterns (``uint16`` numpy arrays or ``torch.bfloat16`` CPU tensors) or, for
+the finite-difference pins, fp64 arrays; every result is an fp64 numpy array.
+
+The arithmetic lives in ``swiglu_oracle.c`` (plain C loops, fp64, OpenMP over
+independent outputs); this module only compiles it on demand and marshals
+arguments.  Formulas and rounding points are documented there; they follow the
+"SwiGLU MLP Drop-H technical report" (lgystoic.github.io/notes/
+swiglu-mlp-drop-h/), forward/backward formulas and fused-kernel pseudo-code,
+and the "SwiGLU MLP forward/backward optimization" note (lgystoic.github.io/
+notes/swiglu-mlp-forward-backward-optimization/), section 2 (silu' forms).
+
+Parity pins (tests/test_oracle.py): silu' against a central finite difference;
+the whole gradient chain against finite differences of L = sum(dy * y); the
+unrounded chain against torch fp64 autograd; bf16 rounding against torch's
+fp32->bf16 conversion and hand-worked ties; closed forms at g = 0, +-20;
+permutation weights, where every product reduces to a gather.  No function
+here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "swiglu_oracle.c")
+_LIB = os.path.join(_HERE, "libswiglu_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, no fast-math, OpenMP) if stale."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            d, i64, i32 = ctypes.c_double, ctypes.c_int64, ctypes.c_int
+            vp = ctypes.c_void_p
+            lib.oracle_round_bf16.restype = d
+            lib.oracle_round_bf16.argtypes = [d]
+            for f in ("oracle_sigmoid", "oracle_silu", "oracle_silu_prime"):
+                getattr(lib, f).restype = d
+                getattr(lib, f).argtypes = [d]
+            lib.oracle_swiglu_fwd.restype = i32
+            lib.oracle_swiglu_fwd.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, vp, i64, i32,
+                                              vp, vp, vp]
+            lib.oracle_swiglu_bwd_rows.restype = i32
+            lib.oracle_swiglu_bwd_rows.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, i64,
+                                                   i32, vp, vp, vp, vp]
+            lib.oracle_swiglu_bwd_cols.restype = i32
+            lib.oracle_swiglu_bwd_cols.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, i64,
+                                                   i32, vp, vp]
+            lib.oracle_num_threads.restype = i32
+            lib.oracle_num_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _bits(a) -> np.ndarray:
+    """bf16 tensor / uint16 bit-pattern array / float64 array -> contiguous numpy array."""
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        import torch
+        return a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.float64":
+        return a.detach().cpu().contiguous().numpy()
+    arr = np.ascontiguousarray(a)
+    if arr.dtype not in (np.uint16, np.float64):
+        raise TypeError(f"expected bf16 bit patterns (uint16) or float64, got {arr.dtype}")
+    return arr
+
+
+def _kind(*arrs) -> int:
+    """0 when every input is bf16 bits, 1 when every input is fp64."""
+    kinds = {a.dtype for a in arrs}
+    if len(kinds) != 1:
+        raise TypeError("inputs must be all bf16 or all float64")
+    return int(kinds.pop() == np.float64)
+
+
+def _index(idx, n):
+    if idx is None:
+        return None, n
+    arr = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
+    return arr, arr.size
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def round_bf16(v: float) -> float:
+    return float(_load().oracle_round_bf16(float(v)))
+
+
+def sigmoid(g: float) -> float:
+    return float(_load().oracle_sigmoid(float(g)))
+
+
+def silu(g: float) -> float:
+    return float(_load().oracle_silu(float(g)))
+
+
+def silu_prime(g: float) -> float:
+    return float(_load().oracle_silu_prime(float(g)))
+
+
+def fwd(x, W1, W2, rows=None, round_intermediates: bool = True):
+    """Forward for the selected token rows (all rows when ``rows`` is None).
+
+    Returns (preact [n,2H], h [n,H], y [n,Dout]) as fp64 arrays.
+    """
+    xb, w1b, w2b = _bits(x), _bits(W1), _bits(W2)
+    M, D = xb.shape
+    H = w1b.shape[0] // 2
+    Dout = w2b.shape[0]
+    if w1b.shape != (2 * H, D) or w2b.shape != (Dout, H):
+        raise ValueError("shape mismatch")
+    ridx, n = _index(rows, M)
+    preact = np.empty((n, 2 * H))
+    h = np.empty((n, H))
+    y = np.empty((n, Dout))
+    rc = _load().oracle_swiglu_fwd(_ptr(xb), _ptr(w1b), _ptr(w2b), _kind(xb, w1b, w2b),
+                                   M, D, H, Dout, _ptr(ridx), n,
+                                   int(round_intermediates), _ptr(preact), _ptr(h), _ptr(y))
+    if rc != 0:
+        raise MemoryError("oracle_swiglu_fwd failed")
+    return preact, h, y
+
+
+def bwd_rows(W1, W2, preact, dy, rows=None, round_intermediates: bool = True):
+    """Row-wise backward outputs for the selected token rows.
+
+    Returns (grad_h [n,H], grad_preact [n,2H], h [n,H], dx [n,D]) as fp64 arrays.
+    """
+    w1b, w2b, pb, dyb = _bits(W1), _bits(W2), _bits(preact), _bits(dy)
+    H2, D = w1b.shape
+    H = H2 // 2
+    Dout = w2b.shape[0]
+    M = pb.shape[0]
+    if pb.shape != (M, 2 * H) or dyb.shape != (M, Dout) or w2b.shape != (Dout, H):
+        raise ValueError("shape mismatch")
+    ridx, n = _index(rows, M)
+    gh = np.empty((n, H))
+    gp = np.empty((n, 2 * H))
+    h = np.empty((n, H))
+    dx = np.empty((n, D))
+    rc = _load().oracle_swiglu_bwd_rows(_ptr(w1b), _ptr(w2b), _ptr(pb), _ptr(dyb),
+                                        _kind(w1b, w2b, pb, dyb), M, D, H, Dout,
+                                        _ptr(ridx), n, int(round_intermediates),
+                                        _ptr(gh), _ptr(gp), _ptr(h), _ptr(dx))
+    if rc != 0:
+        raise MemoryError("oracle_swiglu_bwd_rows failed")
+    return gh, gp, h, dx
+
+
+def bwd_cols(x, W2, preact, dy, cols=None, round_intermediates: bool = True):
+    """Weight gradients for the selected hidden indices j (all j when ``cols`` is None).
+
+    Returns (dW2_cols [n,Dout] -- row k is the column dW2[:, cols[k]],
+             dW1_left [n,D]    -- row k is dW1[cols[k], :],
+             dW1_gate [n,D]    -- row k is dW1[H + cols[k], :]).
+    """
+    xb, w2b, pb, dyb = _bits(x), _bits(W2), _bits(preact), _bits(dy)
+    M, D = xb.shape
+    Dout, H = w2b.shape
+    if pb.shape != (M, 2 * H) or dyb.shape != (M, Dout):
+        raise ValueError("shape mismatch")
+    cidx, n = _index(cols, H)
+    dW2c = np.empty((n, Dout))
+    dW1 = np.empty((2 * n, D))
+    rc = _load().oracle_swiglu_bwd_cols(_ptr(xb), _ptr(w2b), _ptr(pb), _ptr(dyb),
+                                        _kind(xb, w2b, pb, dyb), M, D, H, Dout,
+                                        _ptr(cidx), n, int(round_intermediates),
+                                        _ptr(dW2c), _ptr(dW1))
+    if rc != 0:
+        raise MemoryError("oracle_swiglu_bwd_cols failed")
+    return dW2c, dW1[:n], dW1[n:]
+
+
+def bwd_full(x, W1, W2, preact, dy, round_intermediates: bool = True):
+    """Whole backward on a small problem: (grad_h, grad_preact, h, dx, dW1 [2H,D], dW2 [Dout,H])."""
+    gh, gp, h, dx = bwd_rows(W1, W2, preact, dy, None, round_intermediates)
+    dW2c, dW1l, dW1g = bwd_cols(x, W2, preact, dy, None, round_intermediates)
+    return gh, gp, h, dx, np.concatenate([dW1l, dW1g], axis=0), dW2c.T.copy()
