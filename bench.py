@@ -1,0 +1,392 @@
+"""Benchmark: one training step of the SwiGLU MLP block (forward + backward) at the
+pages' target shape M=11136, D=3584, H=14336, Dout=3584, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  `value` is whole-step TFLOP/s (fwd 6MDH + bwd
+12MDH flops per step, summed over ranks) from CUDA events around K steps whose
+inputs are resident in HBM (468 MB of inputs per step, larger than the 129 MB
+L2, so no flush is needed).  Per-kernel durations come from the library's launch
+trace (events around every kernel, on its stream) over the same timed region.
+`e2e` repeats the step through the public API with the inputs copied in from
+pinned host memory and the outputs copied back every step.  `cpu_baseline` times
+the fp64 CPU oracle on a bounded sample of the same workload.
+
+Multi-GPU: the block does not shard here; each rank runs an independent replica
+(weak scaling), ranks meet only at the barriers around the timed region.
+
+--impl reference times the CPU oracle (the only reference this method has)
+on the host cores, on a bounded per-step sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "target"
+# The pages' own number for this workload: drop-h path, full fwd+bwd 7.3664 ms on a B200
+# (Drop-H report, single-MLP target-shape table) -> 10299.0 GF / 7.3664 ms.
+PAGES_FULL_MS_B200 = 7.3664
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": seen, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle sample
+
+def oracle_sample(s, x, W1, W2, dy, preact, n_rows: int, n_cols: int, seed: int = 0):
+    """Run the CPU oracle on a sample of the workload: forward and row-wise backward
+    for n_rows token rows, weight gradients for n_cols hidden columns.
+    Returns (seconds, flops, threads)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(s.M, size=n_rows, replace=False)
+    cols = rng.choice(s.H, size=n_cols, replace=False)
+    t0 = time.perf_counter()
+    if n_rows:
+        oracle.fwd(x, W1, W2, rows=rows)
+        oracle.bwd_rows(W1, W2, preact, dy, rows=rows)
+    if n_cols:
+        oracle.bwd_cols(x, W2, preact, dy, cols=cols)
+    dt = time.perf_counter() - t0
+    per_row = 2 * (s.D * 2 * s.H + s.H * s.Dout) + 2 * (s.Dout * s.H + 2 * s.H * s.D)
+    per_col = 2 * s.M * s.Dout * 2 + 2 * 2 * s.M * s.D
+    return dt, n_rows * per_row + n_cols * per_col, oracle.num_threads()
+
+
+def cpu_baseline(s, x, W1, W2, dy, preact, seconds: float):
+    """Size a sample to about `seconds` of CPU time from a one-row calibration, then time it."""
+    dt1, f1, _ = oracle_sample(s, x, W1, W2, dy, preact, 2, 0, seed=99)
+    rate = f1 / max(dt1, 1e-6)
+    per_row = f1 / 2
+    per_col = 2 * s.M * s.Dout * 2 + 2 * 2 * s.M * s.D
+    budget = rate * seconds
+    n_cols = max(1, int(0.25 * budget / per_col))
+    n_rows = max(1, int((budget - n_cols * per_col) / per_row))
+    dt, flops, threads = oracle_sample(s, x, W1, W2, dy, preact, n_rows, n_cols)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"fwd + row-wise bwd for {n_rows} of {s.M} token rows and weight grads for {n_cols} "
+                      f"of {s.H} hidden columns of the target block ({flops / 1e9:.1f} GFLOP in {dt:.1f} s, fp64)"}
+
+
+# ----------------------------------------------------------------------------- profile summary
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bwd_gemm_epilogue_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kind: str):
+    """DRAM bytes per launch of `kind` from the committed ncu summary, or None when the
+    kernel sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        data = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    if data.get("source_hash") != kernel_source_hash():
+        return None
+    k = data.get("kernels", {}).get(kind)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from bwd_gemm_epilogue_gb300 import binding, ledger, workloads
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws_n > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    s, x_h, W1_h, W2_h, dy_h = workloads.make_block(WORKLOAD)
+    M, D, H, Do = s.M, s.D, s.H, s.Dout
+    flops = ledger.gemm_flops(M, D, H, Do)
+
+    x, W1, W2, dy = (t.to(dev) for t in (x_h, W1_h, W2_h, dy_h))
+    preact = torch.empty(M, 2 * H, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(M, Do, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty(M, D, dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty(2 * H, D, dtype=torch.bfloat16, device=dev)
+    dW2 = torch.empty(Do, H, dtype=torch.bfloat16, device=dev)
+    ws_f = torch.empty(binding.swiglu_mlp_fwd_workspace_size(M, D, H, Do), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(binding.swiglu_mlp_bwd_workspace_size(M, D, H, Do), dtype=torch.uint8, device=dev)
+
+    def step():
+        binding.swiglu_mlp_fwd(x, W1, W2, preact, y, ws_f)
+        binding.swiglu_mlp_bwd(x, W1, W2, preact, dy, dx, dW1, dW2, ws_b)
+
+    def barrier():
+        if ws_n > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    st = binding.swiglu_mlp_device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"warm-up failed: {binding.swiglu_mlp_strerror(st)}")
+
+    K = args.steps
+    trace = binding.LaunchTrace(6 * K)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with trace:
+        ev0.record()
+        for _ in range(K):
+            step()
+        ev1.record()
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    st = binding.swiglu_mlp_device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"timed steps failed: {binding.swiglu_mlp_strerror(st)}")
+    ms = ev0.elapsed_time(ev1) / K
+    if ws_n > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    recs = trace.records()
+    launches = trace.count
+
+    per_kind = {}
+    for kind, kms in recs:
+        per_kind.setdefault(kind, []).append(kms)
+    kstats = {}
+    total_kernel_ms = sum(sum(v) for v in per_kind.values())
+    kb = ledger.kernel_bytes(M, D, H, Do)
+    pk, pk_src = peaks()
+    for kind, v in per_kind.items():
+        avg = sum(v) / len(v)
+        kstats[kind] = {"launches": len(v), "avg_us": round(avg * 1e3, 2),
+                        "tflops": round(flops[kind] / (avg * 1e-3) / 1e12, 1),
+                        "frac_of_sustained_peak": round(flops[kind] / (avg * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 3),
+                        "hbm_gbs_compulsory": round(kb[kind] / (avg * 1e-3) / 1e9, 1),
+                        "share": round(sum(v) / total_kernel_ms, 3)}
+    dom = max(kstats, key=lambda k: kstats[k]["share"])
+    dom_achieved = kstats[dom]["tflops"]
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": dom_achieved,
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(dom_achieved / pk["bf16_tflops_sustained"], 3),
+                "traffic": measured_traffic(dom),
+                "peak_source": f"{pk_src} bf16_tflops_sustained (kernel timed inside a long step)"}
+    fused = kstats.get("bwd_grad_h", {})
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    hx, hW1, hW2, hdy = (pin(t) for t in (x_h, W1_h, W2_h, dy_h))
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (y, dx, dW1, dW2)]
+    bi = sum(t.numel() * t.element_size() for t in (hx, hW1, hW2, hdy))
+    bo = sum(t.numel() * t.element_size() for t in outs_h)
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        W1.copy_(hW1, non_blocking=True)
+        W2.copy_(hW2, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        step()
+        for dst, src in zip(outs_h, (y, dx, dW1, dW2)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if ws_n > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        pre_h = preact.cpu()
+        cpu = cpu_baseline(s, x_h, W1_h, W2_h, dy_h, pre_h, args.cpu_seconds)
+
+    value = ws_n * flops["step"] / (ms * 1e-3) / 1e12
+    out = {
+        "metric": "SwiGLU MLP fwd+bwd TFLOP/s (bf16, 11136x3584x14336); fused grad_preact us",
+        "value": round(value, 1),
+        "unit": "TFLOP/s",
+        "n_gpus": ws_n,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / ws_n / (flops["step"] / (PAGES_FULL_MS_B200 * 1e-3) / 1e12), 3),
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations/dy, N(0,1/fan_in) weights, bf16)",
+        "config": {"workload": f"SwiGLU MLP block fwd+bwd, M={M} D={D} H={H} Dout={Do}, drop-h, bf16",
+                   "M": M, "D": D, "H": H, "Dout": Do, "parallelism": f"replicas x{ws_n}",
+                   "l2": "inputs larger than L2 (468 MB per step), no flush"},
+        "fused_grad_preact_us": fused.get("avg_us"),
+        "fused_grad_preact_tflops": fused.get("tflops"),
+        "fwd_ms": round(sum(kstats[k]["avg_us"] for k in ("fwd_preact", "fwd_down")) / 1e3, 4),
+        "bwd_ms": round(sum(kstats[k]["avg_us"] for k in ("bwd_grad_h", "bwd_dW2", "bwd_dx", "bwd_dW1")) / 1e3, 4),
+        "kernels": kstats,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(ws_n * flops["step"] / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws_n > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from bwd_gemm_epilogue_gb300 import ledger, workloads
+    s, x, W1, W2, dy = workloads.make_block(WORKLOAD)
+    preact = workloads.make_preact(s, workloads.CONFIGS[WORKLOAD]["seed"])
+    # per-step sample: a few token rows, sized so warm-up + steps take about two minutes
+    dt1, f1, threads = oracle_sample(s, x, W1, W2, dy, preact, 1, 0, seed=7)
+    per_step_s = 120.0 / max(1, args.steps + args.warmup)
+    n_rows = max(1, int(per_step_s / max(dt1, 1e-6)))
+    for i in range(args.warmup):
+        oracle_sample(s, x, W1, W2, dy, preact, n_rows, 0, seed=100 + i)
+    tot_t, tot_f = 0.0, 0
+    for i in range(args.steps):
+        dt, f, threads = oracle_sample(s, x, W1, W2, dy, preact, n_rows, 0, seed=1000 + i)
+        tot_t += dt
+        tot_f += f
+    value = tot_f / tot_t / 1e12
+    flops = ledger.gemm_flops(s.M, s.D, s.H, s.Dout)
+    sample = (f"fwd + row-wise bwd for {n_rows} of {s.M} token rows per step of the target block "
+              f"(fp64 oracle, {threads} threads)")
+    out = {
+        "impl": "reference",
+        "metric": "SwiGLU MLP fwd+bwd TFLOP/s (bf16, 11136x3584x14336); fused grad_preact us",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": flops["step"] / (value * 1e12) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations/dy, N(0,1/fan_in) weights, bf16)",
+        "config": {"workload": f"SwiGLU MLP block fwd+bwd, M={s.M} D={s.D} H={s.H} Dout={s.Dout}, drop-h, bf16",
+                   "M": s.M, "D": s.D, "H": s.H, "Dout": s.Dout, "parallelism": "cpu oracle"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

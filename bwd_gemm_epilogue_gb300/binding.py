@@ -1,0 +1,267 @@
+"""ctypes binding of the C ABI in ``include/swiglu_mlp.h`` -- argument marshalling only.
+
+Each function has the name of the C entry point it calls and takes torch CUDA
+tensors (bf16, contiguous) for the pointer arguments; torch supplies device
+memory and the current stream, every step of the computation runs in the
+library's kernels.  Outputs and workspaces the caller does not pass are
+allocated with torch.  A non-OK status raises ``SwigluError``; a missing
+library raises ``RuntimeError`` (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libswiglu_mlp.so")
+
+STATUS_NAMES = {
+    0: "SWIGLU_OK",
+    1: "SWIGLU_ERR_INVALID_ARG",
+    2: "SWIGLU_ERR_UNSUPPORTED_SHAPE",
+    3: "SWIGLU_ERR_MISALIGNED",
+    4: "SWIGLU_ERR_WORKSPACE_TOO_SMALL",
+    5: "SWIGLU_ERR_LAUNCH",
+    6: "SWIGLU_ERR_TIMEOUT",
+    7: "SWIGLU_ERR_CUDA",
+}
+
+# Every symbol include/swiglu_mlp.h declares: name -> (restype, argtypes)
+_vp, _i64, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
+SIGNATURES = {
+    "swiglu_mlp_fwd_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "swiglu_mlp_bwd_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
+    "swiglu_mlp_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "swiglu_mlp_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "swiglu_mlp_fused_grad_preact": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "swiglu_mlp_gemm_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
+    "swiglu_mlp_device_status": (_i32, [_vp]),
+    "swiglu_mlp_strerror": (ctypes.c_char_p, [_i32]),
+    "swiglu_mlp_set_wait_timeout_ns": (None, [_u64]),
+    "swiglu_mlp_set_debug_flags": (None, [_i32]),
+    "swiglu_mlp_trace_begin": (None, [_vp, _vp, _i32]),
+    "swiglu_mlp_trace_end": (_i32, []),
+    "swiglu_mlp_abi_version": (_i32, []),
+}
+
+KERNEL_KINDS = {1: "fwd_preact", 2: "fwd_down", 3: "bwd_grad_h", 4: "bwd_dW2", 5: "bwd_dx", 6: "bwd_dW1", 7: "gemm"}
+
+
+class SwigluError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise SwigluError(status, where)
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if t.dtype != torch.bfloat16 and t.dtype != torch.uint8:
+        raise TypeError(f"expected bf16 (or a uint8 workspace), got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _empty(shape, like: torch.Tensor) -> torch.Tensor:
+    return torch.empty(shape, dtype=torch.bfloat16, device=like.device)
+
+
+# ---------------------------------------------------------------------------- sizes / status
+
+def swiglu_mlp_fwd_workspace_size(M: int, D: int, H: int, Dout: int) -> int:
+    return int(lib().swiglu_mlp_fwd_workspace_size(M, D, H, Dout))
+
+
+def swiglu_mlp_bwd_workspace_size(M: int, D: int, H: int, Dout: int) -> int:
+    return int(lib().swiglu_mlp_bwd_workspace_size(M, D, H, Dout))
+
+
+def swiglu_mlp_strerror(status: int) -> str:
+    return lib().swiglu_mlp_strerror(status).decode()
+
+
+def swiglu_mlp_device_status(device=None) -> int:
+    """Synchronise the current stream and return the device status code (0 = OK)."""
+    return int(lib().swiglu_mlp_device_status(_stream(device)))
+
+
+def swiglu_mlp_set_wait_timeout_ns(ns: int) -> None:
+    lib().swiglu_mlp_set_wait_timeout_ns(int(ns))
+
+
+def swiglu_mlp_set_debug_flags(flags: int) -> None:
+    lib().swiglu_mlp_set_debug_flags(int(flags))
+
+
+def swiglu_mlp_abi_version() -> int:
+    return int(lib().swiglu_mlp_abi_version())
+
+
+class LaunchTrace:
+    """Brackets every kernel launch of the library (from this thread) with CUDA
+    events, for per-kernel timing inside larger calls:
+
+        with LaunchTrace(capacity) as tr:
+            ...calls...
+        tr.records()  ->  [(kind_name, milliseconds), ...] in launch order
+    """
+
+    def __init__(self, capacity: int):
+        self.capacity = int(capacity)
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * self.capacity)]
+        for e in self.events:          # torch creates the CUDA event lazily, on first record
+            e.record()
+        torch.cuda.synchronize()
+        self._handles = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self._kinds = (ctypes.c_int * self.capacity)()
+        self.count = 0
+
+    def __enter__(self):
+        lib().swiglu_mlp_trace_begin(ctypes.cast(self._handles, ctypes.c_void_p),
+                                     ctypes.cast(self._kinds, ctypes.c_void_p), self.capacity)
+        return self
+
+    def __exit__(self, *exc):
+        self.count = int(lib().swiglu_mlp_trace_end())
+        return False
+
+    def records(self):
+        torch.cuda.synchronize()
+        n = min(self.count, self.capacity)
+        return [(KERNEL_KINDS.get(self._kinds[i], str(self._kinds[i])),
+                 self.events[2 * i].elapsed_time(self.events[2 * i + 1])) for i in range(n)]
+
+
+# ---------------------------------------------------------------------------- compute
+
+def _dims(x, W1, W2):
+    M, D = x.shape
+    H2, D1 = W1.shape
+    Dout, H = W2.shape
+    if D1 != D or H2 != 2 * H:
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)}, W1 {tuple(W1.shape)}, W2 {tuple(W2.shape)}")
+    return M, D, H, Dout
+
+
+def swiglu_mlp_fwd(x, W1, W2, preact=None, y=None, workspace=None):
+    """Forward; returns (preact [M,2H], y [M,Dout])."""
+    M, D, H, Dout = _dims(x, W1, W2)
+    preact = _empty((M, 2 * H), x) if preact is None else preact
+    y = _empty((M, Dout), x) if y is None else y
+    need = swiglu_mlp_fwd_workspace_size(M, D, H, Dout)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    st = lib().swiglu_mlp_fwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), M, D, H, Dout,
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(x.device))
+    _check(st, "swiglu_mlp_fwd")
+    return preact, y
+
+
+def swiglu_mlp_bwd(x, W1, W2, preact, dy, dx=None, dW1=None, dW2=None, workspace=None):
+    """Backward; returns (dx [M,D], dW1 [2H,D], dW2 [Dout,H])."""
+    M, D, H, Dout = _dims(x, W1, W2)
+    if tuple(preact.shape) != (M, 2 * H) or tuple(dy.shape) != (M, Dout):
+        raise ValueError("preact / dy shape mismatch")
+    dx = _empty((M, D), x) if dx is None else dx
+    dW1 = _empty((2 * H, D), x) if dW1 is None else dW1
+    dW2 = _empty((Dout, H), x) if dW2 is None else dW2
+    need = swiglu_mlp_bwd_workspace_size(M, D, H, Dout)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    st = lib().swiglu_mlp_bwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dW1),
+                              _ptr(dW2), M, D, H, Dout, _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(x.device))
+    _check(st, "swiglu_mlp_bwd")
+    return dx, dW1, dW2
+
+
+def bwd_workspace_views(workspace: torch.Tensor, M: int, H: int):
+    """(h [M,H], grad_preact [M,2H]) views of a backward workspace."""
+    off = ((M * H * 2) + 255) // 256 * 256
+    h = workspace[: M * H * 2].view(torch.bfloat16).view(M, H)
+    gp = workspace[off: off + M * 2 * H * 2].view(torch.bfloat16).view(M, 2 * H)
+    return h, gp
+
+
+def swiglu_mlp_fused_grad_preact(dy, W2, preact, grad_preact=None, h=None):
+    """The fused grad_h GEMM + SwiGLU backward alone; returns (grad_preact [M,2H], h [M,H])."""
+    M, Dout = dy.shape
+    Dout2, H = W2.shape
+    if Dout2 != Dout or tuple(preact.shape) != (M, 2 * H):
+        raise ValueError("shape mismatch")
+    grad_preact = _empty((M, 2 * H), dy) if grad_preact is None else grad_preact
+    h = _empty((M, H), dy) if h is None else h
+    st = lib().swiglu_mlp_fused_grad_preact(_ptr(dy), _ptr(W2), _ptr(preact), _ptr(grad_preact), _ptr(h),
+                                            M, H, Dout, _stream(dy.device))
+    _check(st, "swiglu_mlp_fused_grad_preact")
+    return grad_preact, h
+
+
+def swiglu_mlp_gemm_bf16(A, B, M: int, N: int, K: int, a_mn_major: bool, b_mn_major: bool, C=None):
+    """C [M,N] = A * B^T; A is [M,K] (or [K,M] if a_mn_major), B is [N,K] (or [K,N] if b_mn_major)."""
+    C = _empty((M, N), A) if C is None else C
+    st = lib().swiglu_mlp_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(a_mn_major), int(b_mn_major),
+                                    _stream(A.device))
+    _check(st, "swiglu_mlp_gemm_bf16")
+    return C
+
+
+class SwiGLUMLP(torch.autograd.Function):
+    """autograd wrapper: forward saves (x, W1, W2, preact) and drops h; backward
+    calls swiglu_mlp_bwd.  Leading dimensions of x are flattened."""
+
+    @staticmethod
+    def forward(ctx, x, W1, W2):
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        preact, y = swiglu_mlp_fwd(x2, W1.contiguous(), W2.contiguous())
+        ctx.save_for_backward(x2, W1, W2, preact)
+        return y.reshape(*x.shape[:-1], y.shape[-1])
+
+    @staticmethod
+    def backward(ctx, grad_y):
+        x2, W1, W2, preact = ctx.saved_tensors
+        dy = grad_y.reshape(-1, grad_y.shape[-1]).contiguous()
+        dx, dW1, dW2 = swiglu_mlp_bwd(x2, W1.contiguous(), W2.contiguous(), preact, dy)
+        return dx.reshape(*grad_y.shape[:-1], dx.shape[-1]), dW1, dW2
+
+
+def swiglu_mlp(x, W1, W2):
+    return SwiGLUMLP.apply(x, W1, W2)

@@ -1,0 +1,557 @@
+// gemm_kernel.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a with
+// the SwiGLU MLP block's three epilogues.
+//
+//   C[M, N] = A[M, K] * B[N, K]^T        bf16 in, fp32 accumulate in TMEM
+//
+// A and B are each either K-major (K contiguous in memory) or MN-major (M or N
+// contiguous); the TMA boxes and the UMMA shared-memory descriptors differ, the
+// rest of the kernel does not.  One CTA per SM, 256 threads:
+//
+//   warp 0      TMA producer: A/B k-blocks into a STAGES-deep shared-memory ring
+//   warp 1      MMA issuer: tcgen05.mma 128x256x16 into one of two TMEM
+//               accumulators (2 x 256 fp32 columns = all 512 TMEM columns)
+//   warp 2      epilogue-input producer (SWIGLU_BWD only): TMA-prefetches the
+//               saved preact left/gate sub-tiles the epilogue consumes
+//   warp 3      idle
+//   warps 4..7  epilogue: TMEM -> registers (lane quadrant = warp % 4), the
+//               epilogue math, bf16 tiles staged in shared memory, TMA stores
+//
+// Epilogues:
+//   EPI_STORE       C = acc rounded to bf16.
+//   EPI_SWIGLU_FWD  B holds two W1 row slabs, [j0, j0+128) and [H+j0, H+j0+128), so
+//                   accumulator columns [0,128) are `left` and [128,256) the matching
+//                   `gate`.  Stores preact (both halves, bf16) and
+//                   h = bf16(left * bf16(silu(gate))) computed from the bf16 preact.
+//   EPI_SWIGLU_BWD  acc = grad_h[m0:, j0:j0+256] (dy @ W2), never written out.  With the
+//                   prefetched left/gate: dleft = grad_h * silu(gate),
+//                   dgate = grad_h * left * silu'(gate), silu' = sigma + silu*(1 - sigma),
+//                   h = bf16(left * bf16(silu(gate))); stores grad_preact = [dleft|dgate]
+//                   and h.
+// The SwiGLU forms follow the "SwiGLU MLP Drop-H technical report" (original math,
+// and the fused backward kernel's pseudo-code) and the fused dout-GEMM + SwiGLU
+// backward of the "SwiGLU MLP forward/backward optimization" note (section 4): the
+// activation gradient stays on chip, sigma/silu are recomputed from the saved preact.
+//
+// Every mbarrier wait is bounded (GemmParams::timeout_ns, on %globaltimer); a wait
+// that runs out records its role in the device error word, raises a CTA-wide abort
+// flag, every role stops issuing, drains what it has in flight (again bounded),
+// and the CTA frees its TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace swiglu {
+
+enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;            // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;
+constexpr int NUM_THREADS = 256;
+constexpr int EPI_WARP0 = 4;
+constexpr int CHUNK = 32;         // epilogue columns per TMEM load
+constexpr uint32_t TMEM_COLS = 512;
+
+// Device error word bits (one per role that gave up waiting).
+constexpr int ERR_PRODUCER = 1, ERR_MMA = 2, ERR_EPILOGUE = 4, ERR_AUX = 8;
+// Test hook: the producer issues nothing, so the consumers' waits run out.
+constexpr int DEBUG_SKIP_PRODUCER = 1;
+
+struct GemmParams {
+    int M;            // GEMM rows
+    int N;            // EPI_STORE: GEMM columns; SWIGLU epilogues: H
+    int K;
+    int tiles_m, tiles_n, num_tiles;
+    int band;         // n-tiles per raster band (L2 reuse)
+    int k_blocks;
+    unsigned long long timeout_ns;
+    int* err;         // device error word
+    int debug_flags;
+};
+
+template <int EPI>
+struct Cfg {
+    static constexpr int STAGES = (EPI == EPI_STORE) ? 4 : 3;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int NOUT = (EPI == EPI_STORE) ? 1 : 3;
+    static constexpr int OUT_TILE = 32 * CHUNK * 2;               // one warp's 32x32 bf16 tile
+    static constexpr int OUT_BUFS = 2;
+    static constexpr int OUT_WARP_BYTES = OUT_BUFS * NOUT * OUT_TILE;
+    static constexpr int EIN_SLOTS = (EPI == EPI_SWIGLU_BWD) ? 2 : 0;
+    static constexpr int EIN_HALF = BM * CHUNK * 2;               // 128 rows x 32 cols bf16
+    static constexpr int EIN_SLOT_BYTES = 2 * EIN_HALF;           // left + gate
+    static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CHUNK : BN / CHUNK;
+
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_EIN = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_OUT = OFF_EIN + EIN_SLOTS * EIN_SLOT_BYTES;
+    static constexpr int OFF_BAR = OFF_OUT + 4 * OUT_WARP_BYTES;
+    // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], ein_full[E], ein_empty[E], drain
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EIN_SLOTS + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;       // tmem base, abort flag
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;           // slack to align the base
+};
+
+// ---------------------------------------------------------------------------
+// UMMA descriptors
+// ---------------------------------------------------------------------------
+
+// Shared-memory matrix descriptor, 128-byte swizzle.
+//   K-major : rows of 64 bf16 (128 B), 8-row groups 1024 B apart (SBO); LBO unused.
+//   MN-major: 64 MN-contiguous elements per 128-B row, one row per k; 8-k-row groups
+//             1024 B apart (SBO); 64-element MN blocks `mn_block_bytes` apart (LBO).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;   // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A/B, fp32 D, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t umma_idesc(bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                          // D format f32
+           | (1u << 7)                        // A format bf16
+           | (1u << 10)                       // B format bf16
+           | ((a_mn_major ? 1u : 0u) << 15)   // A major-ness
+           | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
+           | ((uint32_t)(BN >> 3) << 17)      // N >> 3
+           | ((uint32_t)(BM >> 4) << 24);     // M >> 4
+}
+
+// ---------------------------------------------------------------------------
+// helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& tm, int& tn) {
+    const int band_tiles = p.band * p.tiles_m;
+    const int b = t / band_tiles;
+    const int r = t - b * band_tiles;
+    const int n0 = b * p.band;
+    const int w = min(p.band, p.tiles_n - n0);
+    tm = r / w;
+    tn = n0 + (r - tm * w);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (after recording `role` in the
+// error word and raising the CTA abort flag) when the limit runs out, or when
+// another role has already aborted.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmParams& p,
+                                          volatile int* abort_flag, int role) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - start > p.timeout_ns) {
+                *abort_flag = 1;
+                atomicOr(p.err, role);
+                return false;
+            }
+        }
+    }
+}
+
+// Short bounded wait used only while draining after an abort.
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t start = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - start > limit_ns) return;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float round_bf16(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// sigma(g) = 1 / (1 + e^-g) with e^-g = 2^(-g * log2 e): MUFU ex2 then MUFU rcp.
+// g -> -inf: ex2 -> +inf, rcp -> 0.  g -> +inf: ex2 -> 0, sigma -> 1.
+__device__ __forceinline__ float sigmoid_mufu(float g) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    return ptx::rcp_approx(1.0f + ptx::ex2_approx(-g * kLog2e));
+}
+
+// 16-byte unit `c` (0..3) of row `r` in a [rows][64 B] tile with 64-byte swizzle.
+__device__ __forceinline__ uint32_t sw64_offset(int r, int c) {
+    return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
+                const __grid_constant__ CUtensorMap tmI0, const GemmParams p) {
+    using C = Cfg<EPI>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t bar0 = base + C::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
+    auto ein_full_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 4 + s); };
+    auto ein_empty_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 4 + C::EIN_SLOTS + s); };
+    const uint32_t drain_bar = bar0 + 8u * (C::NUM_BARS - 1);
+    volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::OFF_MISC + 4);
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), 4);
+        }
+        for (int s = 0; s < C::EIN_SLOTS; ++s) {
+            ptx::mbar_init(ein_full_bar(s), 1);
+            ptx::mbar_init(ein_empty_bar(s), 4);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+        ptx::prefetch_tmap(&tmO0);
+        if (EPI != EPI_STORE) ptx::prefetch_tmap(&tmO1);
+        if (EPI == EPI_SWIGLU_BWD) ptx::prefetch_tmap(&tmI0);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32((const void*)tmem_holder), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && !(p.debug_flags & DEBUG_SKIP_PRODUCER)) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int last_parity[C::STAGES];
+#pragma unroll
+            for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(p, t, tm, tn);
+                const int m0 = tm * BM;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, abort_flag, ERR_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    last_parity[stage] = (int)phase;
+                    const int k0 = kb * BK;
+                    const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
+                    const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
+                    if (A_MN) {
+                        ptx::tma_load_2d(sA, &tmA, fb, m0, k0);
+                        ptx::tma_load_2d(sA + 8192, &tmA, fb, m0 + 64, k0);
+                    } else {
+                        ptx::tma_load_2d(sA, &tmA, fb, k0, m0);
+                    }
+                    if (EPI == EPI_SWIGLU_FWD) {
+                        const int j0 = tn * (BN / 2);
+                        ptx::tma_load_3d(sB, &tmB, fb, k0, j0, 0);
+                        ptx::tma_load_3d(sB + C::B_BYTES / 2, &tmB, fb, k0, j0, 1);
+                    } else if (B_MN) {
+                        const int n0 = tn * BN;
+#pragma unroll
+                        for (int i = 0; i < BN / 64; ++i) ptx::tma_load_2d(sB + i * 8192, &tmB, fb, n0 + 64 * i, k0);
+                    } else {
+                        ptx::tma_load_2d(sB, &tmB, fb, k0, tn * BN);
+                    }
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let the loads already issued land before the CTA's shared memory goes away.
+                for (int s = 0; s < C::STAGES; ++s)
+                    if (last_parity[s] >= 0) drain_wait(full_bar(s), (uint32_t)last_parity[s], p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc(A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+                const int ab = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, p, abort_flag, ERR_MMA)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, p, abort_flag, ERR_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
+                    const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        // K-major: the next 16 k sit 32 bytes further along each 128-B row.
+                        // MN-major: the next 16 k are the next 16 rows of 128 B.
+                        const uint64_t ad = A_MN ? umma_desc_sw128(sA + k * 2048, 8192, 1024)
+                                                 : umma_desc_sw128(sA + k * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? umma_desc_sw128(sB + k * 2048, 8192, 1024)
+                                                 : umma_desc_sw128(sB + k * 32, 16, 1024);
+                        ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty_bar(stage));
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull_bar(ab));
+            }
+            if (!ok) {
+                ptx::mma_commit(drain_bar);
+                drain_wait(drain_bar, 0, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ epilogue-input producer
+        if (EPI == EPI_SWIGLU_BWD && lane == 0) {
+            int slot = 0;
+            uint32_t phase = 0;
+            int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
+            for (int s = 0; s < C::EIN_SLOTS; ++s) last_parity[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(p, t, tm, tn);
+                const int m0 = tm * BM;
+                const int j0 = tn * BN;
+                for (int c = 0; c < C::CHUNKS; ++c) {
+                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, p, abort_flag, ERR_AUX)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = ein_full_bar(slot);
+                    ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
+                    last_parity[slot] = (int)phase;
+                    const uint32_t dst = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
+                    ptx::tma_load_3d(dst, &tmI0, fb, j0 + c * CHUNK, 0, m0);
+                    ptx::tma_load_3d(dst + C::EIN_HALF, &tmI0, fb, j0 + c * CHUNK, 1, m0);
+                    if (++slot == C::EIN_SLOTS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::EIN_SLOTS; ++s)
+                    if (last_parity[s] >= 0) drain_wait(ein_full_bar(s), (uint32_t)last_parity[s], p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= EPI_WARP0) {
+        // ------------------------------------------------------------ epilogue
+        const int wq = warp & 3;                 // TMEM lane quadrant = tile rows [32wq, 32wq+32)
+        const int row = 32 * wq + lane;          // row within the tile
+        const uint32_t out_base = base + C::OFF_OUT + wq * C::OUT_WARP_BYTES;
+        int ein_slot = 0;
+        uint32_t ein_phase = 0;
+        int ob = 0;
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+            int tm, tn;
+            tile_coords(p, t, tm, tn);
+            const int m0 = tm * BM;
+            const int mrow0 = m0 + 32 * wq;     // first output row of this warp's slice
+            const bool rows_live = mrow0 < p.M;
+            const int ab = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            // every lane observes the barrier itself (acquire), the warp agrees on the outcome
+            const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, p, abort_flag, ERR_EPILOGUE));
+            if (!got) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
+
+            for (int c = 0; c < C::CHUNKS; ++c) {
+                uint32_t acc[32];
+                uint32_t acc2[32];
+                if (EPI == EPI_SWIGLU_FWD) {
+                    ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
+                    ptx::tmem_ld_32x32b_x32(t_row + BN / 2 + c * CHUNK, acc2);
+                } else {
+                    ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
+                }
+                ptx::tmem_ld_wait();
+                if (c == C::CHUNKS - 1) {
+                    // Accumulator fully read: hand it back to the MMA warp.
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(tempty_bar(ab));
+                }
+
+                // epilogue inputs (backward): the saved preact left/gate for these 32 columns
+                uint32_t lft[16], gte[16];
+                if (EPI == EPI_SWIGLU_BWD) {
+                    const bool in_ok = __all_sync(
+                        0xffffffffu, wait_bounded(ein_full_bar(ein_slot), ein_phase, p, abort_flag, ERR_EPILOGUE));
+                    if (!in_ok) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t slot_base = base + C::OFF_EIN + ein_slot * C::EIN_SLOT_BYTES;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 l4 = ptx::lds128(slot_base + sw64_offset(row, q));
+                        const uint4 g4 = ptx::lds128(slot_base + C::EIN_HALF + sw64_offset(row, q));
+                        lft[4 * q + 0] = l4.x; lft[4 * q + 1] = l4.y; lft[4 * q + 2] = l4.z; lft[4 * q + 3] = l4.w;
+                        gte[4 * q + 0] = g4.x; gte[4 * q + 1] = g4.y; gte[4 * q + 2] = g4.z; gte[4 * q + 3] = g4.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ein_empty_bar(ein_slot));
+                    if (++ein_slot == C::EIN_SLOTS) {
+                        ein_slot = 0;
+                        ein_phase ^= 1u;
+                    }
+                }
+
+                // outputs for this chunk, packed bf16 pairs
+                uint32_t o0[16], o1[16], o2[16];
+                if (EPI == EPI_STORE) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        o0[i] = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+                } else if (EPI == EPI_SWIGLU_FWD) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t lb = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+                        const uint32_t gb = pack_bf16(__uint_as_float(acc2[2 * i]), __uint_as_float(acc2[2 * i + 1]));
+                        o0[i] = lb;
+                        o1[i] = gb;
+                        float hv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float l = e ? bf16_hi(lb) : bf16_lo(lb);
+                            const float g = e ? bf16_hi(gb) : bf16_lo(gb);
+                            const float silu = g * sigmoid_mufu(g);
+                            hv[e] = l * round_bf16(silu);
+                        }
+                        o2[i] = pack_bf16(hv[0], hv[1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float dl[2], dg[2], hv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float gh = __uint_as_float(acc[2 * i + e]);
+                            const float l = e ? bf16_hi(lft[i]) : bf16_lo(lft[i]);
+                            const float g = e ? bf16_hi(gte[i]) : bf16_lo(gte[i]);
+                            const float sig = sigmoid_mufu(g);
+                            const float silu = g * sig;
+                            const float silu_p = sig + silu * (1.0f - sig);
+                            dl[e] = gh * silu;
+                            dg[e] = gh * l * silu_p;
+                            hv[e] = l * round_bf16(silu);
+                        }
+                        o0[i] = pack_bf16(dl[0], dl[1]);
+                        o1[i] = pack_bf16(dg[0], dg[1]);
+                        o2[i] = pack_bf16(hv[0], hv[1]);
+                    }
+                }
+
+                // stage in shared memory (64-byte swizzle) and TMA-store this warp's 32x32 tiles
+                if (lane == 0) ptx::bulk_wait_group_read<C::OUT_BUFS - 1>();
+                __syncwarp();
+                const uint32_t ob_base = out_base + ob * (C::NOUT * C::OUT_TILE);
+#pragma unroll
+                for (int o = 0; o < C::NOUT; ++o) {
+                    const uint32_t* src = (o == 0) ? o0 : (o == 1) ? o1 : o2;
+                    const uint32_t tile = ob_base + o * C::OUT_TILE;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        ptx::sts128(tile + sw64_offset(lane, q),
+                                    make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]));
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && rows_live) {
+                    if (EPI == EPI_STORE) {
+                        const int n = tn * BN + c * CHUNK;
+                        if (n < p.N) ptx::tma_store_2d(&tmO0, ob_base, n, mrow0);
+                    } else {
+                        const int jw = (EPI == EPI_SWIGLU_FWD) ? BN / 2 : BN;
+                        const int j = tn * jw + c * CHUNK;
+                        if (j < p.N) {
+                            ptx::tma_store_3d(&tmO0, ob_base, j, 0, mrow0);
+                            ptx::tma_store_3d(&tmO0, ob_base + C::OUT_TILE, j, 1, mrow0);
+                            ptx::tma_store_2d(&tmO1, ob_base + 2 * C::OUT_TILE, j, mrow0);
+                        }
+                    }
+                }
+                if (lane == 0) ptx::bulk_commit_group();
+                ob ^= 1;
+            }
+        }
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        ptx::tc_fence_before();
+        __syncwarp();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace swiglu

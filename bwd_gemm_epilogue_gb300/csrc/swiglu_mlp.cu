@@ -1,0 +1,363 @@
+// swiglu_mlp.cu -- host side of the C ABI declared in include/swiglu_mlp.h:
+// argument validation, TMA tensor-map encoding, persistent-grid sizing and the
+// launches of the tcgen05 GEMM kernel variants (gemm_kernel.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_kernel.cuh"
+#include "swiglu_mlp.h"
+
+namespace swiglu {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+__device__ int g_err_word;   // device error word: ERR_* bits of roles that gave up a wait
+
+std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
+std::atomic<int> g_debug_flags{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int* err_word = nullptr;
+};
+
+struct Trace {
+    cudaEvent_t* events = nullptr;
+    int* kinds = nullptr;
+    int capacity = 0;
+    int count = 0;
+};
+thread_local Trace g_trace;
+
+std::mutex g_mutex;
+EncodeTiledFn g_encode = nullptr;
+DeviceState g_dev[kMaxDevices];
+
+swiglu_status get_device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SWIGLU_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return SWIGLU_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SWIGLU_ERR_CUDA;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_word), g_err_word) != cudaSuccess)
+            return SWIGLU_ERR_CUDA;
+        st.ready = true;
+    }
+    *out = &st;
+    return SWIGLU_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows, row
+// pitch `row_bytes`.
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
+               uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz) {
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand maps for the mainloop.  K-major: box 64 (k) x rows; MN-major: box 64 (mn) x 64 (k).
+bool encode_operand(CUtensorMap* m, const void* ptr, int64_t mn, int64_t k, bool mn_major, uint32_t rows) {
+    if (mn_major) return encode_2d(m, ptr, (uint64_t)mn, (uint64_t)k, (uint64_t)mn * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    return encode_2d(m, ptr, (uint64_t)k, (uint64_t)mn, (uint64_t)k * 2, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// [M, 2H] tensor seen as (j, half, m): element (j, half, m) = base[m*2H + half*H + j].
+bool encode_paired(CUtensorMap* m, const void* ptr, int64_t M, int64_t H, uint32_t box_rows) {
+    return encode_3d(m, ptr, (uint64_t)H, 2, (uint64_t)M, (uint64_t)H * 2, (uint64_t)H * 4, CHUNK, 1, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+bool encode_out_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+    return encode_2d(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols * 2, CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
+                     const CUtensorMap& o1, const CUtensorMap& i0, int64_t M, int64_t N, int64_t K,
+                     int64_t tiles_n, cudaStream_t stream) {
+    auto kern = gemm_kernel<EPI, A_MN, B_MN>;
+    constexpr int smem = Cfg<EPI>::SMEM_BYTES;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return SWIGLU_ERR_LAUNCH;
+    GemmParams p;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.tiles_m = (int)((M + BM - 1) / BM);
+    p.tiles_n = (int)tiles_n;
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.band = p.tiles_n < 8 ? p.tiles_n : 8;
+    p.k_blocks = (int)((K + BK - 1) / BK);
+    p.timeout_ns = g_timeout_ns.load();
+    p.err = st->err_word;
+    p.debug_flags = g_debug_flags.load();
+    const int grid = p.num_tiles < st->num_sms ? p.num_tiles : st->num_sms;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    Trace& tr = g_trace;
+    const int slot = tr.events ? tr.count++ : -1;
+    const bool traced = slot >= 0 && slot < tr.capacity;
+    if (traced) {
+        tr.kinds[slot] = kind;
+        if (cudaEventRecord(tr.events[2 * slot], stream) != cudaSuccess) return SWIGLU_ERR_CUDA;
+    }
+    if (cudaLaunchKernelEx(&cfg, kern, a, b, o0, o1, i0, p) != cudaSuccess) return SWIGLU_ERR_LAUNCH;
+    if (traced && cudaEventRecord(tr.events[2 * slot + 1], stream) != cudaSuccess) return SWIGLU_ERR_CUDA;
+    return SWIGLU_OK;
+}
+
+bool dims_ok(int64_t v) { return v > 0 && v % 8 == 0 && v < (int64_t(1) << 31); }
+
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- the block's kernels
+
+// preact = x @ W1^T with the SwiGLU forward epilogue (writes preact and h).
+swiglu_status run_fwd_preact(DeviceState* st, const void* x, const void* W1, void* preact, void* h,
+                             int64_t M, int64_t D, int64_t H, cudaStream_t s) {
+    CUtensorMap a, b, o0, o1;
+    if (!encode_operand(&a, x, M, D, false, BM)) return SWIGLU_ERR_LAUNCH;
+    // W1 [2H, D] as (k, j, half): element (k, j, half) = W1[(half*H + j)*D + k]
+    if (!encode_3d(&b, W1, (uint64_t)D, (uint64_t)H, 2, (uint64_t)D * 2, (uint64_t)H * D * 2, 64, BN / 2, 1,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return SWIGLU_ERR_LAUNCH;
+    if (!encode_paired(&o0, preact, M, H, 32)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_out_2d(&o1, h, M, H)) return SWIGLU_ERR_LAUNCH;
+    return launch<EPI_SWIGLU_FWD, false, false>(st, SWIGLU_KERNEL_FWD_PREACT, a, b, o0, o1, o0, M, H, D, (H + BN / 2 - 1) / (BN / 2), s);
+}
+
+// grad_h = dy @ W2 fused with the SwiGLU backward (writes grad_preact and h).
+swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, const void* preact,
+                            void* grad_preact, void* h, int64_t M, int64_t H, int64_t Dout, cudaStream_t s) {
+    CUtensorMap a, b, o0, o1, i0;
+    if (!encode_operand(&a, dy, M, Dout, false, BM)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_operand(&b, W2, H, Dout, true, 0)) return SWIGLU_ERR_LAUNCH;   // B(n=j, k=o) = W2[o, j]
+    if (!encode_paired(&o0, grad_preact, M, H, 32)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_out_2d(&o1, h, M, H)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_paired(&i0, preact, M, H, BM)) return SWIGLU_ERR_LAUNCH;
+    return launch<EPI_SWIGLU_BWD, false, true>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, b, o0, o1, i0, M, H, Dout, (H + BN - 1) / BN, s);
+}
+
+// C [M,N] = A * B^T with either operand K-major or MN-major.
+swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
+                       int64_t K, bool a_mn, bool b_mn, cudaStream_t s) {
+    CUtensorMap a, b, o0;
+    if (!encode_operand(&a, A, M, K, a_mn, BM)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_operand(&b, B, N, K, b_mn, BN)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_out_2d(&o0, Cp, M, N)) return SWIGLU_ERR_LAUNCH;
+    const int64_t tiles_n = (N + BN - 1) / BN;
+    if (!a_mn && !b_mn) return launch<EPI_STORE, false, false>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    if (!a_mn && b_mn) return launch<EPI_STORE, false, true>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    if (a_mn && b_mn) return launch<EPI_STORE, true, true>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    return launch<EPI_STORE, true, false>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+}
+
+}  // namespace
+}  // namespace swiglu
+
+using namespace swiglu;
+
+extern "C" {
+
+size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
+    (void)D;
+    (void)Dout;
+    if (M <= 0 || H <= 0) return 0;
+    return round256((size_t)M * (size_t)H * 2);
+}
+
+size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
+    (void)D;
+    (void)Dout;
+    if (M <= 0 || H <= 0) return 0;
+    return round256((size_t)M * (size_t)H * 2) + round256((size_t)M * (size_t)H * 4);
+}
+
+swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2, void* preact, void* y, int64_t M,
+                             int64_t D, int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
+        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return SWIGLU_OK;
+    if (!x || !W1 || !W2 || !preact || !y || !workspace) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(preact) || !aligned16(y) ||
+        !aligned16(workspace))
+        return SWIGLU_ERR_MISALIGNED;
+    if (workspace_bytes < swiglu_mlp_fwd_workspace_size(M, D, H, Dout)) return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+    DeviceState* st;
+    swiglu_status rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* h = workspace;
+    rc = run_fwd_preact(st, x, W1, preact, h, M, D, H, s);
+    if (rc != SWIGLU_OK) return rc;
+    return run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h, W2, y, M, Dout, H, false, false, s);   // y = h @ W2^T
+}
+
+swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
+                             void* dx, void* dW1, void* dW2, int64_t M, int64_t D, int64_t H, int64_t Dout,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
+        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    if (!W1 || !W2 || !dW1 || !dW2) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(dW1) || !aligned16(dW2)) return SWIGLU_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M == 0) {
+        if (cudaMemsetAsync(dW1, 0, (size_t)2 * H * D * 2, s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+        if (cudaMemsetAsync(dW2, 0, (size_t)Dout * H * 2, s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+        return SWIGLU_OK;
+    }
+    if (!x || !preact || !dy || !dx || !workspace) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(preact) || !aligned16(dy) || !aligned16(dx) || !aligned16(workspace))
+        return SWIGLU_ERR_MISALIGNED;
+    if (workspace_bytes < swiglu_mlp_bwd_workspace_size(M, D, H, Dout)) return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+    DeviceState* st;
+    swiglu_status rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    void* h = workspace;
+    void* grad_preact = static_cast<uint8_t*>(workspace) + round256((size_t)M * (size_t)H * 2);
+    rc = run_fused_bwd(st, dy, W2, preact, grad_preact, h, M, H, Dout, s);
+    if (rc != SWIGLU_OK) return rc;
+    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, dy, h, dW2, Dout, H, M, true, true, s);            // dW2 = dy^T @ h
+    if (rc != SWIGLU_OK) return rc;
+    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DX, grad_preact, W1, dx, M, D, 2 * H, false, true, s);  // dx = grad_preact @ W1
+    if (rc != SWIGLU_OK) return rc;
+    return run_gemm(st, SWIGLU_KERNEL_BWD_DW1, grad_preact, x, dW1, 2 * H, D, M, true, true, s); // dW1 = grad_preact^T @ x
+}
+
+swiglu_status swiglu_mlp_fused_grad_preact(const void* dy, const void* W2, const void* preact, void* grad_preact,
+                                           void* h, int64_t M, int64_t H, int64_t Dout, void* stream) {
+    if (M < 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (!dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
+        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return SWIGLU_OK;
+    if (!dy || !W2 || !preact || !grad_preact || !h) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(W2) || !aligned16(preact) || !aligned16(grad_preact) || !aligned16(h))
+        return SWIGLU_ERR_MISALIGNED;
+    DeviceState* st;
+    swiglu_status rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    return run_fused_bwd(st, dy, W2, preact, grad_preact, h, M, H, Dout, static_cast<cudaStream_t>(stream));
+}
+
+swiglu_status swiglu_mlp_gemm_bf16(const void* A, const void* B, void* Cp, int64_t M, int64_t N, int64_t K,
+                                   int a_mn_major, int b_mn_major, void* stream) {
+    if (M <= 0 || N <= 0 || K <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (!A || !B || !Cp) return SWIGLU_ERR_INVALID_ARG;
+    const int64_t a_inner = a_mn_major ? M : K;
+    const int64_t b_inner = b_mn_major ? N : K;
+    if (a_inner % 8 || b_inner % 8 || N % 8 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+        K >= (int64_t(1) << 31))
+        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(Cp)) return SWIGLU_ERR_MISALIGNED;
+    DeviceState* st;
+    swiglu_status rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    return run_gemm(st, SWIGLU_KERNEL_GEMM, A, B, Cp, M, N, K, a_mn_major != 0, b_mn_major != 0,
+                    static_cast<cudaStream_t>(stream));
+}
+
+swiglu_status swiglu_mlp_device_status(void* stream) {
+    DeviceState* st;
+    swiglu_status rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, st->err_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return SWIGLU_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(st->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return SWIGLU_ERR_CUDA;
+        return SWIGLU_ERR_TIMEOUT;
+    }
+    return SWIGLU_OK;
+}
+
+const char* swiglu_mlp_strerror(swiglu_status status) {
+    switch (status) {
+        case SWIGLU_OK: return "SWIGLU_OK";
+        case SWIGLU_ERR_INVALID_ARG: return "SWIGLU_ERR_INVALID_ARG: null pointer or invalid size";
+        case SWIGLU_ERR_UNSUPPORTED_SHAPE: return "SWIGLU_ERR_UNSUPPORTED_SHAPE: D, H, Dout must be positive multiples of 8 below 2^31";
+        case SWIGLU_ERR_MISALIGNED: return "SWIGLU_ERR_MISALIGNED: pointers must be 16-byte aligned";
+        case SWIGLU_ERR_WORKSPACE_TOO_SMALL: return "SWIGLU_ERR_WORKSPACE_TOO_SMALL";
+        case SWIGLU_ERR_LAUNCH: return "SWIGLU_ERR_LAUNCH: kernel launch or tensor-map encode failed";
+        case SWIGLU_ERR_TIMEOUT: return "SWIGLU_ERR_TIMEOUT: a device-side wait ran out";
+        case SWIGLU_ERR_CUDA: return "SWIGLU_ERR_CUDA: CUDA runtime error";
+    }
+    return "unknown swiglu_status";
+}
+
+void swiglu_mlp_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void swiglu_mlp_set_debug_flags(int flags) { g_debug_flags.store(flags); }
+
+void swiglu_mlp_trace_begin(void** events, int* kinds, int capacity) {
+    Trace& tr = g_trace;
+    const bool on = events && kinds && capacity > 0;
+    tr.events = on ? reinterpret_cast<cudaEvent_t*>(events) : nullptr;
+    tr.kinds = on ? kinds : nullptr;
+    tr.capacity = on ? capacity : 0;
+    tr.count = 0;
+}
+
+int swiglu_mlp_trace_end(void) {
+    Trace& tr = g_trace;
+    const int n = tr.count;
+    tr = Trace();
+    return n;
+}
+
+int swiglu_mlp_abi_version(void) { return 100; }
+
+}  // extern "C"

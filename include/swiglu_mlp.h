@@ -1,0 +1,171 @@
+/*
+ * swiglu_mlp.h -- C ABI of the GB300 (sm_103a) SwiGLU MLP block.
+ *
+ * The block (notation of the "SwiGLU MLP Drop-H technical report",
+ * lgystoic.github.io/notes/swiglu-mlp-drop-h/, "original math" section):
+ *
+ *   forward   preact = x @ W1^T        x [M,D], W1 [2H,D] with rows [left | gate]
+ *             h      = left * silu(gate)    (left = preact[:, :H], gate = preact[:, H:])
+ *             y      = h @ W2^T        W2 [Dout,H]
+ *   backward  grad_h      = dy @ W2
+ *             grad_preact = [grad_h * silu(gate) | grad_h * left * silu'(gate)]
+ *             dx  = grad_preact @ W1,  dW1 = grad_preact^T @ x,  dW2 = dy^T @ h
+ *
+ * The forward keeps preact (saved for the backward) and drops h after the down
+ * projection (the report's "drop-h" saved-tensor policy).  The backward computes
+ * grad_h = dy @ W2 on the tensor cores and applies the SwiGLU backward in that
+ * GEMM's epilogue, recomputing sigma/silu and h from the saved preact, so grad_h
+ * never reaches HBM (the fused dout-GEMM + SwiGLU-backward segment of the
+ * "SwiGLU MLP forward/backward optimization" note, section 4).
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor is a dense, row-major bf16 array in device memory, given as a
+ *    plain pointer; shapes are given in elements.  The caller owns all memory
+ *    (outputs and workspaces included).  The library allocates nothing, frees
+ *    nothing and never synchronises, except swiglu_mlp_device_status.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) of the current CUDA device; a call returns once it is enqueued.
+ *  - Inputs are never written (the backward is non-inplace: preact and dy keep
+ *    their contents).  Outputs must not alias inputs or each other.
+ *  - Pointers must be 16-byte aligned; D, H and Dout must be positive multiples of
+ *    8 (TMA row strides are multiples of 16 bytes); M may be any value >= 0, and
+ *    M, 2H, D, Dout must stay below 2^31.
+ *  - Errors are returned as a swiglu_status; argument errors are detected before
+ *    anything is enqueued.  A kernel that stops making progress (a bounded device
+ *    wait ran out) records it in a device error word, which
+ *    swiglu_mlp_device_status reads.
+ */
+#ifndef SWIGLU_MLP_H
+#define SWIGLU_MLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SWIGLU_OK = 0,
+    SWIGLU_ERR_INVALID_ARG = 1,        /* null pointer, negative size, aliasing */
+    SWIGLU_ERR_UNSUPPORTED_SHAPE = 2,  /* D, H, Dout not positive multiples of 8, or too large */
+    SWIGLU_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+    SWIGLU_ERR_WORKSPACE_TOO_SMALL = 4,
+    SWIGLU_ERR_LAUNCH = 5,             /* a kernel launch or tensor-map encode failed */
+    SWIGLU_ERR_TIMEOUT = 6,            /* a device-side wait ran out (see swiglu_mlp_device_status) */
+    SWIGLU_ERR_CUDA = 7                /* any other CUDA runtime error */
+} swiglu_status;
+
+/* Bytes of workspace swiglu_mlp_fwd needs: the transient h [M,H] bf16. */
+size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
+
+/* Bytes of workspace swiglu_mlp_bwd needs: h [M,H] and grad_preact [M,2H], bf16,
+ * each starting on a 256-byte boundary. */
+size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
+
+/*
+ * Forward.  Drop-H report, "Forward: save preact, not h".
+ *   x [M,D], W1 [2H,D], W2 [Dout,H]           inputs
+ *   preact [M,2H]                              output, saved for the backward
+ *   y [M,Dout]                                 output
+ *   workspace >= swiglu_mlp_fwd_workspace_size bytes; holds h between the two GEMMs.
+ * Kernels: x @ W1^T with a SwiGLU epilogue that writes preact and
+ * h = bf16(left * bf16(silu(gate))), then y = h @ W2^T.
+ */
+swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2,
+                             void* preact, void* y,
+                             int64_t M, int64_t D, int64_t H, int64_t Dout,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward.  Drop-H report, "Backward: fused h recompute and grad_preact"
+ * (backward formulas), with grad_h fused as in the optimization note, section 4.
+ *   x [M,D], W1 [2H,D], W2 [Dout,H], preact [M,2H] (from the forward), dy [M,Dout]   inputs
+ *   dx [M,D], dW1 [2H,D], dW2 [Dout,H]                                               outputs
+ *   workspace >= swiglu_mlp_bwd_workspace_size bytes; on return (once the stream has
+ *   run) it holds h [M,H] at offset 0 and grad_preact [M,2H] at the next 256-byte
+ *   boundary after h.
+ * Kernels: grad_h = dy @ W2 fused with the SwiGLU backward (writes grad_preact and
+ * h), dW2 = dy^T @ h, dx = grad_preact @ W1, dW1 = grad_preact^T @ x (one merged
+ * [2H,M] @ [M,D] product).  With M = 0, dW1 and dW2 are set to zero.
+ */
+swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2,
+                             const void* preact, const void* dy,
+                             void* dx, void* dW1, void* dW2,
+                             int64_t M, int64_t D, int64_t H, int64_t Dout,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The fused segment alone: grad_h = dy @ W2 (never stored) and the SwiGLU
+ * backward epilogue.  Optimization note, section 4; Drop-H report, fused kernel
+ * pseudo-code.
+ *   dy [M,Dout], W2 [Dout,H], preact [M,2H]   inputs
+ *   grad_preact [M,2H] = [dleft | dgate], h [M,H]   outputs
+ */
+swiglu_status swiglu_mlp_fused_grad_preact(const void* dy, const void* W2, const void* preact,
+                                           void* grad_preact, void* h,
+                                           int64_t M, int64_t H, int64_t Dout, void* stream);
+
+/*
+ * The plain tcgen05 GEMM the block's other products use:
+ *   C [M,N] = A * B^T, bf16 in, fp32 accumulate, bf16 out.
+ *   A is [M,K] row-major when a_mn_major = 0, or [K,M] row-major (A^T stored) when 1.
+ *   B is [N,K] row-major when b_mn_major = 0, or [K,N] row-major when 1.
+ * M, N, K >= 1; the contiguous dimension of each operand and N must be multiples of 8.
+ */
+swiglu_status swiglu_mlp_gemm_bf16(const void* A, const void* B, void* C,
+                                   int64_t M, int64_t N, int64_t K,
+                                   int a_mn_major, int b_mn_major, void* stream);
+
+/*
+ * Synchronises `stream`, then returns SWIGLU_TIMEOUT if any kernel of this
+ * library on the current device gave up a bounded wait since the last call
+ * (and clears that record), SWIGLU_ERR_CUDA if the stream reports a CUDA
+ * error, else SWIGLU_OK.
+ */
+swiglu_status swiglu_mlp_device_status(void* stream);
+
+/* Human-readable name of a status. */
+const char* swiglu_mlp_strerror(swiglu_status status);
+
+/* Limit of every device-side wait, in nanoseconds (default 4e9).  Process-wide. */
+void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook, process-wide, default 0.  Bit 0: the GEMMs' TMA producer issues no
+ * loads, so the consumers' waits run out and the kernel returns with
+ * SWIGLU_ERR_TIMEOUT recorded (used to test the timeout path; no fault). */
+void swiglu_mlp_set_debug_flags(int flags);
+
+/* Kernel kinds reported by the launch trace. */
+typedef enum {
+    SWIGLU_KERNEL_FWD_PREACT = 1,   /* x @ W1^T + SwiGLU forward epilogue */
+    SWIGLU_KERNEL_FWD_DOWN = 2,     /* y = h @ W2^T */
+    SWIGLU_KERNEL_BWD_GRAD_H = 3,   /* dy @ W2 + SwiGLU backward epilogue (the fused segment) */
+    SWIGLU_KERNEL_BWD_DW2 = 4,      /* dW2 = dy^T @ h */
+    SWIGLU_KERNEL_BWD_DX = 5,       /* dx = grad_preact @ W1 */
+    SWIGLU_KERNEL_BWD_DW1 = 6,      /* dW1 = grad_preact^T @ x */
+    SWIGLU_KERNEL_GEMM = 7          /* swiglu_mlp_gemm_bf16 */
+} swiglu_kernel_kind;
+
+/*
+ * Launch trace for timing individual kernels inside a larger call.  After
+ * swiglu_mlp_trace_begin, the i-th kernel this library launches from the calling
+ * thread (i < capacity) is bracketed by cudaEventRecord(events[2i]) and
+ * cudaEventRecord(events[2i+1]) on its stream, and kinds[i] receives its
+ * swiglu_kernel_kind.  `events` holds 2*capacity cudaEvent_t handles created by
+ * the caller with timing enabled; `kinds` holds capacity ints; both stay owned by
+ * the caller and must outlive the trace.  swiglu_mlp_trace_end stops tracing and
+ * returns the number of launches seen (which may exceed capacity; only the first
+ * capacity are recorded).  Tracing adds two event records per launch, nothing else.
+ */
+void swiglu_mlp_trace_begin(void** events, int* kinds, int capacity);
+int swiglu_mlp_trace_end(void);
+
+/* ABI version of this header (major * 100 + minor). */
+int swiglu_mlp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_MLP_H */

@@ -1,0 +1,87 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+
+import pytest
+
+from helpers import ensure_library, header_functions
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_library()
+    from bwd_gemm_epilogue_gb300 import binding
+    return binding.lib()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from bwd_gemm_epilogue_gb300 import binding
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in binding.SIGNATURES, f"binding misses {n}"
+
+
+def test_workspace_sizes():
+    from bwd_gemm_epilogue_gb300 import binding as b
+    M, D, H, Dout = 11136, 3584, 14336, 3584
+    assert b.swiglu_mlp_fwd_workspace_size(M, D, H, Dout) == M * H * 2
+    assert b.swiglu_mlp_bwd_workspace_size(M, D, H, Dout) == M * H * 2 + M * 2 * H * 2
+    assert b.swiglu_mlp_fwd_workspace_size(0, D, H, Dout) == 0
+    # ragged: each buffer starts on a 256-byte boundary
+    assert b.swiglu_mlp_bwd_workspace_size(3, 8, 8, 8) == 256 + 256
+
+
+def test_strerror_and_version():
+    from bwd_gemm_epilogue_gb300 import binding as b
+    for code, name in b.STATUS_NAMES.items():
+        assert b.swiglu_mlp_strerror(code).startswith(name)
+    assert b.swiglu_mlp_abi_version() == 100
+
+
+A16 = 0x10000          # fake, 16-byte aligned "device" addresses: validation never dereferences them
+BIG = 1 << 40
+
+
+def _fwd(lib, x=A16, w1=A16, w2=A16, pre=A16, y=A16, M=128, D=256, H=512, Do=256, ws=A16, wsb=BIG):
+    return lib.swiglu_mlp_fwd(x, w1, w2, pre, y, M, D, H, Do, ws, wsb, None)
+
+
+def _bwd(lib, ptr=A16, M=128, D=256, H=512, Do=256, ws=A16, wsb=BIG, **over):
+    p = dict(x=ptr, w1=ptr, w2=ptr, pre=ptr, dy=ptr, dx=ptr, dw1=ptr, dw2=ptr)
+    p.update(over)
+    return lib.swiglu_mlp_bwd(p["x"], p["w1"], p["w2"], p["pre"], p["dy"], p["dx"], p["dw1"], p["dw2"],
+                              M, D, H, Do, ws, wsb, None)
+
+
+def test_argument_validation_before_launch(lib):
+    INVALID, SHAPE, MISALIGNED, WS = 1, 2, 3, 4
+    assert _fwd(lib, D=100) == SHAPE                 # not a multiple of 8
+    assert _fwd(lib, H=0) == INVALID
+    assert _fwd(lib, Do=-8) == INVALID
+    assert _fwd(lib, M=-1) == INVALID
+    assert _fwd(lib, M=1 << 31) == SHAPE
+    assert _fwd(lib, x=None) == INVALID
+    assert _fwd(lib, y=A16 + 8) == MISALIGNED
+    assert _fwd(lib, wsb=128 * 512 * 2 - 1) == WS
+    assert _fwd(lib, M=0) == 0                       # empty input: nothing to do
+    assert _bwd(lib, H=12) == SHAPE
+    assert _bwd(lib, dw1=None) == INVALID
+    assert _bwd(lib, pre=A16 + 2) == MISALIGNED
+    assert _bwd(lib, wsb=100) == WS
+    assert lib.swiglu_mlp_fused_grad_preact(A16, A16, A16, A16, None, 4, 8, 8, None) == INVALID
+    assert lib.swiglu_mlp_fused_grad_preact(A16, A16, A16, A16, A16, 4, 8, 9, None) == SHAPE
+    assert lib.swiglu_mlp_fused_grad_preact(A16, A16, A16, A16, A16, 0, 8, 8, None) == 0
+    assert lib.swiglu_mlp_gemm_bf16(A16, A16, A16, 0, 8, 8, 0, 0, None) == INVALID
+    assert lib.swiglu_mlp_gemm_bf16(A16, A16, A16, 5, 8, 12, 0, 0, None) == SHAPE   # K-major A needs K % 8
+    assert lib.swiglu_mlp_gemm_bf16(A16, A16, A16, 5, 8, 12, 1, 1, None) == SHAPE   # MN-major A needs M % 8
+    assert lib.swiglu_mlp_gemm_bf16(A16 + 4, A16, A16, 8, 8, 8, 0, 0, None) == MISALIGNED
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from bwd_gemm_epilogue_gb300 import binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="build the CUDA library"):
+        b.lib()

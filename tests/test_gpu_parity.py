@@ -1,0 +1,211 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Small shapes are compared element by element over whole tensors; they span
+several tiles in every dimension and end in ragged tails (M, N and K not
+multiples of the 128/256/64 tiles).  The named workloads at their full sizes
+run in the same launch configuration the benchmark times and are compared on
+sampled rows (row-wise outputs) and sampled hidden columns (weight gradients),
+which the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bwd_gemm_epilogue_gb300 import workloads
+from bwd_gemm_epilogue_gb300.workloads import Shape
+from helpers import ensure_library, parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def b():
+    ensure_library()
+    from bwd_gemm_epilogue_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def dev(t):
+    return t.cuda().contiguous()
+
+
+def ok_status(b):
+    assert b.swiglu_mlp_device_status() == 0
+
+
+# ---------------------------------------------------------------------------- plain GEMM layouts
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True), (True, False)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 264, 200), (16, 520, 1000), (8, 8, 8)])
+def test_gemm_layouts_against_fp64_matmul(b, a_mn, b_mn, M, N, K):
+    g = torch.Generator().manual_seed(M * 7 + N * 3 + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    ref = A.double() @ B.double().T
+    A_in = A.T.contiguous() if a_mn else A
+    B_in = B.T.contiguous() if b_mn else B
+    C = b.swiglu_mlp_gemm_bf16(dev(A_in), dev(B_in), M, N, K, a_mn, b_mn)
+    ok_status(b)
+    parity(C, ref.numpy(), f"C a_mn={a_mn} b_mn={b_mn}")
+
+
+# ---------------------------------------------------------------------------- fused segment
+
+SMALL = [Shape(128, 256, 512, 256), Shape(300, 320, 392, 264), Shape(1, 64, 136, 72), Shape(16, 128, 384, 512)]
+
+
+@pytest.mark.parametrize("s", SMALL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
+def test_fused_grad_preact_matches_oracle(b, s):
+    _, x, W1, W2, dy = workloads.make_block(s, seed=11)
+    preact = workloads.make_preact(s, seed=11, gate_sweep=True)
+    gh, gp_ref, h_ref, _ = oracle.bwd_rows(W1, W2, preact, dy)
+    gp, h = b.swiglu_mlp_fused_grad_preact(dev(dy), dev(W2), dev(preact))
+    ok_status(b)
+    parity(gp[:, : s.H], gp_ref[:, : s.H], "dleft")
+    parity(gp[:, s.H:], gp_ref[:, s.H:], "dgate")
+    parity(h, h_ref, "h")
+
+
+def test_fused_epilogue_saturation_and_zeros(b):
+    # gate spans [-30, 30] plus exact zeros; left has zeros; checks sigma saturation paths
+    s = Shape(256, 64, 256, 128)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=5)
+    g = torch.Generator().manual_seed(9)
+    left = torch.randn(s.M, s.H, generator=g)
+    gate = torch.linspace(-30, 30, s.M * s.H).reshape(s.M, s.H)
+    gate[::7] = 0.0
+    left[:, ::5] = 0.0
+    preact = torch.cat([left, gate], dim=1).to(torch.bfloat16)
+    _, gp_ref, h_ref, _ = oracle.bwd_rows(W1, W2, preact, dy)
+    gp, h = b.swiglu_mlp_fused_grad_preact(dev(dy), dev(W2), dev(preact))
+    ok_status(b)
+    parity(gp, gp_ref, "grad_preact")
+    parity(h, h_ref, "h")
+
+
+# ---------------------------------------------------------------------------- whole block, small
+
+@pytest.mark.parametrize("s", SMALL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
+def test_forward_matches_oracle(b, s):
+    _, x, W1, W2, dy = workloads.make_block(s, seed=3, gate_sweep=True)
+    p_ref, h_ref, y_ref = oracle.fwd(x, W1, W2)
+    preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2))
+    ok_status(b)
+    parity(preact, p_ref, "preact")
+    parity(y, y_ref, "y")
+
+
+@pytest.mark.parametrize("s", SMALL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
+def test_backward_matches_oracle(b, s):
+    _, x, W1, W2, dy = workloads.make_block(s, seed=4)
+    preact = workloads.make_preact(s, seed=4, gate_sweep=True)
+    gh, gp_ref, h_ref, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, preact, dy)
+    ws = torch.empty(b.swiglu_mlp_bwd_workspace_size(s.M, s.D, s.H, s.Dout), dtype=torch.uint8, device="cuda")
+    dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(preact), dev(dy), workspace=ws)
+    ok_status(b)
+    h, gp = b.bwd_workspace_views(ws, s.M, s.H)
+    parity(gp, gp_ref, "grad_preact")
+    parity(h, h_ref, "h")
+    parity(dx, dx_ref, "dx")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
+
+
+def test_tiny_workload_full_chain(b):
+    s, x, W1, W2, dy = workloads.make_block("tiny")
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2)
+    preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2))
+    parity(preact, p_ref, "preact")
+    parity(y, y_ref, "y")
+    # the backward runs on the oracle's preact (never on the GPU's own)
+    pre_in = torch.from_numpy(p_ref).to(torch.bfloat16)
+    _, gp_ref, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre_in, dy)
+    dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(pre_in), dev(dy))
+    ok_status(b)
+    parity(dx, dx_ref, "dx")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
+
+
+def test_empty_batch(b):
+    s = Shape(0, 64, 128, 64)
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    W1 = torch.randn(256, 64).to(torch.bfloat16).cuda()
+    W2 = torch.randn(64, 128).to(torch.bfloat16).cuda()
+    preact, y = b.swiglu_mlp_fwd(x, W1, W2)
+    assert preact.shape == (0, 256) and y.shape == (0, 64)
+    dx, dW1, dW2 = b.swiglu_mlp_bwd(x, W1, W2, preact, torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"),
+                                    dW1=torch.full((256, 64), 7.0, dtype=torch.bfloat16, device="cuda"),
+                                    dW2=torch.full((64, 128), 7.0, dtype=torch.bfloat16, device="cuda"))
+    ok_status(b)
+    assert dW1.abs().max().item() == 0 and dW2.abs().max().item() == 0
+
+
+def test_autograd_wrapper(b):
+    s = Shape(40, 64, 96, 48)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=8)
+    xg, w1g, w2g = (dev(t).requires_grad_(True) for t in (x.reshape(5, 8, 64), W1, W2))
+    y = b.swiglu_mlp(xg, w1g, w2g)
+    y.backward(dev(dy).reshape(5, 8, 48))
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2)
+    parity(y.reshape(40, 48), y_ref, "y")
+    pre_gpu = torch.from_numpy(p_ref).to(torch.bfloat16)
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre_gpu, dy)
+    parity(xg.grad.reshape(40, 64), dx_ref, "dx")
+    parity(w1g.grad, dW1_ref, "dW1")
+    parity(w2g.grad, dW2_ref, "dW2")
+
+
+# ---------------------------------------------------------------------------- full sizes, sampled
+
+def _sample(n, k, seed):
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(n, size=min(k, n), replace=False)
+    return np.unique(np.concatenate([idx, [0, n - 1]]))
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "target"])
+def test_full_size_workloads_sampled(b, name):
+    s, x, W1, W2, dy = workloads.make_block(name)
+    preact_in = workloads.make_preact(s, workloads.CONFIGS[name]["seed"])
+    xd, W1d, W2d, dyd, prd = dev(x), dev(W1), dev(W2), dev(dy), dev(preact_in)
+    preact, y = b.swiglu_mlp_fwd(xd, W1d, W2d)
+    ws = torch.empty(b.swiglu_mlp_bwd_workspace_size(s.M, s.D, s.H, s.Dout), dtype=torch.uint8, device="cuda")
+    dx, dW1, dW2 = b.swiglu_mlp_bwd(xd, W1d, W2d, prd, dyd, workspace=ws)
+    ok_status(b)
+    h, gp = b.bwd_workspace_views(ws, s.M, s.H)
+
+    rows = _sample(s.M, 6, 1)
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2, rows=rows)
+    parity(preact[rows], p_ref, "preact[rows]")
+    parity(y[rows], y_ref, "y[rows]")
+    _, gp_ref, h_ref, dx_ref = oracle.bwd_rows(W1, W2, preact_in, dy, rows=rows)
+    parity(gp[rows], gp_ref, "grad_preact[rows]")
+    parity(h[rows], h_ref, "h[rows]")
+    parity(dx[rows], dx_ref, "dx[rows]")
+    cols = _sample(s.H, 6, 2)
+    dW2c_ref, dW1l_ref, dW1g_ref = oracle.bwd_cols(x, W2, preact_in, dy, cols=cols)
+    parity(dW2[:, cols].T, dW2c_ref, "dW2[:, cols]")
+    parity(dW1[cols], dW1l_ref, "dW1[cols]")
+    parity(dW1[s.H + cols], dW1g_ref, "dW1[H + cols]")
+
+
+# ---------------------------------------------------------------------------- bounded waits
+
+def test_bounded_wait_times_out_and_context_survives(b):
+    A = torch.randn(256, 128).to(torch.bfloat16).cuda()
+    B = torch.randn(256, 128).to(torch.bfloat16).cuda()
+    b.swiglu_mlp_set_wait_timeout_ns(50_000_000)
+    b.swiglu_mlp_set_debug_flags(1)        # producer issues nothing: every consumer wait runs out
+    try:
+        b.swiglu_mlp_gemm_bf16(A, B, 256, 256, 128, False, False)
+        assert b.swiglu_mlp_device_status() == 6      # SWIGLU_ERR_TIMEOUT
+    finally:
+        b.swiglu_mlp_set_debug_flags(0)
+        b.swiglu_mlp_set_wait_timeout_ns(4_000_000_000)
+    assert b.swiglu_mlp_device_status() == 0           # recorded once, then cleared
+    C = b.swiglu_mlp_gemm_bf16(A, B, 256, 256, 128, False, False)
+    ok_status(b)
+    parity(C, (A.double() @ B.double().T).cpu().numpy(), "C after timeout")
