@@ -40,6 +40,7 @@ SIGNATURES = {
     "swiglu_mlp_gemm_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
     "swiglu_mlp_device_status": (_i32, [_vp]),
     "swiglu_mlp_strerror": (ctypes.c_char_p, [_i32]),
+    "swiglu_mlp_last_error_detail": (ctypes.c_char_p, []),
     "swiglu_mlp_set_wait_timeout_ns": (None, [_u64]),
     "swiglu_mlp_set_debug_flags": (None, [_i32]),
     "swiglu_mlp_trace_begin": (None, [_vp, _vp, _i32]),
@@ -51,9 +52,11 @@ KERNEL_KINDS = {1: "fwd_preact", 2: "fwd_down", 3: "bwd_grad_h", 4: "bwd_dW2", 5
 
 
 class SwigluError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.detail = detail
+        msg = f"{where}: {STATUS_NAMES.get(status, status)}"
+        super().__init__(f"{msg} ({detail})" if detail else msg)
 
 
 _lock = threading.Lock()
@@ -80,7 +83,7 @@ def lib() -> ctypes.CDLL:
 
 def _check(status: int, where: str) -> None:
     if status != 0:
-        raise SwigluError(status, where)
+        raise SwigluError(status, where, lib().swiglu_mlp_last_error_detail().decode(errors="replace"))
 
 
 def _ptr(t: torch.Tensor | None):

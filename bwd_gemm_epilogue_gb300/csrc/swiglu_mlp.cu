@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -41,29 +42,45 @@ struct Trace {
 };
 thread_local Trace g_trace;
 
+// Last failure on this thread, for swiglu_mlp_last_error_detail.
+thread_local char g_detail[256];
+
+swiglu_status fail(swiglu_status st, const char* what, cudaError_t err = cudaSuccess) {
+    if (err != cudaSuccess)
+        std::snprintf(g_detail, sizeof g_detail, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+    else
+        std::snprintf(g_detail, sizeof g_detail, "%s", what);
+    return st;
+}
+
 std::mutex g_mutex;
 EncodeTiledFn g_encode = nullptr;
 DeviceState g_dev[kMaxDevices];
 
 swiglu_status get_device_state(DeviceState** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SWIGLU_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_CUDA, "cudaGetDevice", e);
+    // A thread that has not used CUDA yet (an autograd worker, a fresh std::thread) has
+    // no current context, and the tensor-map encoder needs one.  Binding the current
+    // device's primary context is a no-op when it is already current.
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaSetDevice", e);
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_encode) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || fn == nullptr)
-            return SWIGLU_ERR_CUDA;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return fail(SWIGLU_ERR_CUDA, "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", e);
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
     DeviceState& st = g_dev[dev];
     if (!st.ready) {
-        if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return SWIGLU_ERR_CUDA;
-        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_word), g_err_word) != cudaSuccess)
-            return SWIGLU_ERR_CUDA;
+        e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaDeviceGetAttribute", e);
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_word), g_err_word);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaGetSymbolAddress(error word)", e);
         st.ready = true;
     }
     *out = &st;
@@ -118,8 +135,8 @@ swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUte
                      int64_t tiles_n, cudaStream_t stream) {
     auto kern = gemm_kernel<EPI, A_MN, B_MN>;
     constexpr int smem = Cfg<EPI>::SMEM_BYTES;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return SWIGLU_ERR_LAUNCH;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem)", e);
     GemmParams p;
     p.M = (int)M;
     p.N = (int)N;
@@ -147,10 +164,15 @@ swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUte
     const bool traced = slot >= 0 && slot < tr.capacity;
     if (traced) {
         tr.kinds[slot] = kind;
-        if (cudaEventRecord(tr.events[2 * slot], stream) != cudaSuccess) return SWIGLU_ERR_CUDA;
+        e = cudaEventRecord(tr.events[2 * slot], stream);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventRecord(trace)", e);
     }
-    if (cudaLaunchKernelEx(&cfg, kern, a, b, o0, o1, i0, p) != cudaSuccess) return SWIGLU_ERR_LAUNCH;
-    if (traced && cudaEventRecord(tr.events[2 * slot + 1], stream) != cudaSuccess) return SWIGLU_ERR_CUDA;
+    e = cudaLaunchKernelEx(&cfg, kern, a, b, o0, o1, i0, p);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaLaunchKernelEx", e);
+    if (traced) {
+        e = cudaEventRecord(tr.events[2 * slot + 1], stream);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventRecord(trace)", e);
+    }
     return SWIGLU_OK;
 }
 
@@ -164,13 +186,13 @@ size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 swiglu_status run_fwd_preact(DeviceState* st, const void* x, const void* W1, void* preact, void* h,
                              int64_t M, int64_t D, int64_t H, cudaStream_t s) {
     CUtensorMap a, b, o0, o1;
-    if (!encode_operand(&a, x, M, D, false, BM)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_operand(&a, x, M, D, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
     // W1 [2H, D] as (k, j, half): element (k, j, half) = W1[(half*H + j)*D + k]
     if (!encode_3d(&b, W1, (uint64_t)D, (uint64_t)H, 2, (uint64_t)D * 2, (uint64_t)H * D * 2, 64, BN / 2, 1,
                    CU_TENSOR_MAP_SWIZZLE_128B))
-        return SWIGLU_ERR_LAUNCH;
-    if (!encode_paired(&o0, preact, M, H, 32)) return SWIGLU_ERR_LAUNCH;
-    if (!encode_out_2d(&o1, h, M, H)) return SWIGLU_ERR_LAUNCH;
+        return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (W1 slabs)");
+    if (!encode_paired(&o0, preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
+    if (!encode_out_2d(&o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
     return launch<EPI_SWIGLU_FWD, false, false>(st, SWIGLU_KERNEL_FWD_PREACT, a, b, o0, o1, o0, M, H, D, (H + BN / 2 - 1) / (BN / 2), s);
 }
 
@@ -178,11 +200,11 @@ swiglu_status run_fwd_preact(DeviceState* st, const void* x, const void* W1, voi
 swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, const void* preact,
                             void* grad_preact, void* h, int64_t M, int64_t H, int64_t Dout, cudaStream_t s) {
     CUtensorMap a, b, o0, o1, i0;
-    if (!encode_operand(&a, dy, M, Dout, false, BM)) return SWIGLU_ERR_LAUNCH;
-    if (!encode_operand(&b, W2, H, Dout, true, 0)) return SWIGLU_ERR_LAUNCH;   // B(n=j, k=o) = W2[o, j]
-    if (!encode_paired(&o0, grad_preact, M, H, 32)) return SWIGLU_ERR_LAUNCH;
-    if (!encode_out_2d(&o1, h, M, H)) return SWIGLU_ERR_LAUNCH;
-    if (!encode_paired(&i0, preact, M, H, BM)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_operand(&a, dy, M, Dout, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
+    if (!encode_operand(&b, W2, H, Dout, true, 0)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");   // B(n=j, k=o) = W2[o, j]
+    if (!encode_paired(&o0, grad_preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
+    if (!encode_out_2d(&o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
+    if (!encode_paired(&i0, preact, M, H, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
     return launch<EPI_SWIGLU_BWD, false, true>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, b, o0, o1, i0, M, H, Dout, (H + BN - 1) / BN, s);
 }
 
@@ -190,9 +212,9 @@ swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, con
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
                        int64_t K, bool a_mn, bool b_mn, cudaStream_t s) {
     CUtensorMap a, b, o0;
-    if (!encode_operand(&a, A, M, K, a_mn, BM)) return SWIGLU_ERR_LAUNCH;
-    if (!encode_operand(&b, B, N, K, b_mn, BN)) return SWIGLU_ERR_LAUNCH;
-    if (!encode_out_2d(&o0, Cp, M, N)) return SWIGLU_ERR_LAUNCH;
+    if (!encode_operand(&a, A, M, K, a_mn, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
+    if (!encode_operand(&b, B, N, K, b_mn, BN)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
+    if (!encode_out_2d(&o0, Cp, M, N)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
     const int64_t tiles_n = (N + BN - 1) / BN;
     if (!a_mn && !b_mn) return launch<EPI_STORE, false, false>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
     if (!a_mn && b_mn) return launch<EPI_STORE, false, true>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
@@ -253,8 +275,9 @@ swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, cons
     if (!aligned16(W1) || !aligned16(W2) || !aligned16(dW1) || !aligned16(dW2)) return SWIGLU_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 0) {
-        if (cudaMemsetAsync(dW1, 0, (size_t)2 * H * D * 2, s) != cudaSuccess) return SWIGLU_ERR_CUDA;
-        if (cudaMemsetAsync(dW2, 0, (size_t)Dout * H * 2, s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+        cudaError_t e = cudaMemsetAsync(dW1, 0, (size_t)2 * H * D * 2, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, (size_t)Dout * H * 2, s);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync", e);
         return SWIGLU_OK;
     }
     if (!x || !preact || !dy || !dx || !workspace) return SWIGLU_ERR_INVALID_ARG;
@@ -312,13 +335,16 @@ swiglu_status swiglu_mlp_device_status(void* stream) {
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return SWIGLU_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaStreamSynchronize", e);
     int word = 0;
-    if (cudaMemcpy(&word, st->err_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return SWIGLU_ERR_CUDA;
+    e = cudaMemcpy(&word, st->err_word, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemcpy(error word)", e);
     if (word != 0) {
         const int zero = 0;
-        if (cudaMemcpy(st->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
-            return SWIGLU_ERR_CUDA;
+        e = cudaMemcpy(st->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemcpy(error word)", e);
+        std::snprintf(g_detail, sizeof g_detail, "device wait timed out (role bits 0x%x)", word);
         return SWIGLU_ERR_TIMEOUT;
     }
     return SWIGLU_OK;
@@ -337,6 +363,8 @@ const char* swiglu_mlp_strerror(swiglu_status status) {
     }
     return "unknown swiglu_status";
 }
+
+const char* swiglu_mlp_last_error_detail(void) { return g_detail; }
 
 void swiglu_mlp_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 

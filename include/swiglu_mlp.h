@@ -128,6 +128,12 @@ swiglu_status swiglu_mlp_device_status(void* stream);
 /* Human-readable name of a status. */
 const char* swiglu_mlp_strerror(swiglu_status status);
 
+/* Detail of the last failure reported on the calling thread: the CUDA call or
+ * check that failed and the CUDA error name.  Empty before the first failure.
+ * The string is owned by the library and stays valid until the thread's next
+ * failing call. */
+const char* swiglu_mlp_last_error_detail(void);
+
 /* Limit of every device-side wait, in nanoseconds (default 4e9).  Process-wide. */
 void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
 

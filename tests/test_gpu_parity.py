@@ -209,3 +209,25 @@ def test_bounded_wait_times_out_and_context_survives(b):
     C = b.swiglu_mlp_gemm_bf16(A, B, 256, 256, 128, False, False)
     ok_status(b)
     parity(C, (A.double() @ B.double().T).cpu().numpy(), "C after timeout")
+
+
+def test_call_from_worker_thread(b):
+    # autograd runs CUDA backward functions on its own worker thread; the library
+    # must work from any thread.
+    import threading
+    A = torch.randn(256, 128).to(torch.bfloat16).cuda()
+    B = torch.randn(256, 128).to(torch.bfloat16).cuda()
+    out = {}
+
+    def work():
+        try:
+            out["C"] = b.swiglu_mlp_gemm_bf16(A, B, 256, 256, 128, False, False)
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001
+            out["err"] = e
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert "err" not in out, out.get("err")
+    parity(out["C"], (A.double() @ B.double().T).cpu().numpy(), "C from worker thread")
