@@ -36,6 +36,7 @@ SIGNATURES = {
     "swiglu_mlp_bwd_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
     "swiglu_mlp_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "swiglu_mlp_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
     "swiglu_mlp_fused_grad_preact": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "swiglu_mlp_gemm_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
     "swiglu_mlp_device_status": (_i32, [_vp]),
@@ -195,6 +196,22 @@ def swiglu_mlp_fwd(x, W1, W2, preact=None, y=None, workspace=None):
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream(x.device))
     _check(st, "swiglu_mlp_fwd")
+    return preact, y
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def swiglu_mlp_fwd_noalloc(x, W1, W2, preact=None, y=None):
+    """Forward whose transient h lives in the library's built-in 64 MiB device array
+    instead of a caller workspace (for callers that cannot allocate; M*H <= 2^25).
+    Calls share that array: calls that overlap on the GPU race.  Returns (preact, y)."""
+    M, D, H, Dout = _dims(x, W1, W2)
+    preact = _empty((M, 2 * H), x) if preact is None else preact
+    y = _empty((M, Dout), x) if y is None else y
+    st = lib().swiglu_mlp_fwd_noalloc(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), M, D, H, Dout,
+                                      _stream(x.device))
+    _check(st, "swiglu_mlp_fwd_noalloc")
     return preact, y
 
 

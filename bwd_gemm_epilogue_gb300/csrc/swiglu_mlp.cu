@@ -389,3 +389,71 @@ int swiglu_mlp_trace_end(void) {
 int swiglu_mlp_abi_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward.
+//
+// Some callers cannot hand the library a workspace: a plugin whose host
+// framework owns every device allocation and exposes no scratch hook, a
+// real-time loop that must not call cudaMalloc (it can synchronise the device),
+// or a process whose device memory budget is fixed at start-up.  For them the
+// forward's transient h lives in a fixed array in this library's own device
+// memory.  The array exists on every GPU that loads the library, for the life
+// of the process.
+// ---------------------------------------------------------------------------
+namespace swiglu {
+namespace {
+
+__device__ __align__(256) uint8_t g_fwd_scratch[SWIGLU_MLP_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices];
+
+// Device address of g_fwd_scratch on the current device, looked up once per device
+// (the host-side name of the array is not a device address).
+swiglu_status scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_CUDA, "cudaGetDevice", e);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fwd_scratch);
+        if (e != cudaSuccess || !p) return fail(SWIGLU_ERR_CUDA, "cudaGetSymbolAddress(static scratch)", e);
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return SWIGLU_OK;
+}
+
+}  // namespace
+}  // namespace swiglu
+
+extern "C" swiglu_status swiglu_mlp_fwd_noalloc(const void* x, const void* W1, const void* W2, void* preact,
+                                                void* y, int64_t M, int64_t D, int64_t H, int64_t Dout,
+                                                void* stream) {
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
+        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return SWIGLU_OK;
+    if (!x || !W1 || !W2 || !preact || !y) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(preact) || !aligned16(y))
+        return SWIGLU_ERR_MISALIGNED;
+    const size_t need = (size_t)M * (size_t)H * 2;
+    if (need > (size_t)SWIGLU_MLP_NOALLOC_SCRATCH_BYTES) {
+        std::snprintf(g_detail, sizeof g_detail,
+                      "swiglu_mlp_fwd_noalloc: h needs %zu bytes (M*H*2) but the built-in scratch holds %zu",
+                      need, (size_t)SWIGLU_MLP_NOALLOC_SCRATCH_BYTES);
+        return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+    }
+    DeviceState* st;
+    swiglu_status rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    void* h = nullptr;
+    rc = scratch_address(&h);
+    if (rc != SWIGLU_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = run_fwd_preact(st, x, W1, preact, h, M, D, H, s);
+    if (rc != SWIGLU_OK) return rc;
+    return run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h, W2, y, M, Dout, H, false, false, s);
+}

@@ -125,6 +125,28 @@ swiglu_status swiglu_mlp_gemm_bf16(const void* A, const void* B, void* C,
  */
 swiglu_status swiglu_mlp_device_status(void* stream);
 
+/*
+ * Forward without a caller-supplied workspace.  The pages have no counterpart:
+ * this is a convenience for callers that cannot allocate device memory (a plugin
+ * whose host framework owns all device allocations and offers no scratch hook, a
+ * real-time loop that must not call cudaMalloc because it can synchronise the
+ * device, a process whose device memory is fixed at start-up).
+ *   Same inputs, outputs and results as swiglu_mlp_fwd; h [M,H] is kept in a
+ *   fixed array of SWIGLU_MLP_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library's
+ *   device memory, which every GPU that loads the library holds until the process
+ *   exits.  M*H*2 must not exceed that size (M*H <= 33554432), else
+ *   SWIGLU_ERR_WORKSPACE_TOO_SMALL is returned before anything is enqueued.
+ *   The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.  All calls share the one array and each overwrites it, so calls whose
+ *   work can overlap on the GPU (different streams without ordering) race on it.
+ */
+#define SWIGLU_MLP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+swiglu_status swiglu_mlp_fwd_noalloc(const void* x, const void* W1, const void* W2,
+                                     void* preact, void* y,
+                                     int64_t M, int64_t D, int64_t H, int64_t Dout, void* stream);
+
 /* Human-readable name of a status. */
 const char* swiglu_mlp_strerror(swiglu_status status);
 
