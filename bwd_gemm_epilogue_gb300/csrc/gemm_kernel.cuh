@@ -8,13 +8,22 @@
 // rest of the kernel does not.  One CTA per SM, 256 threads:
 //
 //   warp 0      TMA producer: A/B k-blocks into a STAGES-deep shared-memory ring
-//   warp 1      MMA issuer: tcgen05.mma 128x256x16 into one of two TMEM
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma into one of two TMEM
 //               accumulators (2 x 256 fp32 columns = all 512 TMEM columns)
 //   warp 2      epilogue-input producer (SWIGLU_BWD only): TMA-prefetches the
 //               saved preact left/gate sub-tiles the epilogue consumes
 //   warp 3      idle
 //   warps 4..7  epilogue: TMEM -> registers (lane quadrant = warp % 4), the
 //               epilogue math, bf16 tiles staged in shared memory, TMA stores
+//
+// CG = 1: each CTA computes a 128 x 256 output tile with cta_group::1 MMAs.
+// CG = 2: a cluster of two CTAs computes a 256 x 256 tile with cta_group::2 MMAs.
+//         Each CTA loads its own 128 rows of A and its own 128 rows (N) of B, both
+//         CTAs' loads complete on the leader CTA's (rank 0) stage barrier, the
+//         leader issues the 256 x 256 x 16 MMAs and multicasts its commits to both
+//         CTAs, and each CTA drains its own 128 accumulator rows.  Per k-block a CTA
+//         moves 32 KB instead of 48 KB, so the ring holds more stages and L2 serves
+//         a third less.
 //
 // Epilogues:
 //   EPI_STORE       C = acc rounded to bf16.
@@ -47,8 +56,8 @@ namespace swiglu {
 
 enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;           // accumulator rows per CTA
+constexpr int BN = 256;           // accumulator columns
 constexpr int BK = 64;            // one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
 constexpr int NUM_THREADS = 256;
@@ -65,7 +74,8 @@ struct GemmParams {
     int M;            // GEMM rows
     int N;            // EPI_STORE: GEMM columns; SWIGLU epilogues: H
     int K;
-    int tiles_m, tiles_n, num_tiles;
+    int tiles_m;      // tiles of BM * CG rows
+    int tiles_n, num_tiles;
     int band;         // n-tiles per raster band (L2 reuse)
     int k_blocks;
     unsigned long long timeout_ns;
@@ -73,17 +83,19 @@ struct GemmParams {
     int debug_flags;
 };
 
-template <int EPI>
+template <int EPI, int CG>
 struct Cfg {
-    static constexpr int STAGES = (EPI == EPI_STORE) ? 4 : 3;
+    static constexpr int STAGES = CG == 1 ? (EPI == EPI_STORE ? 4 : 3) : (EPI == EPI_STORE ? 6 : EPI == EPI_SWIGLU_FWD ? 5 : 4);
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_ROWS = BN / CG;                        // B rows (N) held by this CTA
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TX_BYTES = STAGE_BYTES * CG;             // what the leader's stage barrier waits for
     static constexpr int NOUT = (EPI == EPI_STORE) ? 1 : 3;
     static constexpr int OUT_TILE = 32 * CHUNK * 2;               // one warp's 32x32 bf16 tile
     static constexpr int OUT_BUFS = 2;
     static constexpr int OUT_WARP_BYTES = OUT_BUFS * NOUT * OUT_TILE;
-    static constexpr int EIN_SLOTS = (EPI == EPI_SWIGLU_BWD) ? 2 : 0;
+    static constexpr int EIN_SLOTS = (EPI == EPI_SWIGLU_BWD) ? (CG == 1 ? 2 : 3) : 0;
     static constexpr int EIN_HALF = BM * CHUNK * 2;               // 128 rows x 32 cols bf16
     static constexpr int EIN_SLOT_BYTES = 2 * EIN_HALF;           // left + gate
     static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CHUNK : BN / CHUNK;
@@ -98,6 +110,7 @@ struct Cfg {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;       // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;           // slack to align the base
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 // ---------------------------------------------------------------------------
@@ -107,7 +120,7 @@ struct Cfg {
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   K-major : rows of 64 bf16 (128 B), 8-row groups 1024 B apart (SBO); LBO unused.
 //   MN-major: 64 MN-contiguous elements per 128-B row, one row per k; 8-k-row groups
-//             1024 B apart (SBO); 64-element MN blocks `mn_block_bytes` apart (LBO).
+//             1024 B apart (SBO); 64-element MN blocks `lbo_bytes` apart (LBO).
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
                                                     uint32_t sbo_bytes) {
     uint64_t d = 0;
@@ -119,15 +132,15 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A/B, fp32 D, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t umma_idesc(bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor, kind::f16: bf16 A/B, fp32 D, M = 128 * CG, N = 256.
+__host__ __device__ constexpr uint32_t umma_idesc(bool a_mn_major, bool b_mn_major, int cg) {
     return (1u << 4)                          // D format f32
            | (1u << 7)                        // A format bf16
            | (1u << 10)                       // B format bf16
            | ((a_mn_major ? 1u : 0u) << 15)   // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
            | ((uint32_t)(BN >> 3) << 17)      // N >> 3
-           | ((uint32_t)(BM >> 4) << 24);     // M >> 4
+           | ((uint32_t)((BM * cg) >> 4) << 24);   // M >> 4
 }
 
 // ---------------------------------------------------------------------------
@@ -147,7 +160,7 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& tm,
 // Bounded wait on an mbarrier phase.  Returns false (after recording `role` in the
 // error word and raising the CTA abort flag) when the limit runs out, or when
 // another role has already aborted.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const GemmParams& p,
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long timeout_ns, int* err,
                                           volatile int* abort_flag, int role) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t start = ptx::globaltimer();
@@ -155,9 +168,9 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const G
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((n & 63) == 0) {
             if (*abort_flag) return false;
-            if (ptx::globaltimer() - start > p.timeout_ns) {
+            if (ptx::globaltimer() - start > timeout_ns) {
                 *abort_flag = 1;
-                atomicOr(p.err, role);
+                atomicOr(err, role);
                 return false;
             }
         }
@@ -169,6 +182,14 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t 
     const uint64_t start = ptx::globaltimer();
     while (!ptx::mbar_try_wait(bar, parity)) {
         if (ptx::globaltimer() - start > limit_ns) return;
+    }
+}
+
+// Spin for `ns` nanoseconds (lets copies already issued land after an abort when
+// their completion barrier lives in the other CTA of the pair).
+__device__ __noinline__ void spin_ns(uint64_t ns) {
+    const uint64_t start = ptx::globaltimer();
+    while (ptx::globaltimer() - start < ns) {
     }
 }
 
@@ -199,12 +220,12 @@ __device__ __forceinline__ uint32_t sw64_offset(int r, int c) {
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                 const __grid_constant__ CUtensorMap tmI0, const GemmParams p) {
-    using C = Cfg<EPI>;
+    using C = Cfg<EPI, CG>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -212,6 +233,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;   // position in the CTA pair
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x / CG;
+    const int num_clusters = gridDim.x / CG;
+    const unsigned long long tmo = p.timeout_ns;
 
     const uint32_t bar0 = base + C::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -231,7 +257,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull_bar(b), 1);
-            ptx::mbar_init(tempty_bar(b), 4);
+            ptx::mbar_init(tempty_bar(b), 4 * CG);   // every epilogue warp of the pair
         }
         for (int s = 0; s < C::EIN_SLOTS; ++s) {
             ptx::mbar_init(ein_full_bar(s), 1);
@@ -247,11 +273,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (EPI == EPI_SWIGLU_BWD) ptx::prefetch_tmap(&tmI0);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32((const void*)tmem_holder), TMEM_COLS);
-        ptx::tmem_relinquish();
+        if (CG == 2) {
+            ptx::tmem_alloc_pair(ptx::smem_u32((const void*)tmem_holder), TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32((const void*)tmem_holder), TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if (CG == 2) ptx::cluster_sync();   // the peer's barriers exist before anything signals them
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -264,37 +296,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            for (int t = cluster; t < p.num_tiles && ok; t += num_clusters) {
                 int tm, tn;
                 tile_coords(p, t, tm, tn);
-                const int m0 = tm * BM;
+                const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, abort_flag, ERR_PRODUCER)) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, p.err, abort_flag, ERR_PRODUCER)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = full_bar(stage);
-                    ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t fb_local = full_bar(stage);
+                    // CG == 2: both CTAs' copies complete on the leader's stage barrier.
+                    const uint32_t fb = CG == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
+                    if (leader) ptx::mbar_arrive_expect_tx(fb_local, C::TX_BYTES);
                     last_parity[stage] = (int)phase;
                     const int k0 = kb * BK;
                     const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
                     const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
+                    auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+                        if (CG == 2) ptx::tma_load_2d_pair(dst, m, fb, c0, c1);
+                        else ptx::tma_load_2d(dst, m, fb, c0, c1);
+                    };
                     if (A_MN) {
-                        ptx::tma_load_2d(sA, &tmA, fb, m0, k0);
-                        ptx::tma_load_2d(sA + 8192, &tmA, fb, m0 + 64, k0);
+                        load2(sA, &tmA, m0, k0);
+                        load2(sA + 8192, &tmA, m0 + 64, k0);
                     } else {
-                        ptx::tma_load_2d(sA, &tmA, fb, k0, m0);
+                        load2(sA, &tmA, k0, m0);
                     }
                     if (EPI == EPI_SWIGLU_FWD) {
+                        // W1 as (k, j, half): CG == 1 loads both slabs, CG == 2 the slab of its rank
                         const int j0 = tn * (BN / 2);
-                        ptx::tma_load_3d(sB, &tmB, fb, k0, j0, 0);
-                        ptx::tma_load_3d(sB + C::B_BYTES / 2, &tmB, fb, k0, j0, 1);
+                        if (CG == 2) {
+                            ptx::tma_load_3d_pair(sB, &tmB, fb, k0, j0, (int)rank);
+                        } else {
+                            ptx::tma_load_3d(sB, &tmB, fb, k0, j0, 0);
+                            ptx::tma_load_3d(sB + C::B_BYTES / 2, &tmB, fb, k0, j0, 1);
+                        }
                     } else if (B_MN) {
-                        const int n0 = tn * BN;
+                        const int n0 = tn * BN + C::B_ROWS * (int)rank;
 #pragma unroll
-                        for (int i = 0; i < BN / 64; ++i) ptx::tma_load_2d(sB + i * 8192, &tmB, fb, n0 + 64 * i, k0);
+                        for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, &tmB, n0 + 64 * i, k0);
                     } else {
-                        ptx::tma_load_2d(sB, &tmB, fb, k0, tn * BN);
+                        load2(sB, &tmB, k0, tn * BN + C::B_ROWS * (int)rank);
                     }
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -304,30 +347,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok) {
                 // Let the loads already issued land before the CTA's shared memory goes away.
-                for (int s = 0; s < C::STAGES; ++s)
-                    if (last_parity[s] >= 0) drain_wait(full_bar(s), (uint32_t)last_parity[s], p.timeout_ns);
+                if (leader) {
+                    for (int s = 0; s < C::STAGES; ++s)
+                        if (last_parity[s] >= 0) drain_wait(full_bar(s), (uint32_t)last_parity[s], tmo);
+                } else {
+                    spin_ns(100000);
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc(A_MN, B_MN);
+        // ------------------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = umma_idesc(A_MN, B_MN, CG);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+            for (int t = cluster; t < p.num_tiles && ok; t += num_clusters, ++local) {
                 const int ab = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
-                if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, p, abort_flag, ERR_MMA)) {
+                if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, tmo, p.err, abort_flag, ERR_MMA)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!wait_bounded(full_bar(stage), phase, p, abort_flag, ERR_MMA)) {
+                    if (!wait_bounded(full_bar(stage), phase, tmo, p.err, abort_flag, ERR_MMA)) {
                         ok = false;
                         break;
                     }
@@ -342,20 +389,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                  : umma_desc_sw128(sA + k * 32, 16, 1024);
                         const uint64_t bd = B_MN ? umma_desc_sw128(sB + k * 2048, 8192, 1024)
                                                  : umma_desc_sw128(sB + k * 32, 16, 1024);
-                        ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        if (CG == 2) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        else ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
-                    ptx::mma_commit(empty_bar(stage));
+                    if (CG == 2) ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
+                    else ptx::mma_commit(empty_bar(stage));
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit(tfull_bar(ab));
+                if (CG == 2) ptx::mma_commit_pair_mc(tfull_bar(ab), 0x3);
+                else ptx::mma_commit(tfull_bar(ab));
             }
             if (!ok) {
-                ptx::mma_commit(drain_bar);
-                drain_wait(drain_bar, 0, p.timeout_ns);
+                if (CG == 2) ptx::mma_commit_pair_mc(drain_bar, 0x1);
+                else ptx::mma_commit(drain_bar);
+                drain_wait(drain_bar, 0, tmo);
             }
         }
         __syncwarp();
@@ -367,13 +418,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
             for (int s = 0; s < C::EIN_SLOTS; ++s) last_parity[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            for (int t = cluster; t < p.num_tiles && ok; t += num_clusters) {
                 int tm, tn;
                 tile_coords(p, t, tm, tn);
-                const int m0 = tm * BM;
+                const int m0 = tm * (BM * CG) + BM * (int)rank;
                 const int j0 = tn * BN;
                 for (int c = 0; c < C::CHUNKS; ++c) {
-                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, p, abort_flag, ERR_AUX)) {
+                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, tmo, p.err, abort_flag, ERR_AUX)) {
                         ok = false;
                         break;
                     }
@@ -391,30 +442,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok) {
                 for (int s = 0; s < C::EIN_SLOTS; ++s)
-                    if (last_parity[s] >= 0) drain_wait(ein_full_bar(s), (uint32_t)last_parity[s], p.timeout_ns);
+                    if (last_parity[s] >= 0) drain_wait(ein_full_bar(s), (uint32_t)last_parity[s], tmo);
             }
         }
         __syncwarp();
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
         const int wq = warp & 3;                 // TMEM lane quadrant = tile rows [32wq, 32wq+32)
-        const int row = 32 * wq + lane;          // row within the tile
+        const int row = 32 * wq + lane;          // row within this CTA's 128 rows
         const uint32_t out_base = base + C::OFF_OUT + wq * C::OUT_WARP_BYTES;
         int ein_slot = 0;
         uint32_t ein_phase = 0;
         int ob = 0;
         int local = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++local) {
+        for (int t = cluster; t < p.num_tiles && ok; t += num_clusters, ++local) {
             int tm, tn;
             tile_coords(p, t, tm, tn);
-            const int m0 = tm * BM;
+            const int m0 = tm * (BM * CG) + BM * (int)rank;
             const int mrow0 = m0 + 32 * wq;     // first output row of this warp's slice
             const bool rows_live = mrow0 < p.M;
             const int ab = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             // every lane observes the barrier itself (acquire), the warp agrees on the outcome
-            const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, p, abort_flag, ERR_EPILOGUE));
+            const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, tmo, p.err, abort_flag,
+                                                                  ERR_EPILOGUE));
             if (!got) {
                 ok = false;
                 break;
@@ -433,17 +485,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::tmem_ld_wait();
                 if (c == C::CHUNKS - 1) {
-                    // Accumulator fully read: hand it back to the MMA warp.
+                    // Accumulator fully read: hand it back to the MMA warp (of the leader CTA).
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(tempty_bar(ab));
+                    if (lane == 0) {
+                        if (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(ab), 0));
+                        else ptx::mbar_arrive(tempty_bar(ab));
+                    }
                 }
 
                 // epilogue inputs (backward): the saved preact left/gate for these 32 columns
                 uint32_t lft[16], gte[16];
                 if (EPI == EPI_SWIGLU_BWD) {
                     const bool in_ok = __all_sync(
-                        0xffffffffu, wait_bounded(ein_full_bar(ein_slot), ein_phase, p, abort_flag, ERR_EPILOGUE));
+                        0xffffffffu, wait_bounded(ein_full_bar(ein_slot), ein_phase, tmo, p.err, abort_flag, ERR_EPILOGUE));
                     if (!in_ok) {
                         ok = false;
                         break;
@@ -548,9 +603,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     __syncthreads();
+    if (CG == 2) ptx::cluster_sync();   // no CTA leaves while its peer may still touch it
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        if (CG == 2) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else ptx::tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

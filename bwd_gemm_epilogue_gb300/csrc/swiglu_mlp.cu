@@ -129,19 +129,28 @@ bool encode_out_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) 
     return encode_2d(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols * 2, CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+// Host-only test hook bit: run every GEMM with single-CTA tiles.
+constexpr int DEBUG_FORCE_SINGLE_CTA = 2;
+
+// CTA-pair tiles (256 rows) pay off once the GEMM has more than one 128-row tile.
+int pick_cg(int64_t M) {
+    if (g_debug_flags.load() & DEBUG_FORCE_SINGLE_CTA) return 1;
+    return M > BM ? 2 : 1;
+}
+
+template <int EPI, bool A_MN, bool B_MN, int CG>
 swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
                      const CUtensorMap& o1, const CUtensorMap& i0, int64_t M, int64_t N, int64_t K,
                      int64_t tiles_n, cudaStream_t stream) {
-    auto kern = gemm_kernel<EPI, A_MN, B_MN>;
-    constexpr int smem = Cfg<EPI>::SMEM_BYTES;
+    auto kern = gemm_kernel<EPI, A_MN, B_MN, CG>;
+    constexpr int smem = Cfg<EPI, CG>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem)", e);
     GemmParams p;
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.tiles_m = (int)((M + BM - 1) / BM);
+    p.tiles_m = (int)((M + BM * CG - 1) / (BM * CG));
     p.tiles_n = (int)tiles_n;
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.band = p.tiles_n < 8 ? p.tiles_n : 8;
@@ -149,16 +158,37 @@ swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUte
     p.timeout_ns = g_timeout_ns.load();
     p.err = st->err_word;
     p.debug_flags = g_debug_flags.load();
-    const int grid = p.num_tiles < st->num_sms ? p.num_tiles : st->num_sms;
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(grid);
+    cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
+    int slots = st->num_sms;   // persistent CTAs (CG == 1) or CTA pairs (CG == 2) that fit at once
+    if (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        static int max_clusters[kMaxDevices];
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (max_clusters[dev] <= 0) {
+            cfg.gridDim = dim3(2 * (st->num_sms / 2));
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess || n <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters", e);
+            max_clusters[dev] = n;
+        }
+        slots = max_clusters[dev];
+    }
+    const int units = p.num_tiles < slots ? p.num_tiles : slots;
+    cfg.gridDim = dim3(units * CG);
     Trace& tr = g_trace;
     const int slot = tr.events ? tr.count++ : -1;
     const bool traced = slot >= 0 && slot < tr.capacity;
@@ -193,7 +223,10 @@ swiglu_status run_fwd_preact(DeviceState* st, const void* x, const void* W1, voi
         return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (W1 slabs)");
     if (!encode_paired(&o0, preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
     if (!encode_out_2d(&o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
-    return launch<EPI_SWIGLU_FWD, false, false>(st, SWIGLU_KERNEL_FWD_PREACT, a, b, o0, o1, o0, M, H, D, (H + BN / 2 - 1) / (BN / 2), s);
+    const int64_t tiles_n = (H + BN / 2 - 1) / (BN / 2);
+    if (pick_cg(M) == 2)
+        return launch<EPI_SWIGLU_FWD, false, false, 2>(st, SWIGLU_KERNEL_FWD_PREACT, a, b, o0, o1, o0, M, H, D, tiles_n, s);
+    return launch<EPI_SWIGLU_FWD, false, false, 1>(st, SWIGLU_KERNEL_FWD_PREACT, a, b, o0, o1, o0, M, H, D, tiles_n, s);
 }
 
 // grad_h = dy @ W2 fused with the SwiGLU backward (writes grad_preact and h).
@@ -205,21 +238,31 @@ swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, con
     if (!encode_paired(&o0, grad_preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
     if (!encode_out_2d(&o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
     if (!encode_paired(&i0, preact, M, H, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
-    return launch<EPI_SWIGLU_BWD, false, true>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, b, o0, o1, i0, M, H, Dout, (H + BN - 1) / BN, s);
+    const int64_t tiles_n = (H + BN - 1) / BN;
+    if (pick_cg(M) == 2)
+        return launch<EPI_SWIGLU_BWD, false, true, 2>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, b, o0, o1, i0, M, H, Dout, tiles_n, s);
+    return launch<EPI_SWIGLU_BWD, false, true, 1>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, b, o0, o1, i0, M, H, Dout, tiles_n, s);
 }
 
 // C [M,N] = A * B^T with either operand K-major or MN-major.
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
                        int64_t K, bool a_mn, bool b_mn, cudaStream_t s) {
+    const int cg = pick_cg(M);
     CUtensorMap a, b, o0;
     if (!encode_operand(&a, A, M, K, a_mn, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
-    if (!encode_operand(&b, B, N, K, b_mn, BN)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
+    if (!encode_operand(&b, B, N, K, b_mn, BN / cg)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
     if (!encode_out_2d(&o0, Cp, M, N)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
     const int64_t tiles_n = (N + BN - 1) / BN;
-    if (!a_mn && !b_mn) return launch<EPI_STORE, false, false>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-    if (!a_mn && b_mn) return launch<EPI_STORE, false, true>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-    if (a_mn && b_mn) return launch<EPI_STORE, true, true>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-    return launch<EPI_STORE, true, false>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    if (cg == 2) {
+        if (!a_mn && !b_mn) return launch<EPI_STORE, false, false, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+        if (!a_mn && b_mn) return launch<EPI_STORE, false, true, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+        if (a_mn && b_mn) return launch<EPI_STORE, true, true, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+        return launch<EPI_STORE, true, false, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    }
+    if (!a_mn && !b_mn) return launch<EPI_STORE, false, false, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    if (!a_mn && b_mn) return launch<EPI_STORE, false, true, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    if (a_mn && b_mn) return launch<EPI_STORE, true, true, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    return launch<EPI_STORE, true, false, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
 }
 
 }  // namespace

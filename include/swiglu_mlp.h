@@ -159,9 +159,11 @@ const char* swiglu_mlp_last_error_detail(void);
 /* Limit of every device-side wait, in nanoseconds (default 4e9).  Process-wide. */
 void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
 
-/* Test hook, process-wide, default 0.  Bit 0: the GEMMs' TMA producer issues no
+/* Test hooks, process-wide, default 0.  Bit 0: the GEMMs' TMA producer issues no
  * loads, so the consumers' waits run out and the kernel returns with
- * SWIGLU_ERR_TIMEOUT recorded (used to test the timeout path; no fault). */
+ * SWIGLU_ERR_TIMEOUT recorded (used to test the timeout path; no fault).
+ * Bit 1: every GEMM uses single-CTA 128-row tiles instead of CTA-pair 256-row
+ * tiles (both paths compute the same result; used to test each). */
 void swiglu_mlp_set_debug_flags(int flags);
 
 /* Kernel kinds reported by the launch trace. */

@@ -35,11 +35,20 @@ def ok_status(b):
     assert b.swiglu_mlp_device_status() == 0
 
 
+@pytest.fixture(params=["pair", "single"])
+def cta_mode(request, b):
+    """Run a test with CTA-pair 256-row tiles (the default for M > 128) and with
+    single-CTA 128-row tiles forced through the test hook."""
+    b.swiglu_mlp_set_debug_flags(2 if request.param == "single" else 0)
+    yield request.param
+    b.swiglu_mlp_set_debug_flags(0)
+
+
 # ---------------------------------------------------------------------------- plain GEMM layouts
 
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True), (True, False)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 264, 200), (16, 520, 1000), (8, 8, 8)])
-def test_gemm_layouts_against_fp64_matmul(b, a_mn, b_mn, M, N, K):
+def test_gemm_layouts_against_fp64_matmul(b, cta_mode, a_mn, b_mn, M, N, K):
     g = torch.Generator().manual_seed(M * 7 + N * 3 + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     B = torch.randn(N, K, generator=g).to(torch.bfloat16)
@@ -53,11 +62,12 @@ def test_gemm_layouts_against_fp64_matmul(b, a_mn, b_mn, M, N, K):
 
 # ---------------------------------------------------------------------------- fused segment
 
-SMALL = [Shape(128, 256, 512, 256), Shape(300, 320, 392, 264), Shape(1, 64, 136, 72), Shape(16, 128, 384, 512)]
+SMALL = [Shape(128, 256, 512, 256), Shape(300, 320, 392, 264), Shape(1, 64, 136, 72), Shape(16, 128, 384, 512),
+         Shape(640, 256, 768, 512)]
 
 
 @pytest.mark.parametrize("s", SMALL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
-def test_fused_grad_preact_matches_oracle(b, s):
+def test_fused_grad_preact_matches_oracle(b, cta_mode, s):
     _, x, W1, W2, dy = workloads.make_block(s, seed=11)
     preact = workloads.make_preact(s, seed=11, gate_sweep=True)
     gh, gp_ref, h_ref, _ = oracle.bwd_rows(W1, W2, preact, dy)
@@ -88,7 +98,7 @@ def test_fused_epilogue_saturation_and_zeros(b):
 # ---------------------------------------------------------------------------- whole block, small
 
 @pytest.mark.parametrize("s", SMALL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
-def test_forward_matches_oracle(b, s):
+def test_forward_matches_oracle(b, cta_mode, s):
     _, x, W1, W2, dy = workloads.make_block(s, seed=3, gate_sweep=True)
     p_ref, h_ref, y_ref = oracle.fwd(x, W1, W2)
     preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2))
@@ -98,7 +108,7 @@ def test_forward_matches_oracle(b, s):
 
 
 @pytest.mark.parametrize("s", SMALL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
-def test_backward_matches_oracle(b, s):
+def test_backward_matches_oracle(b, cta_mode, s):
     _, x, W1, W2, dy = workloads.make_block(s, seed=4)
     preact = workloads.make_preact(s, seed=4, gate_sweep=True)
     gh, gp_ref, h_ref, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, preact, dy)
