@@ -49,7 +49,8 @@ SIGNATURES = {
     "swiglu_mlp_abi_version": (_i32, []),
 }
 
-KERNEL_KINDS = {1: "fwd_preact", 2: "fwd_down", 3: "bwd_grad_h", 4: "bwd_dW2", 5: "bwd_dx", 6: "bwd_dW1", 7: "gemm"}
+KERNEL_KINDS = {1: "fwd_preact", 2: "fwd_down", 3: "bwd_grad_h", 4: "bwd_dW2", 5: "bwd_dx", 6: "bwd_dW1", 7: "gemm",
+                8: "bwd_gemms"}
 
 
 class SwigluError(RuntimeError):

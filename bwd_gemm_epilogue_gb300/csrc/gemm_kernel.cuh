@@ -41,7 +41,7 @@
 // backward of the "SwiGLU MLP forward/backward optimization" note (section 4): the
 // activation gradient stays on chip, sigma/silu are recomputed from the saved preact.
 //
-// Every mbarrier wait is bounded (GemmParams::timeout_ns, on %globaltimer); a wait
+// Every mbarrier wait is bounded (KernelArgs::timeout_ns, on %globaltimer); a wait
 // that runs out records its role in the device error word, raises a CTA-wide abort
 // flag, every role stops issuing, drains what it has in flight (again bounded),
 // and the CTA frees its TMEM and returns.
@@ -49,6 +49,7 @@
 
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -70,18 +71,41 @@ constexpr int ERR_PRODUCER = 1, ERR_MMA = 2, ERR_EPILOGUE = 4, ERR_AUX = 8;
 // Test hook: the producer issues nothing, so the consumers' waits run out.
 constexpr int DEBUG_SKIP_PRODUCER = 1;
 
-struct GemmParams {
+// One GEMM of a launch.  A launch runs one problem, or (EPI_STORE) up to
+// MAX_PROBLEMS independent ones whose tiles share the persistent grid.
+constexpr int MAX_PROBLEMS = 3;
+struct Problem {
     int M;            // GEMM rows
     int N;            // EPI_STORE: GEMM columns; SWIGLU epilogues: H
     int K;
     int tiles_m;      // tiles of BM * CG rows
-    int tiles_n, num_tiles;
+    int tiles_n;
     int band;         // n-tiles per raster band (L2 reuse)
     int k_blocks;
+    int a_mn, b_mn;   // operand major-ness (1 = M- or N-contiguous)
+    int tile_begin;   // index of this problem's first tile in the launch
+};
+
+struct KernelArgs {
+    CUtensorMap a[MAX_PROBLEMS], b[MAX_PROBLEMS], o0[MAX_PROBLEMS];
+    CUtensorMap o1, i0;   // SWIGLU epilogues: h output; preact input (backward)
+    Problem prob[MAX_PROBLEMS];
+    int num_problems;
+    int num_tiles;
     unsigned long long timeout_ns;
     int* err;         // device error word
     int debug_flags;
 };
+
+// A launch with an explicit per-cluster tile list (longest tiles first, balanced on
+// the host): cluster c runs tiles sched[sched_off[c] .. sched_off[c + 1]).
+constexpr int MAX_CLUSTERS = 128;
+constexpr int MAX_SCHED = 12288;
+struct ScheduledArgs : KernelArgs {
+    uint16_t sched_off[MAX_CLUSTERS + 1];
+    uint16_t sched[MAX_SCHED];
+};
+static_assert(sizeof(ScheduledArgs) <= 32764, "kernel parameter block limit");
 
 template <int EPI, int CG>
 struct Cfg {
@@ -147,7 +171,7 @@ __host__ __device__ constexpr uint32_t umma_idesc(bool a_mn_major, bool b_mn_maj
 // helpers
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& tm, int& tn) {
+__device__ __forceinline__ void tile_coords(const Problem& p, int t, int& tm, int& tn) {
     const int band_tiles = p.band * p.tiles_m;
     const int b = t / band_tiles;
     const int r = t - b * band_tiles;
@@ -155,6 +179,31 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& tm,
     const int w = min(p.band, p.tiles_n - n0);
     tm = r / w;
     tn = n0 + (r - tm * w);
+}
+
+// Which problem a launch-wide tile index belongs to.
+__device__ __forceinline__ int problem_of(const KernelArgs& a, int t) {
+    int pi = 0;
+    if (a.num_problems > 1 && t >= a.prob[1].tile_begin) pi = 1;
+    if (a.num_problems > 2 && t >= a.prob[2].tile_begin) pi = 2;
+    return pi;
+}
+
+// The tiles of cluster c: round robin over the launch, or the host's list.
+template <bool SCHED, class Args>
+__device__ __forceinline__ int tiles_first(const Args& a, int c) {
+    if constexpr (SCHED) return a.sched_off[c];
+    else return c;
+}
+template <bool SCHED, class Args>
+__device__ __forceinline__ int tiles_end(const Args& a, int c) {
+    if constexpr (SCHED) return a.sched_off[c + 1];
+    else return a.num_tiles;
+}
+template <bool SCHED, class Args>
+__device__ __forceinline__ int tile_at(const Args& a, int i) {
+    if constexpr (SCHED) return a.sched[i];
+    else return i;
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (after recording `role` in the
@@ -220,11 +269,12 @@ __device__ __forceinline__ uint32_t sw64_offset(int r, int c) {
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int EPI, bool A_MN, bool B_MN, int CG>
+template <int EPI, int CG, bool SCHED>
+using ArgsOf = typename std::conditional<SCHED, ScheduledArgs, KernelArgs>::type;
+
+template <int EPI, int CG, bool SCHED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
-                const __grid_constant__ CUtensorMap tmI0, const GemmParams p) {
+    gemm_kernel(const __grid_constant__ ArgsOf<EPI, CG, SCHED> args) {
     using C = Cfg<EPI, CG>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -237,7 +287,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool leader = rank == 0;
     const int cluster = blockIdx.x / CG;
     const int num_clusters = gridDim.x / CG;
-    const unsigned long long tmo = p.timeout_ns;
+    const unsigned long long tmo = args.timeout_ns;
+    int* const err = args.err;
+    const int t_first = tiles_first<SCHED>(args, cluster);
+    const int t_end = tiles_end<SCHED>(args, cluster);
+    const int t_step = SCHED ? 1 : num_clusters;
 
     const uint32_t bar0 = base + C::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -266,11 +320,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
-        ptx::prefetch_tmap(&tmA);
-        ptx::prefetch_tmap(&tmB);
-        ptx::prefetch_tmap(&tmO0);
-        if (EPI != EPI_STORE) ptx::prefetch_tmap(&tmO1);
-        if (EPI == EPI_SWIGLU_BWD) ptx::prefetch_tmap(&tmI0);
+        for (int q = 0; q < args.num_problems; ++q) {
+            ptx::prefetch_tmap(&args.a[q]);
+            ptx::prefetch_tmap(&args.b[q]);
+            ptx::prefetch_tmap(&args.o0[q]);
+        }
+        if (EPI != EPI_STORE) ptx::prefetch_tmap(&args.o1);
+        if (EPI == EPI_SWIGLU_BWD) ptx::prefetch_tmap(&args.i0);
     }
     if (warp == 1) {
         if (CG == 2) {
@@ -289,19 +345,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && !(p.debug_flags & DEBUG_SKIP_PRODUCER)) {
+        if (lane == 0 && !(args.debug_flags & DEBUG_SKIP_PRODUCER)) {
             int stage = 0;
             uint32_t phase = 0;
             int last_parity[C::STAGES];
 #pragma unroll
             for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
             bool ok = true;
-            for (int t = cluster; t < p.num_tiles && ok; t += num_clusters) {
+            for (int it = t_first; it < t_end && ok; it += t_step) {
+                const int t = tile_at<SCHED>(args, it);
+                const int pi = problem_of(args, t);
+                const CUtensorMap* mA = &args.a[pi];
+                const CUtensorMap* mB = &args.b[pi];
+                // per-tile fields in registers: the asm statements below clobber memory
+                const Problem pr = args.prob[pi];
+                const int k_blocks = pr.k_blocks;
+                const bool a_mn = pr.a_mn != 0, b_mn = pr.b_mn != 0;
                 int tm, tn;
-                tile_coords(p, t, tm, tn);
+                tile_coords(pr, t - pr.tile_begin, tm, tn);
                 const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, p.err, abort_flag, ERR_PRODUCER)) {
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
                         ok = false;
                         break;
                     }
@@ -317,27 +381,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (CG == 2) ptx::tma_load_2d_pair(dst, m, fb, c0, c1);
                         else ptx::tma_load_2d(dst, m, fb, c0, c1);
                     };
-                    if (A_MN) {
-                        load2(sA, &tmA, m0, k0);
-                        load2(sA + 8192, &tmA, m0 + 64, k0);
+                    if (a_mn) {
+                        load2(sA, mA, m0, k0);
+                        load2(sA + 8192, mA, m0 + 64, k0);
                     } else {
-                        load2(sA, &tmA, k0, m0);
+                        load2(sA, mA, k0, m0);
                     }
                     if (EPI == EPI_SWIGLU_FWD) {
                         // W1 as (k, j, half): CG == 1 loads both slabs, CG == 2 the slab of its rank
                         const int j0 = tn * (BN / 2);
                         if (CG == 2) {
-                            ptx::tma_load_3d_pair(sB, &tmB, fb, k0, j0, (int)rank);
+                            ptx::tma_load_3d_pair(sB, mB, fb, k0, j0, (int)rank);
                         } else {
-                            ptx::tma_load_3d(sB, &tmB, fb, k0, j0, 0);
-                            ptx::tma_load_3d(sB + C::B_BYTES / 2, &tmB, fb, k0, j0, 1);
+                            ptx::tma_load_3d(sB, mB, fb, k0, j0, 0);
+                            ptx::tma_load_3d(sB + C::B_BYTES / 2, mB, fb, k0, j0, 1);
                         }
-                    } else if (B_MN) {
+                    } else if (b_mn) {
                         const int n0 = tn * BN + C::B_ROWS * (int)rank;
 #pragma unroll
-                        for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, &tmB, n0 + 64 * i, k0);
+                        for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mB, n0 + 64 * i, k0);
                     } else {
-                        load2(sB, &tmB, k0, tn * BN + C::B_ROWS * (int)rank);
+                        load2(sB, mB, k0, tn * BN + C::B_ROWS * (int)rank);
                     }
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -359,22 +423,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader CTA)
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc = umma_idesc(A_MN, B_MN, CG);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int t = cluster; t < p.num_tiles && ok; t += num_clusters, ++local) {
+            for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
+                const int pi = problem_of(args, tile_at<SCHED>(args, it));
+                const int k_blocks = args.prob[pi].k_blocks;
+                const bool a_mn = args.prob[pi].a_mn != 0, b_mn = args.prob[pi].b_mn != 0;
+                const uint32_t idesc = umma_idesc(a_mn, b_mn, CG);
                 const int ab = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
-                if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, tmo, p.err, abort_flag, ERR_MMA)) {
+                if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, tmo, err, abort_flag, ERR_MMA)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!wait_bounded(full_bar(stage), phase, tmo, p.err, abort_flag, ERR_MMA)) {
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, tmo, err, abort_flag, ERR_MMA)) {
                         ok = false;
                         break;
                     }
@@ -385,9 +452,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         // K-major: the next 16 k sit 32 bytes further along each 128-B row.
                         // MN-major: the next 16 k are the next 16 rows of 128 B.
-                        const uint64_t ad = A_MN ? umma_desc_sw128(sA + k * 2048, 8192, 1024)
+                        const uint64_t ad = a_mn ? umma_desc_sw128(sA + k * 2048, 8192, 1024)
                                                  : umma_desc_sw128(sA + k * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? umma_desc_sw128(sB + k * 2048, 8192, 1024)
+                        const uint64_t bd = b_mn ? umma_desc_sw128(sB + k * 2048, 8192, 1024)
                                                  : umma_desc_sw128(sB + k * 32, 16, 1024);
                         if (CG == 2) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         else ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
@@ -418,13 +485,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
             for (int s = 0; s < C::EIN_SLOTS; ++s) last_parity[s] = -1;
             bool ok = true;
-            for (int t = cluster; t < p.num_tiles && ok; t += num_clusters) {
+            for (int it = t_first; it < t_end && ok; it += t_step) {
+                const int t = tile_at<SCHED>(args, it);
                 int tm, tn;
-                tile_coords(p, t, tm, tn);
+                const Problem pr0 = args.prob[0];
+                tile_coords(pr0, t, tm, tn);
                 const int m0 = tm * (BM * CG) + BM * (int)rank;
                 const int j0 = tn * BN;
                 for (int c = 0; c < C::CHUNKS; ++c) {
-                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, tmo, p.err, abort_flag, ERR_AUX)) {
+                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, tmo, err, abort_flag, ERR_AUX)) {
                         ok = false;
                         break;
                     }
@@ -432,8 +501,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
                     last_parity[slot] = (int)phase;
                     const uint32_t dst = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
-                    ptx::tma_load_3d(dst, &tmI0, fb, j0 + c * CHUNK, 0, m0);
-                    ptx::tma_load_3d(dst + C::EIN_HALF, &tmI0, fb, j0 + c * CHUNK, 1, m0);
+                    ptx::tma_load_3d(dst, &args.i0, fb, j0 + c * CHUNK, 0, m0);
+                    ptx::tma_load_3d(dst + C::EIN_HALF, &args.i0, fb, j0 + c * CHUNK, 1, m0);
                     if (++slot == C::EIN_SLOTS) {
                         slot = 0;
                         phase ^= 1u;
@@ -456,16 +525,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int ob = 0;
         int local = 0;
         bool ok = true;
-        for (int t = cluster; t < p.num_tiles && ok; t += num_clusters, ++local) {
+        for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
+            const int t = tile_at<SCHED>(args, it);
+            const int pi = problem_of(args, t);
+            const Problem pr = args.prob[pi];   // registers (asm statements clobber memory)
+            const int n_limit = pr.N;
+            const CUtensorMap* mO0 = &args.o0[pi];
             int tm, tn;
-            tile_coords(p, t, tm, tn);
+            tile_coords(pr, t - pr.tile_begin, tm, tn);
             const int m0 = tm * (BM * CG) + BM * (int)rank;
             const int mrow0 = m0 + 32 * wq;     // first output row of this warp's slice
-            const bool rows_live = mrow0 < p.M;
+            const bool rows_live = mrow0 < pr.M;
             const int ab = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             // every lane observes the barrier itself (acquire), the warp agrees on the outcome
-            const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, tmo, p.err, abort_flag,
+            const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, tmo, err, abort_flag,
                                                                   ERR_EPILOGUE));
             if (!got) {
                 ok = false;
@@ -498,7 +572,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint32_t lft[16], gte[16];
                 if (EPI == EPI_SWIGLU_BWD) {
                     const bool in_ok = __all_sync(
-                        0xffffffffu, wait_bounded(ein_full_bar(ein_slot), ein_phase, tmo, p.err, abort_flag, ERR_EPILOGUE));
+                        0xffffffffu, wait_bounded(ein_full_bar(ein_slot), ein_phase, tmo, err, abort_flag, ERR_EPILOGUE));
                     if (!in_ok) {
                         ok = false;
                         break;
@@ -582,14 +656,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0 && rows_live) {
                     if (EPI == EPI_STORE) {
                         const int n = tn * BN + c * CHUNK;
-                        if (n < p.N) ptx::tma_store_2d(&tmO0, ob_base, n, mrow0);
+                        if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
                     } else {
                         const int jw = (EPI == EPI_SWIGLU_FWD) ? BN / 2 : BN;
                         const int j = tn * jw + c * CHUNK;
-                        if (j < p.N) {
-                            ptx::tma_store_3d(&tmO0, ob_base, j, 0, mrow0);
-                            ptx::tma_store_3d(&tmO0, ob_base + C::OUT_TILE, j, 1, mrow0);
-                            ptx::tma_store_2d(&tmO1, ob_base + 2 * C::OUT_TILE, j, mrow0);
+                        if (j < n_limit) {
+                            ptx::tma_store_3d(mO0, ob_base, j, 0, mrow0);
+                            ptx::tma_store_3d(mO0, ob_base + C::OUT_TILE, j, 1, mrow0);
+                            ptx::tma_store_2d(&args.o1, ob_base + 2 * C::OUT_TILE, j, mrow0);
                         }
                     }
                 }

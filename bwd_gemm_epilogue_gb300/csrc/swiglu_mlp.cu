@@ -4,7 +4,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -138,26 +143,73 @@ int pick_cg(int64_t M) {
     return M > BM ? 2 : 1;
 }
 
-template <int EPI, bool A_MN, bool B_MN, int CG>
-swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o0,
-                     const CUtensorMap& o1, const CUtensorMap& i0, int64_t M, int64_t N, int64_t K,
-                     int64_t tiles_n, cudaStream_t stream) {
-    auto kern = gemm_kernel<EPI, A_MN, B_MN, CG>;
-    constexpr int smem = Cfg<EPI, CG>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem)", e);
-    GemmParams p;
+// Host-only test hook bit: the backward's dW2, dx and dW1 run as three launches.
+constexpr int DEBUG_UNGROUPED = 4;
+
+Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn, bool b_mn, int cg) {
+    Problem p;
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.tiles_m = (int)((M + BM * CG - 1) / (BM * CG));
+    p.tiles_m = (int)((M + BM * cg - 1) / (BM * cg));
     p.tiles_n = (int)tiles_n;
-    p.num_tiles = p.tiles_m * p.tiles_n;
     p.band = p.tiles_n < 8 ? p.tiles_n : 8;
     p.k_blocks = (int)((K + BK - 1) / BK);
-    p.timeout_ns = g_timeout_ns.load();
-    p.err = st->err_word;
-    p.debug_flags = g_debug_flags.load();
+    p.a_mn = a_mn ? 1 : 0;
+    p.b_mn = b_mn ? 1 : 0;
+    p.tile_begin = 0;
+    return p;
+}
+
+// Longest-processing-time assignment of the launch's tiles to `units` clusters:
+// tiles in order of decreasing k-blocks (stable within a problem), each to the
+// least-loaded cluster.  Returns false if the lists do not fit the parameter block.
+bool build_schedule(ScheduledArgs& a, int units) {
+    if (units > MAX_CLUSTERS || a.num_tiles > MAX_SCHED || a.num_tiles > 65535) return false;
+    int order[MAX_PROBLEMS];
+    for (int q = 0; q < a.num_problems; ++q) order[q] = q;
+    std::stable_sort(order, order + a.num_problems,
+                     [&](int x, int y) { return a.prob[x].k_blocks > a.prob[y].k_blocks; });
+    std::vector<std::vector<uint16_t>> lists(units);
+    using Slot = std::pair<long long, int>;   // (load, cluster)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int u = 0; u < units; ++u) heap.push({0, u});
+    for (int oi = 0; oi < a.num_problems; ++oi) {
+        const Problem& p = a.prob[order[oi]];
+        const int n = p.tiles_m * p.tiles_n;
+        for (int t = 0; t < n; ++t) {
+            Slot s = heap.top();
+            heap.pop();
+            lists[s.second].push_back((uint16_t)(p.tile_begin + t));
+            heap.push({s.first + p.k_blocks, s.second});
+        }
+    }
+    int off = 0;
+    for (int u = 0; u < units; ++u) {
+        a.sched_off[u] = (uint16_t)off;
+        for (uint16_t t : lists[u]) a.sched[off++] = t;
+    }
+    a.sched_off[units] = (uint16_t)off;
+    return true;
+}
+
+// Launch one persistent grid over args' problems.  args' tensor maps and problems
+// are filled in by the caller; this sets the common fields and the grid.
+template <int EPI, int CG, bool SCHED>
+swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cudaStream_t stream) {
+    auto kern = gemm_kernel<EPI, CG, SCHED>;
+    constexpr int smem = Cfg<EPI, CG>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem)", e);
+    int tiles = 0;
+    for (int q = 0; q < args.num_problems; ++q) {
+        args.prob[q].tile_begin = tiles;
+        tiles += args.prob[q].tiles_m * args.prob[q].tiles_n;
+    }
+    args.num_tiles = tiles;
+    args.timeout_ns = g_timeout_ns.load();
+    args.err = st->err_word;
+    args.debug_flags = g_debug_flags.load();
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -187,7 +239,10 @@ swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUte
         }
         slots = max_clusters[dev];
     }
-    const int units = p.num_tiles < slots ? p.num_tiles : slots;
+    const int units = tiles < slots ? tiles : slots;
+    if constexpr (SCHED) {
+        if (!build_schedule(args, units)) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "tile schedule too large");
+    }
     cfg.gridDim = dim3(units * CG);
     Trace& tr = g_trace;
     const int slot = tr.events ? tr.count++ : -1;
@@ -197,7 +252,7 @@ swiglu_status launch(DeviceState* st, int kind, const CUtensorMap& a, const CUte
         e = cudaEventRecord(tr.events[2 * slot], stream);
         if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventRecord(trace)", e);
     }
-    e = cudaLaunchKernelEx(&cfg, kern, a, b, o0, o1, i0, p);
+    e = cudaLaunchKernelEx(&cfg, kern, args);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaLaunchKernelEx", e);
     if (traced) {
         e = cudaEventRecord(tr.events[2 * slot + 1], stream);
@@ -215,54 +270,79 @@ size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 // preact = x @ W1^T with the SwiGLU forward epilogue (writes preact and h).
 swiglu_status run_fwd_preact(DeviceState* st, const void* x, const void* W1, void* preact, void* h,
                              int64_t M, int64_t D, int64_t H, cudaStream_t s) {
-    CUtensorMap a, b, o0, o1;
-    if (!encode_operand(&a, x, M, D, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
+    const int cg = pick_cg(M);
+    KernelArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (!encode_operand(&a.a[0], x, M, D, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
     // W1 [2H, D] as (k, j, half): element (k, j, half) = W1[(half*H + j)*D + k]
-    if (!encode_3d(&b, W1, (uint64_t)D, (uint64_t)H, 2, (uint64_t)D * 2, (uint64_t)H * D * 2, 64, BN / 2, 1,
+    if (!encode_3d(&a.b[0], W1, (uint64_t)D, (uint64_t)H, 2, (uint64_t)D * 2, (uint64_t)H * D * 2, 64, BN / 2, 1,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (W1 slabs)");
-    if (!encode_paired(&o0, preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
-    if (!encode_out_2d(&o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
-    const int64_t tiles_n = (H + BN / 2 - 1) / (BN / 2);
-    if (pick_cg(M) == 2)
-        return launch<EPI_SWIGLU_FWD, false, false, 2>(st, SWIGLU_KERNEL_FWD_PREACT, a, b, o0, o1, o0, M, H, D, tiles_n, s);
-    return launch<EPI_SWIGLU_FWD, false, false, 1>(st, SWIGLU_KERNEL_FWD_PREACT, a, b, o0, o1, o0, M, H, D, tiles_n, s);
+    if (!encode_paired(&a.o0[0], preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
+    if (!encode_out_2d(&a.o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
+    a.num_problems = 1;
+    a.prob[0] = make_problem(M, H, D, (H + BN / 2 - 1) / (BN / 2), false, false, cg);
+    if (cg == 2) return launch<EPI_SWIGLU_FWD, 2, false>(st, SWIGLU_KERNEL_FWD_PREACT, a, s);
+    return launch<EPI_SWIGLU_FWD, 1, false>(st, SWIGLU_KERNEL_FWD_PREACT, a, s);
 }
 
 // grad_h = dy @ W2 fused with the SwiGLU backward (writes grad_preact and h).
 swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, const void* preact,
                             void* grad_preact, void* h, int64_t M, int64_t H, int64_t Dout, cudaStream_t s) {
-    CUtensorMap a, b, o0, o1, i0;
-    if (!encode_operand(&a, dy, M, Dout, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
-    if (!encode_operand(&b, W2, H, Dout, true, 0)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");   // B(n=j, k=o) = W2[o, j]
-    if (!encode_paired(&o0, grad_preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
-    if (!encode_out_2d(&o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
-    if (!encode_paired(&i0, preact, M, H, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
-    const int64_t tiles_n = (H + BN - 1) / BN;
-    if (pick_cg(M) == 2)
-        return launch<EPI_SWIGLU_BWD, false, true, 2>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, b, o0, o1, i0, M, H, Dout, tiles_n, s);
-    return launch<EPI_SWIGLU_BWD, false, true, 1>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, b, o0, o1, i0, M, H, Dout, tiles_n, s);
+    const int cg = pick_cg(M);
+    KernelArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (!encode_operand(&a.a[0], dy, M, Dout, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
+    // B(n = j, k = o) = W2[o, j]: MN-major
+    if (!encode_operand(&a.b[0], W2, H, Dout, true, 0)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
+    if (!encode_paired(&a.o0[0], grad_preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
+    if (!encode_out_2d(&a.o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
+    if (!encode_paired(&a.i0, preact, M, H, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
+    a.num_problems = 1;
+    a.prob[0] = make_problem(M, H, Dout, (H + BN - 1) / BN, false, true, cg);
+    if (cg == 2) return launch<EPI_SWIGLU_BWD, 2, false>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
+    return launch<EPI_SWIGLU_BWD, 1, false>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
 }
 
-// C [M,N] = A * B^T with either operand K-major or MN-major.
+struct GemmSpec {
+    const void* A;
+    const void* B;
+    void* C;
+    int64_t M, N, K;
+    bool a_mn, b_mn;
+};
+
+// Fill problem q of `a`: C [M,N] = A * B^T with either operand K-major or MN-major.
+bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg) {
+    if (!encode_operand(&a.a[q], g.A, g.M, g.K, g.a_mn, BM)) return false;
+    if (!encode_operand(&a.b[q], g.B, g.N, g.K, g.b_mn, BN / cg)) return false;
+    if (!encode_out_2d(&a.o0[q], g.C, g.M, g.N)) return false;
+    a.prob[q] = make_problem(g.M, g.N, g.K, (g.N + BN - 1) / BN, g.a_mn, g.b_mn, cg);
+    return true;
+}
+
+// One plain GEMM.
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
                        int64_t K, bool a_mn, bool b_mn, cudaStream_t s) {
     const int cg = pick_cg(M);
-    CUtensorMap a, b, o0;
-    if (!encode_operand(&a, A, M, K, a_mn, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
-    if (!encode_operand(&b, B, N, K, b_mn, BN / cg)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
-    if (!encode_out_2d(&o0, Cp, M, N)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
-    const int64_t tiles_n = (N + BN - 1) / BN;
-    if (cg == 2) {
-        if (!a_mn && !b_mn) return launch<EPI_STORE, false, false, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-        if (!a_mn && b_mn) return launch<EPI_STORE, false, true, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-        if (a_mn && b_mn) return launch<EPI_STORE, true, true, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-        return launch<EPI_STORE, true, false, 2>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-    }
-    if (!a_mn && !b_mn) return launch<EPI_STORE, false, false, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-    if (!a_mn && b_mn) return launch<EPI_STORE, false, true, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-    if (a_mn && b_mn) return launch<EPI_STORE, true, true, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
-    return launch<EPI_STORE, true, false, 1>(st, kind, a, b, o0, o0, o0, M, N, K, tiles_n, s);
+    KernelArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (!add_problem(a, 0, GemmSpec{A, B, Cp, M, N, K, a_mn, b_mn}, cg))
+        return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
+    a.num_problems = 1;
+    if (cg == 2) return launch<EPI_STORE, 2, false>(st, kind, a, s);
+    return launch<EPI_STORE, 1, false>(st, kind, a, s);
+}
+
+// Several independent plain GEMMs in one persistent launch, tiles balanced across
+// the CTA pairs by the host schedule (CTA-pair tiles; all M > 128).
+swiglu_status run_gemm_group(DeviceState* st, int kind, const GemmSpec* g, int n, cudaStream_t s) {
+    static thread_local ScheduledArgs a;   // ~26 KB: not on the stack
+    std::memset(static_cast<KernelArgs*>(&a), 0, sizeof(KernelArgs));
+    for (int q = 0; q < n; ++q)
+        if (!add_problem(a, q, g[q], 2)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (group)");
+    a.num_problems = n;
+    return launch<EPI_STORE, 2, true>(st, kind, a, s);
 }
 
 }  // namespace
@@ -334,11 +414,21 @@ swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, cons
     void* grad_preact = static_cast<uint8_t*>(workspace) + round256((size_t)M * (size_t)H * 2);
     rc = run_fused_bwd(st, dy, W2, preact, grad_preact, h, M, H, Dout, s);
     if (rc != SWIGLU_OK) return rc;
-    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, dy, h, dW2, Dout, H, M, true, true, s);            // dW2 = dy^T @ h
+    const GemmSpec g[3] = {
+        {dy, h, dW2, Dout, H, M, true, true},                 // dW2 = dy^T @ h
+        {grad_preact, W1, dx, M, D, 2 * H, false, true},      // dx = grad_preact @ W1
+        {grad_preact, x, dW1, 2 * H, D, M, true, true},       // dW1 = grad_preact^T @ x (merged)
+    };
+    int64_t pair_tiles = 0;   // tiles of the grouped launch (256-row CTA-pair tiles)
+    for (const GemmSpec& q : g) pair_tiles += ((q.M + 2 * BM - 1) / (2 * BM)) * ((q.N + BN - 1) / BN);
+    const bool grouped = !(g_debug_flags.load() & (DEBUG_UNGROUPED | DEBUG_FORCE_SINGLE_CTA)) && Dout > BM &&
+                         M > BM && 2 * H > BM && pair_tiles <= MAX_SCHED;
+    if (grouped) return run_gemm_group(st, SWIGLU_KERNEL_BWD_GEMMS, g, 3, s);
+    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, g[0].A, g[0].B, g[0].C, g[0].M, g[0].N, g[0].K, true, true, s);
     if (rc != SWIGLU_OK) return rc;
-    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DX, grad_preact, W1, dx, M, D, 2 * H, false, true, s);  // dx = grad_preact @ W1
+    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DX, g[1].A, g[1].B, g[1].C, g[1].M, g[1].N, g[1].K, false, true, s);
     if (rc != SWIGLU_OK) return rc;
-    return run_gemm(st, SWIGLU_KERNEL_BWD_DW1, grad_preact, x, dW1, 2 * H, D, M, true, true, s); // dW1 = grad_preact^T @ x
+    return run_gemm(st, SWIGLU_KERNEL_BWD_DW1, g[2].A, g[2].B, g[2].C, g[2].M, g[2].N, g[2].K, true, true, s);
 }
 
 swiglu_status swiglu_mlp_fused_grad_preact(const void* dy, const void* W2, const void* preact, void* grad_preact,

@@ -22,6 +22,7 @@ def gemm_flops(M: int, D: int, H: int, Dout: int) -> dict:
         "bwd_dx": 2 * M * 2 * H * D,       # grad_preact @ W1
         "bwd_dW1": 2 * 2 * H * M * D,      # grad_preact^T @ x, one merged product
     }
+    f["bwd_gemms"] = f["bwd_dW2"] + f["bwd_dx"] + f["bwd_dW1"]   # the grouped launch
     f["fwd"] = f["fwd_preact"] + f["fwd_down"]
     f["bwd"] = f["bwd_grad_h"] + f["bwd_dW2"] + f["bwd_dx"] + f["bwd_dW1"]
     f["step"] = f["fwd"] + f["bwd"]
@@ -31,7 +32,7 @@ def gemm_flops(M: int, D: int, H: int, Dout: int) -> dict:
 def kernel_bytes(M: int, D: int, H: int, Dout: int) -> dict:
     """Compulsory HBM bytes per launch of each kernel."""
     b = BF16
-    return {
+    k = {
         # x, W1 in; preact [M,2H] and h [M,H] out
         "fwd_preact": b * (M * D + 2 * H * D + 2 * M * H + M * H),
         # h, W2 in; y out
@@ -42,3 +43,5 @@ def kernel_bytes(M: int, D: int, H: int, Dout: int) -> dict:
         "bwd_dx": b * (2 * M * H + 2 * H * D + M * D),
         "bwd_dW1": b * (2 * M * H + M * D + 2 * H * D),
     }
+    k["bwd_gemms"] = k["bwd_dW2"] + k["bwd_dx"] + k["bwd_dW1"]
+    return k

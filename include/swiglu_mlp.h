@@ -86,8 +86,10 @@ swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2,
  *   run) it holds h [M,H] at offset 0 and grad_preact [M,2H] at the next 256-byte
  *   boundary after h.
  * Kernels: grad_h = dy @ W2 fused with the SwiGLU backward (writes grad_preact and
- * h), dW2 = dy^T @ h, dx = grad_preact @ W1, dW1 = grad_preact^T @ x (one merged
- * [2H,M] @ [M,D] product).  With M = 0, dW1 and dW2 are set to zero.
+ * h), then dW2 = dy^T @ h, dx = grad_preact @ W1, dW1 = grad_preact^T @ x (one merged
+ * [2H,M] @ [M,D] product) -- these three independent GEMMs share one persistent
+ * launch whose tiles are balanced across the SMs.  With M = 0, dW1 and dW2 are set
+ * to zero.
  */
 swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2,
                              const void* preact, const void* dy,
@@ -163,7 +165,9 @@ void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
  * loads, so the consumers' waits run out and the kernel returns with
  * SWIGLU_ERR_TIMEOUT recorded (used to test the timeout path; no fault).
  * Bit 1: every GEMM uses single-CTA 128-row tiles instead of CTA-pair 256-row
- * tiles (both paths compute the same result; used to test each). */
+ * tiles.  Bit 2: the backward launches dW2, dx and dW1 separately instead of as
+ * one grouped launch.  (Every setting computes the same result; the bits exist
+ * to test each path.) */
 void swiglu_mlp_set_debug_flags(int flags);
 
 /* Kernel kinds reported by the launch trace. */
@@ -174,7 +178,8 @@ typedef enum {
     SWIGLU_KERNEL_BWD_DW2 = 4,      /* dW2 = dy^T @ h */
     SWIGLU_KERNEL_BWD_DX = 5,       /* dx = grad_preact @ W1 */
     SWIGLU_KERNEL_BWD_DW1 = 6,      /* dW1 = grad_preact^T @ x */
-    SWIGLU_KERNEL_GEMM = 7          /* swiglu_mlp_gemm_bf16 */
+    SWIGLU_KERNEL_GEMM = 7,         /* swiglu_mlp_gemm_bf16 */
+    SWIGLU_KERNEL_BWD_GEMMS = 8     /* dW2, dx and dW1 in one launch (the backward's default) */
 } swiglu_kernel_kind;
 
 /*

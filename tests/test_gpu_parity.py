@@ -107,8 +107,17 @@ def test_forward_matches_oracle(b, cta_mode, s):
     parity(y, y_ref, "y")
 
 
+@pytest.fixture(params=["grouped", "ungrouped", "single"])
+def bwd_mode(request, b):
+    """The backward's dW2/dx/dW1 as one grouped launch (default), as three launches,
+    and with single-CTA tiles."""
+    b.swiglu_mlp_set_debug_flags({"grouped": 0, "ungrouped": 4, "single": 2}[request.param])
+    yield request.param
+    b.swiglu_mlp_set_debug_flags(0)
+
+
 @pytest.mark.parametrize("s", SMALL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
-def test_backward_matches_oracle(b, cta_mode, s):
+def test_backward_matches_oracle(b, bwd_mode, s):
     _, x, W1, W2, dy = workloads.make_block(s, seed=4)
     preact = workloads.make_preact(s, seed=4, gate_sweep=True)
     gh, gp_ref, h_ref, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, preact, dy)
@@ -241,3 +250,25 @@ def test_call_from_worker_thread(b):
     t.join()
     assert "err" not in out, out.get("err")
     parity(out["C"], (A.double() @ B.double().T).cpu().numpy(), "C from worker thread")
+
+
+def test_host_step_runner_matches_direct_calls(b):
+    from bwd_gemm_epilogue_gb300.pipeline import HostStepRunner
+    s = Shape(300, 320, 392, 264)
+    steps = []
+    for seed in (31, 32, 33):
+        _, x, W1, W2, dy = workloads.make_block(s, seed=seed)
+        steps.append({"x": x.pin_memory(), "W1": W1.pin_memory(), "W2": W2.pin_memory(), "dy": dy.pin_memory()})
+    outs = [{k: torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+             for k, shape in (("y", (s.M, s.Dout)), ("dx", (s.M, s.D)), ("dW1", (2 * s.H, s.D)), ("dW2", (s.Dout, s.H)))}
+            for _ in steps]
+    r = HostStepRunner(s.M, s.D, s.H, s.Dout)
+    r.run(steps, outs)
+    r.synchronize()
+    ok_status(b)
+    for inp, out in zip(steps, outs):
+        d = {k: v.cuda() for k, v in inp.items()}
+        pre, y = b.swiglu_mlp_fwd(d["x"], d["W1"], d["W2"])
+        dx, dW1, dW2 = b.swiglu_mlp_bwd(d["x"], d["W1"], d["W2"], pre, d["dy"])
+        for k, ref in (("y", y), ("dx", dx), ("dW1", dW1), ("dW2", dW2)):
+            assert torch.equal(out[k], ref.cpu()), k
