@@ -4,9 +4,10 @@
 
 Inputs are the target block's widths (D = Dout = 3584, H = 14336) with a smaller
 token count M, so the operands still exceed the 129 MB L2 while the whole case
-holds well under a few GB of device memory.  Each iteration launches exactly one
-kernel of the chosen kind (the fused segment, the forward GEMM with its SwiGLU
-epilogue, or one of the plain GEMMs) through the C ABI.
+holds well under a few GB of device memory.  Each iteration launches one kernel
+of the chosen kind (the fused segment, the forward GEMM with its SwiGLU epilogue,
+or one of the plain GEMMs) through the C ABI, or the whole forward ("fwd": two
+launches) or backward ("bwd": the fused kernel, then the grouped dW2/dx/dW1).
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ import torch
 from . import binding, workloads
 from .workloads import Shape
 
-KERNELS = ("fwd_preact", "fwd_down", "bwd_grad_h", "bwd_dW2", "bwd_dx", "bwd_dW1")
+KERNELS = ("fwd_preact", "fwd_down", "bwd_grad_h", "bwd_dW2", "bwd_dx", "bwd_dW1", "fwd", "bwd")
 
 
 def main():
@@ -51,6 +52,10 @@ def main():
             binding.swiglu_mlp_gemm_bf16(gp, W1, s.M, s.D, 2 * s.H, False, True)
         elif k == "bwd_dW1":
             binding.swiglu_mlp_gemm_bf16(gp, x, 2 * s.H, s.D, s.M, True, True)
+        elif k == "fwd":      # x @ W1^T + SwiGLU epilogue, then h @ W2^T
+            binding.swiglu_mlp_fwd(x, W1, W2)
+        elif k == "bwd":      # fused grad_h + SwiGLU backward, then the grouped dW2 / dx / dW1 launch
+            binding.swiglu_mlp_bwd(x, W1, W2, preact, dy)
     st = binding.swiglu_mlp_device_status(dev)
     if st != 0:
         raise SystemExit(f"device status {binding.swiglu_mlp_strerror(st)}")

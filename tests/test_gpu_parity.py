@@ -272,3 +272,35 @@ def test_host_step_runner_matches_direct_calls(b):
         dx, dW1, dW2 = b.swiglu_mlp_bwd(d["x"], d["W1"], d["W2"], pre, d["dy"])
         for k, ref in (("y", y), ("dx", dx), ("dW1", dW1), ("dW2", dW2)):
             assert torch.equal(out[k], ref.cpu()), k
+
+
+def test_three_layer_stack_against_the_oracle_chain(b):
+    # The oracle runs its own chain: its bf16-rounded y_l feeds layer l+1, its bf16-rounded
+    # dx_l is the dy of layer l-1 (the tensors the GPU path stores in bf16).  No oracle
+    # input comes from the GPU.
+    from bwd_gemm_epilogue_gb300.stack import SwiGLUStack
+    s = Shape(300, 256, 392, 256)
+    x, dy = workloads.make_activations(s, 41)
+    layers = [workloads.make_weights(s, 50 + l) for l in range(3)]
+    st = SwiGLUStack([(W1.cuda(), W2.cuda()) for W1, W2 in layers], s.M)
+    y = st.forward(x.cuda())
+    dx, grads = st.backward(dy.cuda())
+    ok_status(b)
+    acts, pres = [x], []
+    for W1, W2 in layers:
+        p, _, yl = oracle.fwd(acts[-1], W1, W2)
+        pres.append(torch.from_numpy(p).to(torch.bfloat16))
+        acts.append(torch.from_numpy(yl).to(torch.bfloat16))
+    parity(y, oracle.fwd(acts[-2], *layers[-1])[2], "stack y")
+    cur = dy
+    ref_grads = [None] * 3
+    for l in range(2, -1, -1):
+        W1, W2 = layers[l]
+        _, _, _, dxl, dW1l, dW2l = oracle.bwd_full(acts[l], W1, W2, pres[l], cur)
+        ref_grads[l] = (dW1l, dW2l)
+        cur = torch.from_numpy(dxl).to(torch.bfloat16)
+        last_dx = dxl
+    parity(dx, last_dx, "stack dx")
+    for l in range(3):
+        parity(grads[l][0], ref_grads[l][0], f"stack dW1[{l}]")
+        parity(grads[l][1], ref_grads[l][1], f"stack dW2[{l}]")
