@@ -50,7 +50,7 @@ SIGNATURES = {
 }
 
 KERNEL_KINDS = {1: "fwd_preact", 2: "fwd_down", 3: "bwd_grad_h", 4: "bwd_dW2", 5: "bwd_dx", 6: "bwd_dW1", 7: "gemm",
-                8: "bwd_gemms"}
+                8: "bwd_gemms", 9: "elementwise"}
 
 
 class SwigluError(RuntimeError):

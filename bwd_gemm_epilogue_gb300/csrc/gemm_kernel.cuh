@@ -119,6 +119,11 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;             // what the leader's stage barrier waits for
     static constexpr int NOUT = (EPI == EPI_STORE) ? 1 : 3;
+    // Store-only epilogues (64 registers) run two warps per TMEM lane quadrant, each
+    // draining every other chunk, so twice the TMA stores are in flight; the SwiGLU
+    // epilogues need too many registers for that and keep one warp per quadrant.
+    static constexpr int EPI_WARPS = (EPI == EPI_STORE) ? 8 : 4;
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     static constexpr int OUT_TILE = 32 * CHUNK * 2;               // one warp's 32x32 bf16 tile
     static constexpr int OUT_BUFS = (EPI == EPI_SWIGLU_BWD && CG == 2) ? 1 : 2;
     static constexpr int OUT_WARP_BYTES = OUT_BUFS * NOUT * OUT_TILE;
@@ -131,7 +136,7 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EIN = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_OUT = OFF_EIN + EIN_SLOTS * EIN_SLOT_BYTES;
-    static constexpr int OFF_BAR = OFF_OUT + 4 * OUT_WARP_BYTES;
+    static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_WARP_BYTES;
     // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], ein_full[E], ein_empty[E], drain
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EIN_SLOTS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;       // tmem base, abort flag
@@ -192,6 +197,14 @@ __device__ __forceinline__ int problem_of(const KernelArgs& a, int t) {
     return pi;
 }
 
+// Per-problem fields selected with constant indices only: indexing the parameter
+// block with a run-time value makes every access go through generic loads (and
+// measured 12-20% slower mainloops).
+template <class T>
+__device__ __forceinline__ const T* pick3(int pi, const T* p0, const T* p1, const T* p2) {
+    return pi == 0 ? p0 : (pi == 1 ? p1 : p2);
+}
+
 // The tiles of cluster c: round robin over the launch, or the host's list.
 template <bool SCHED, class Args>
 __device__ __forceinline__ int tiles_first(const Args& a, int c) {
@@ -211,10 +224,10 @@ __device__ __forceinline__ int tile_at(const Args& a, int i) {
 
 // Bounded wait on an mbarrier phase.  Returns false (after recording `role` in the
 // error word and raising the CTA abort flag) when the limit runs out, or when
-// another role has already aborted.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long timeout_ns, int* err,
-                                          volatile int* abort_flag, int role) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+// another role has already aborted.  The first probe is inline; only a wait that
+// has to spin calls out.
+__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+                                               int* err, volatile int* abort_flag, int role) {
     const uint64_t start = ptx::globaltimer();
     for (uint32_t n = 1;; ++n) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -227,6 +240,12 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigne
             }
         }
     }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, unsigned long long timeout_ns, int* err,
+                                             volatile int* abort_flag, int role) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_bounded_slow(bar, parity, timeout_ns, err, abort_flag, role);
 }
 
 // Short bounded wait used only while draining after an abort.
@@ -276,7 +295,7 @@ template <int EPI, int CG, bool SCHED>
 using ArgsOf = typename std::conditional<SCHED, ScheduledArgs, KernelArgs>::type;
 
 template <int EPI, int CG, bool SCHED>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     gemm_kernel(const __grid_constant__ ArgsOf<EPI, CG, SCHED> args) {
     using C = Cfg<EPI, CG>;
     extern __shared__ uint8_t smem_raw[];
@@ -314,7 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull_bar(b), 1);
-            ptx::mbar_init(tempty_bar(b), 4 * CG);   // every epilogue warp of the pair
+            ptx::mbar_init(tempty_bar(b), C::EPI_WARPS * CG);   // every epilogue warp of the pair
         }
         for (int s = 0; s < C::EIN_SLOTS; ++s) {
             ptx::mbar_init(ein_full_bar(s), 1);
@@ -323,10 +342,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
-        for (int q = 0; q < args.num_problems; ++q) {
-            ptx::prefetch_tmap(&args.a[q]);
-            ptx::prefetch_tmap(&args.b[q]);
-            ptx::prefetch_tmap(&args.o0[q]);
+#pragma unroll
+        for (int q = 0; q < MAX_PROBLEMS; ++q) {
+            if (q < args.num_problems) {
+                ptx::prefetch_tmap(&args.a[q]);
+                ptx::prefetch_tmap(&args.b[q]);
+                ptx::prefetch_tmap(&args.o0[q]);
+            }
         }
         if (EPI != EPI_STORE) ptx::prefetch_tmap(&args.o1);
         if (EPI == EPI_SWIGLU_BWD) ptx::prefetch_tmap(&args.i0);
@@ -349,6 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && !(args.debug_flags & DEBUG_SKIP_PRODUCER)) {
+            const uint32_t full_bar_leader = CG == 2 ? ptx::mapa_shared(full_bar(0), 0) : 0u;
             int stage = 0;
             uint32_t phase = 0;
             int last_parity[C::STAGES];
@@ -357,11 +380,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int it = t_first; it < t_end && ok; it += t_step) {
                 const int t = tile_at<SCHED>(args, it);
-                const int pi = problem_of(args, t);
-                const CUtensorMap* mA = &args.a[pi];
-                const CUtensorMap* mB = &args.b[pi];
+                const int pi = SCHED ? problem_of(args, t) : 0;
+                const CUtensorMap* mA = SCHED ? pick3(pi, &args.a[0], &args.a[1], &args.a[2]) : &args.a[0];
+                const CUtensorMap* mB = SCHED ? pick3(pi, &args.b[0], &args.b[1], &args.b[2]) : &args.b[0];
                 // per-tile fields in registers: the asm statements below clobber memory
-                const Problem pr = args.prob[pi];
+                const Problem pr = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
                 const int k_blocks = pr.k_blocks;
                 const bool a_mn = pr.a_mn != 0, b_mn = pr.b_mn != 0;
                 int tm, tn;
@@ -374,7 +397,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t fb_local = full_bar(stage);
                     // CG == 2: both CTAs' copies complete on the leader's stage barrier.
-                    const uint32_t fb = CG == 2 ? ptx::mapa_shared(fb_local, 0) : fb_local;
+                    const uint32_t fb = CG == 2 ? full_bar_leader + 8u * stage : fb_local;
                     if (leader) ptx::mbar_arrive_expect_tx(fb_local, C::TX_BYTES);
                     last_parity[stage] = (int)phase;
                     const int k0 = kb * BK;
@@ -431,10 +454,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             int local = 0;
             for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
-                const int pi = problem_of(args, tile_at<SCHED>(args, it));
-                const int k_blocks = args.prob[pi].k_blocks;
-                const bool a_mn = args.prob[pi].a_mn != 0, b_mn = args.prob[pi].b_mn != 0;
+                const int pi = SCHED ? problem_of(args, tile_at<SCHED>(args, it)) : 0;
+                const Problem& pq = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
+                const int k_blocks = pq.k_blocks;
+                const bool a_mn = pq.a_mn != 0, b_mn = pq.b_mn != 0;
                 const uint32_t idesc = umma_idesc(a_mn, b_mn, CG);
+                // Descriptors of stage 0, k = 0; a stage and a 16-k step only move the start
+                // address (low 14 bits, in 16-byte units, no carry below 256 KB).
+                // K-major: the next 16 k sit 32 bytes further along each 128-B row;
+                // MN-major: they are the next 16 rows of 128 B.
+                const uint64_t a_desc0 = a_mn ? umma_desc_sw128(base + C::OFF_A, 8192, 1024)
+                                              : umma_desc_sw128(base + C::OFF_A, 16, 1024);
+                const uint64_t b_desc0 = b_mn ? umma_desc_sw128(base + C::OFF_B, 8192, 1024)
+                                              : umma_desc_sw128(base + C::OFF_B, 16, 1024);
+                const int a_kstep = a_mn ? (2048 >> 4) : (32 >> 4);
+                const int b_kstep = b_mn ? (2048 >> 4) : (32 >> 4);
                 const int ab = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
                 if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, tmo, err, abort_flag, ERR_MMA)) {
@@ -449,16 +483,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
-                    const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
+                    const uint64_t ad0 = a_desc0 + (uint64_t)(stage * (C::A_BYTES >> 4));
+                    const uint64_t bd0 = b_desc0 + (uint64_t)(stage * (C::B_BYTES >> 4));
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
-                        // K-major: the next 16 k sit 32 bytes further along each 128-B row.
-                        // MN-major: the next 16 k are the next 16 rows of 128 B.
-                        const uint64_t ad = a_mn ? umma_desc_sw128(sA + k * 2048, 8192, 1024)
-                                                 : umma_desc_sw128(sA + k * 32, 16, 1024);
-                        const uint64_t bd = b_mn ? umma_desc_sw128(sB + k * 2048, 8192, 1024)
-                                                 : umma_desc_sw128(sB + k * 32, 16, 1024);
+                        const uint64_t ad = ad0 + (uint64_t)(k * a_kstep);
+                        const uint64_t bd = bd0 + (uint64_t)(k * b_kstep);
                         if (CG == 2) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         else ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
@@ -522,7 +552,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int wq = warp & 3;                 // TMEM lane quadrant = tile rows [32wq, 32wq+32)
         const int row = 32 * wq + lane;          // row within this CTA's 128 rows
-        const uint32_t out_base = base + C::OFF_OUT + wq * C::OUT_WARP_BYTES;
+        const int grp = (warp - EPI_WARP0) >> 2; // which of the quadrant's warps (store-only: 0 or 1)
+        constexpr int GROUPS = C::EPI_WARPS / 4;
+        const uint32_t out_base = base + C::OFF_OUT + (warp - EPI_WARP0) * C::OUT_WARP_BYTES;
         int ein_slot = 0;
         uint32_t ein_phase = 0;
         int ob = 0;
@@ -530,10 +562,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
             const int t = tile_at<SCHED>(args, it);
-            const int pi = problem_of(args, t);
-            const Problem pr = args.prob[pi];   // registers (asm statements clobber memory)
+            const int pi = SCHED ? problem_of(args, t) : 0;
+            // registers (asm statements clobber memory)
+            const Problem pr = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
             const int n_limit = pr.N;
-            const CUtensorMap* mO0 = &args.o0[pi];
+            const CUtensorMap* mO0 = SCHED ? pick3(pi, &args.o0[0], &args.o0[1], &args.o0[2]) : &args.o0[0];
             int tm, tn;
             tile_coords(pr, t - pr.tile_begin, tm, tn);
             const int m0 = tm * (BM * CG) + BM * (int)rank;
@@ -551,7 +584,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_fence_after();
             const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
 
-            for (int c = 0; c < C::CHUNKS; ++c) {
+            for (int c = grp; c < C::CHUNKS; c += GROUPS) {
                 uint32_t acc[32];
                 uint32_t acc2[32];
                 if (EPI == EPI_SWIGLU_FWD) {
@@ -561,7 +594,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
                 }
                 ptx::tmem_ld_wait();
-                if (c == C::CHUNKS - 1) {
+                if (c + GROUPS >= C::CHUNKS) {   // this warp's last chunk of the tile
                     // Accumulator fully read: hand it back to the MMA warp (of the leader CTA).
                     ptx::tc_fence_before();
                     __syncwarp();

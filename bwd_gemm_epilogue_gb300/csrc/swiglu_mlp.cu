@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "gemm_kernel.cuh"
+#include "skinny_kernel.cuh"
 #include "swiglu_mlp.h"
 
 namespace swiglu {
@@ -214,7 +215,7 @@ swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cu
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(Cfg<EPI, CG>::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = nullptr;
@@ -261,9 +262,159 @@ swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cu
     return SWIGLU_OK;
 }
 
+// ---------------------------------------------------------------- small-M (decode) path
+
+// Host-only test hook bit: keep the 128/256-row tile path even for M <= 64.
+constexpr int DEBUG_NO_SKINNY = 8;
+
+bool use_skinny(int64_t M) { return M >= 1 && M <= SK_MAX_M && !(g_debug_flags.load() & DEBUG_NO_SKINNY); }
+int64_t skinny_ld(int64_t M) { return (M + 15) / 16 * 16; }
+
+template <class F>
+swiglu_status launch_traced(int kind, cudaStream_t stream, F&& do_launch) {
+    Trace& tr = g_trace;
+    const int slot = tr.events ? tr.count++ : -1;
+    const bool traced = slot >= 0 && slot < tr.capacity;
+    cudaError_t e;
+    if (traced) {
+        tr.kinds[slot] = kind;
+        e = cudaEventRecord(tr.events[2 * slot], stream);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventRecord(trace)", e);
+    }
+    e = do_launch();
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "kernel launch", e);
+    if (traced) {
+        e = cudaEventRecord(tr.events[2 * slot + 1], stream);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventRecord(trace)", e);
+    }
+    return SWIGLU_OK;
+}
+
+// acc [N, ld] fp32 = W * X^T with W [N, K] (w_mn = 0) or [K, N] (w_mn = 1) and X [M, K];
+// split over K so the work units cover the SMs.  acc is zeroed here first.
+swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, const void* X, float* acc, int64_t N,
+                         int64_t K, int64_t M, cudaStream_t s) {
+    const int64_t ld = skinny_ld(M);
+    cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)N * ld * 4, s);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync(skinny accumulator)", e);
+    static thread_local SkinnyArgs a;
+    std::memset(&a, 0, sizeof a);
+    if (!encode_operand(&a.w, W, N, K, w_mn, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny w)");
+    if (!encode_operand(&a.x, X, M, K, false, (uint32_t)ld)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny x)");
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)N};
+        cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+        cuuint32_t box[2] = {16, 32};
+        cuuint32_t estr[2] = {1, 1};
+        if (g_encode(&a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny accumulator)");
+    }
+    a.N = (int)N;
+    a.K = (int)K;
+    a.n_mma = (int)ld;
+    a.w_mn = w_mn ? 1 : 0;
+    a.n_tiles = (int)((N + BM - 1) / BM);
+    a.k_blocks = (int)((K + BK - 1) / BK);
+    // Split count: the fewest splits whose makespan ceil(tiles * s / SMs) / s (in
+    // whole-K tiles) is within 2% of the best over s = 1..32 with >= 2 k-blocks per
+    // split (fewer splits, less fp32 reduce traffic and per-unit overhead).
+    auto span_of = [&](int sp) {
+        const long long units = (long long)a.n_tiles * sp;
+        return (double)((units + st->num_sms - 1) / st->num_sms) / sp;
+    };
+    double best = span_of(1);
+    for (int sp = 2; sp <= 32 && sp * 2 <= a.k_blocks; ++sp) best = span_of(sp) < best ? span_of(sp) : best;
+    int splits = 1;
+    while (span_of(splits) > best * 1.02) ++splits;
+    a.kb_per_split = (a.k_blocks + splits - 1) / splits;
+    a.splits = (a.k_blocks + a.kb_per_split - 1) / a.kb_per_split;   // every split non-empty
+    a.timeout_ns = g_timeout_ns.load();
+    a.err = st->err_word;
+    a.debug_flags = g_debug_flags.load();
+    e = cudaFuncSetAttribute(skinny_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(skinny smem)", e);
+    const int units = a.n_tiles * a.splits;
+    const int grid = units < st->num_sms ? units : st->num_sms;
+    return launch_traced(kind, s, [&]() {
+        skinny_gemm_kernel<<<grid, NUM_THREADS, SK_SMEM_BYTES, s>>>(a);
+        return cudaGetLastError();
+    });
+}
+
+int elementwise_grid(DeviceState* st, long long total) {
+    long long g = (total + 255) / 256;
+    const long long cap = (long long)st->num_sms * 8;
+    return (int)(g < cap ? (g < 1 ? 1 : g) : cap);
+}
+
+struct SkinnyFwdWs { void* h; float* pt; float* yt; };
+struct SkinnyBwdWs { void* h; void* gp; float* gt; float* dxt; };
+
+size_t skinny_fwd_ws(int64_t M, int64_t H, int64_t Dout, SkinnyFwdWs* w, void* base);
+size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, SkinnyBwdWs* w, void* base);
+
 bool dims_ok(int64_t v) { return v > 0 && v % 8 == 0 && v < (int64_t(1) << 31); }
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace layouts of the small-M path: the regular buffers first (h; h and
+// grad_preact), then the fp32 transposed accumulators.
+size_t skinny_fwd_ws(int64_t M, int64_t H, int64_t Dout, SkinnyFwdWs* w, void* base) {
+    const int64_t ld = skinny_ld(M);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+        off += round256(bytes);
+        return p;
+    };
+    uint8_t* h = take((size_t)M * H * 2);
+    uint8_t* pt = take((size_t)2 * H * ld * 4);
+    uint8_t* yt = take((size_t)Dout * ld * 4);
+    if (w) *w = SkinnyFwdWs{h, reinterpret_cast<float*>(pt), reinterpret_cast<float*>(yt)};
+    return off;
+}
+
+size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, SkinnyBwdWs* w, void* base) {
+    const int64_t ld = skinny_ld(M);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+        off += round256(bytes);
+        return p;
+    };
+    uint8_t* h = take((size_t)M * H * 2);
+    uint8_t* gp = take((size_t)M * 2 * H * 2);
+    uint8_t* gt = take((size_t)H * ld * 4);
+    uint8_t* dxt = take((size_t)D * ld * 4);
+    if (w) *w = SkinnyBwdWs{h, gp, reinterpret_cast<float*>(gt), reinterpret_cast<float*>(dxt)};
+    return off;
+}
+
+// Forward for M <= 64 tokens.
+swiglu_status run_fwd_skinny(DeviceState* st, const void* x, const void* W1, const void* W2, void* preact, void* y,
+                             int64_t M, int64_t D, int64_t H, int64_t Dout, void* ws, cudaStream_t s) {
+    SkinnyFwdWs w;
+    skinny_fwd_ws(M, H, Dout, &w, ws);
+    const int ld = (int)skinny_ld(M);
+    swiglu_status rc = run_skinny(st, SWIGLU_KERNEL_FWD_PREACT, W1, false, x, w.pt, 2 * H, D, M, s);   // preact^T
+    if (rc != SWIGLU_OK) return rc;
+    const int g = elementwise_grid(st, (long long)M * H);
+    rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
+        skinny_swiglu_fwd_kernel<<<g, 256, 0, s>>>(w.pt, ld, static_cast<__nv_bfloat16*>(preact),
+                                                    static_cast<__nv_bfloat16*>(w.h), (int)M, (int)H);
+        return cudaGetLastError();
+    });
+    if (rc != SWIGLU_OK) return rc;
+    rc = run_skinny(st, SWIGLU_KERNEL_FWD_DOWN, W2, false, w.h, w.yt, Dout, H, M, s);   // y^T
+    if (rc != SWIGLU_OK) return rc;
+    const int g2 = elementwise_grid(st, (long long)M * Dout);
+    return launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
+        skinny_cast_kernel<<<g2, 256, 0, s>>>(w.yt, ld, static_cast<__nv_bfloat16*>(y), (int)M, (int)Dout);
+        return cudaGetLastError();
+    });
+}
 
 // ---------------------------------------------------------------- the block's kernels
 
@@ -354,15 +505,15 @@ extern "C" {
 
 size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
     (void)D;
-    (void)Dout;
     if (M <= 0 || H <= 0) return 0;
+    if (M <= SK_MAX_M && Dout > 0) return skinny_fwd_ws(M, H, Dout, nullptr, nullptr);
     return round256((size_t)M * (size_t)H * 2);
 }
 
 size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
-    (void)D;
     (void)Dout;
     if (M <= 0 || H <= 0) return 0;
+    if (M <= SK_MAX_M && D > 0) return skinny_bwd_ws(M, D, H, nullptr, nullptr);
     return round256((size_t)M * (size_t)H * 2) + round256((size_t)M * (size_t)H * 4);
 }
 
@@ -382,6 +533,7 @@ swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2, void
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (use_skinny(M)) return run_fwd_skinny(st, x, W1, W2, preact, y, M, D, H, Dout, workspace, s);
     void* h = workspace;
     rc = run_fwd_preact(st, x, W1, preact, h, M, D, H, s);
     if (rc != SWIGLU_OK) return rc;
@@ -412,6 +564,37 @@ swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, cons
     if (rc != SWIGLU_OK) return rc;
     void* h = workspace;
     void* grad_preact = static_cast<uint8_t*>(workspace) + round256((size_t)M * (size_t)H * 2);
+    if (use_skinny(M)) {
+        // M <= 64 tokens: weight-streaming products transposed and split over K
+        SkinnyBwdWs w;
+        skinny_bwd_ws(M, D, H, &w, workspace);
+        const int ld = (int)skinny_ld(M);
+        rc = run_skinny(st, SWIGLU_KERNEL_BWD_GRAD_H, W2, true, dy, w.gt, H, Dout, M, s);   // grad_h^T = W2^T dy^T
+        if (rc != SWIGLU_OK) return rc;
+        const int ge = elementwise_grid(st, (long long)M * H);
+        rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
+            skinny_swiglu_bwd_kernel<<<ge, 256, 0, s>>>(w.gt, ld, static_cast<const __nv_bfloat16*>(preact),
+                                                         static_cast<__nv_bfloat16*>(w.gp),
+                                                         static_cast<__nv_bfloat16*>(w.h), (int)M, (int)H);
+            return cudaGetLastError();
+        });
+        if (rc != SWIGLU_OK) return rc;
+        rc = run_skinny(st, SWIGLU_KERNEL_BWD_DX, W1, true, w.gp, w.dxt, D, 2 * H, M, s);   // dx^T = W1^T gp^T
+        if (rc != SWIGLU_OK) return rc;
+        const int gc = elementwise_grid(st, (long long)M * D);
+        rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
+            skinny_cast_kernel<<<gc, 256, 0, s>>>(w.dxt, ld, static_cast<__nv_bfloat16*>(dx), (int)M, (int)D);
+            return cudaGetLastError();
+        });
+        if (rc != SWIGLU_OK) return rc;
+        // the weight gradients (K = M) are output-bound: the regular kernels, as one launch when both use CTA pairs
+        const GemmSpec wg[2] = {{dy, w.h, dW2, Dout, H, M, true, true}, {w.gp, x, dW1, 2 * H, D, M, true, true}};
+        if (pick_cg(Dout) == 2 && pick_cg(2 * H) == 2 && !(g_debug_flags.load() & DEBUG_UNGROUPED))
+            return run_gemm_group(st, SWIGLU_KERNEL_BWD_GEMMS, wg, 2, s);
+        rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, dy, w.h, dW2, Dout, H, M, true, true, s);
+        if (rc != SWIGLU_OK) return rc;
+        return run_gemm(st, SWIGLU_KERNEL_BWD_DW1, w.gp, x, dW1, 2 * H, D, M, true, true, s);
+    }
     rc = run_fused_bwd(st, dy, W2, preact, grad_preact, h, M, H, Dout, s);
     if (rc != SWIGLU_OK) return rc;
     const GemmSpec g[3] = {

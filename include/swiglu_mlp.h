@@ -56,11 +56,14 @@ typedef enum {
     SWIGLU_ERR_CUDA = 7                /* any other CUDA runtime error */
 } swiglu_status;
 
-/* Bytes of workspace swiglu_mlp_fwd needs: the transient h [M,H] bf16. */
+/* Bytes of workspace swiglu_mlp_fwd needs: the transient h [M,H] bf16; for M <= 64
+ * also two fp32 accumulators of the small-M path (preact^T [2H, M16] and
+ * y^T [Dout, M16], M16 = M rounded up to 16), each on a 256-byte boundary. */
 size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
 
 /* Bytes of workspace swiglu_mlp_bwd needs: h [M,H] and grad_preact [M,2H], bf16,
- * each starting on a 256-byte boundary. */
+ * each starting on a 256-byte boundary; for M <= 64 also the small-M path's fp32
+ * accumulators grad_h^T [H, M16] and dx^T [D, M16]. */
 size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
 
 /*
@@ -70,7 +73,10 @@ size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Do
  *   y [M,Dout]                                 output
  *   workspace >= swiglu_mlp_fwd_workspace_size bytes; holds h between the two GEMMs.
  * Kernels: x @ W1^T with a SwiGLU epilogue that writes preact and
- * h = bf16(left * bf16(silu(gate))), then y = h @ W2^T.
+ * h = bf16(left * bf16(silu(gate))), then y = h @ W2^T.  For M <= 64 tokens
+ * (decode) the two products run transposed with the weights as the 128-row MMA
+ * operand, split over K into fp32 workspace sums, and small element-wise kernels
+ * apply the SwiGLU and round to bf16.
  */
 swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2,
                              void* preact, void* y,
@@ -166,7 +172,8 @@ void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
  * SWIGLU_ERR_TIMEOUT recorded (used to test the timeout path; no fault).
  * Bit 1: every GEMM uses single-CTA 128-row tiles instead of CTA-pair 256-row
  * tiles.  Bit 2: the backward launches dW2, dx and dW1 separately instead of as
- * one grouped launch.  (Every setting computes the same result; the bits exist
+ * one grouped launch.  Bit 3: M <= 64 keeps the 128-row tile path instead of the
+ * small-M path.  (Every setting computes the same result; the bits exist
  * to test each path.) */
 void swiglu_mlp_set_debug_flags(int flags);
 
@@ -179,7 +186,8 @@ typedef enum {
     SWIGLU_KERNEL_BWD_DX = 5,       /* dx = grad_preact @ W1 */
     SWIGLU_KERNEL_BWD_DW1 = 6,      /* dW1 = grad_preact^T @ x */
     SWIGLU_KERNEL_GEMM = 7,         /* swiglu_mlp_gemm_bf16 */
-    SWIGLU_KERNEL_BWD_GEMMS = 8     /* dW2, dx and dW1 in one launch (the backward's default) */
+    SWIGLU_KERNEL_BWD_GEMMS = 8,    /* dW2, dx and dW1 in one launch (the backward's default) */
+    SWIGLU_KERNEL_ELEMENTWISE = 9   /* small-M path: SwiGLU forward/backward or cast of fp32 sums */
 } swiglu_kernel_kind;
 
 /*

@@ -30,7 +30,10 @@ def test_workspace_sizes():
     assert b.swiglu_mlp_bwd_workspace_size(M, D, H, Dout) == M * H * 2 + M * 2 * H * 2
     assert b.swiglu_mlp_fwd_workspace_size(0, D, H, Dout) == 0
     # ragged: each buffer starts on a 256-byte boundary
-    assert b.swiglu_mlp_bwd_workspace_size(3, 8, 8, 8) == 256 + 256
+    assert b.swiglu_mlp_bwd_workspace_size(3, 8, 8, 8) == 256 + 256 + 512 + 512   # + small-M fp32 sums
+    assert b.swiglu_mlp_bwd_workspace_size(65, 8, 8, 8) == 1280 + 2304            # M > 64: h, grad_preact
+    # small-M forward: h, preact^T [2H, 16], y^T [Dout, 16] (fp32)
+    assert b.swiglu_mlp_fwd_workspace_size(16, 4096, 11008, 4096) == 16 * 11008 * 2 + 2 * 11008 * 16 * 4 + 4096 * 16 * 4
 
 
 def test_strerror_and_version():

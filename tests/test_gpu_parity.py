@@ -304,3 +304,31 @@ def test_three_layer_stack_against_the_oracle_chain(b):
     for l in range(3):
         parity(grads[l][0], ref_grads[l][0], f"stack dW1[{l}]")
         parity(grads[l][1], ref_grads[l][1], f"stack dW2[{l}]")
+
+
+@pytest.mark.parametrize("M", [1, 16, 40, 64])
+@pytest.mark.parametrize("small_m_path", [True, False])
+def test_few_token_block_matches_oracle(b, M, small_m_path):
+    # M <= 64 runs the transposed, K-split weight-streaming kernels (small_m_path);
+    # the test hook bit 3 keeps the 128/256-row tile kernels for comparison.
+    s = Shape(M, 512, 1024, 768)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=60 + M)
+    b.swiglu_mlp_set_debug_flags(0 if small_m_path else 8)
+    try:
+        preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2))
+        pre_in = workloads.make_preact(s, seed=60 + M, gate_sweep=True)
+        ws = torch.empty(b.swiglu_mlp_bwd_workspace_size(M, s.D, s.H, s.Dout), dtype=torch.uint8, device="cuda")
+        dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(pre_in), dev(dy), workspace=ws)
+        ok_status(b)
+    finally:
+        b.swiglu_mlp_set_debug_flags(0)
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2)
+    parity(preact, p_ref, "preact")
+    parity(y, y_ref, "y")
+    _, gp_ref, h_ref, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre_in, dy)
+    h, gp = b.bwd_workspace_views(ws, M, s.H)
+    parity(gp, gp_ref, "grad_preact")
+    parity(h, h_ref, "h")
+    parity(dx, dx_ref, "dx")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
