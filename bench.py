@@ -156,9 +156,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(kind: str):
-    """DRAM bytes per launch of `kind` from the committed ncu summary, or None when the
-    kernel sources changed since the capture."""
+def measured_traffic(kind: str, workload: str = "target"):
+    """DRAM bytes per launch of `kind` from the committed ncu summary of the target
+    step, or None for another workload or when the kernel sources changed since."""
+    if workload != "target":
+        return None
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         data = json.load(open(path))
@@ -268,14 +270,14 @@ def run_ours(args):
         # 16 tokens: every kernel streams its weights; the HBM roofline bounds it
         dom_gbs = kstats[dom]["hbm_gbs_compulsory"]
         roofline = {"kernel": dom, "bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(dom_gbs / pk["hbm_gbs"], 3), "traffic": measured_traffic(dom),
+                    "frac": round(dom_gbs / pk["hbm_gbs"], 3), "traffic": measured_traffic(dom, wl),
                     "peak_source": f"{pk_src} hbm_gbs"}
     else:
         dom_achieved = kstats[dom]["tflops"]
         roofline = {"kernel": dom, "bound": "tensor", "achieved": dom_achieved,
                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                     "frac": round(dom_achieved / pk["bf16_tflops_sustained"], 3),
-                    "traffic": measured_traffic(dom),
+                    "traffic": measured_traffic(dom, wl),
                     "peak_source": f"{pk_src} bf16_tflops_sustained (kernel timed inside a long step)"}
     fused = kstats.get("bwd_grad_h", {})
 
