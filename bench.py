@@ -63,6 +63,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The slowest rank's value (timings are reported as the max over ranks)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: every rank runs its own replica (weak scaling)."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- clocks
 
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -239,11 +255,7 @@ def run_ours(args):
     st = binding.swiglu_mlp_device_status(dev)
     if st != 0:
         raise RuntimeError(f"timed steps failed: {binding.swiglu_mlp_strerror(st)}")
-    ms = ev0.elapsed_time(ev1) / K
-    if ws_n > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / K, dev)
     recs = trace.records()
     launches = trace.count
 
@@ -299,10 +311,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
     barrier()
-    if ws_n > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     st = binding.swiglu_mlp_device_status(dev)
     if st != 0:
         raise RuntimeError(f"e2e steps failed: {binding.swiglu_mlp_strerror(st)}")
@@ -314,7 +323,7 @@ def run_ours(args):
         cpu = cpu_baseline(s, x_h, W1_h, W2_h, dy_h, pre_h, args.cpu_seconds)
         cpu["sample"] = cpu["sample"].replace("target block", f"{wl} block")
 
-    value = ws_n * flops["step"] / (ms * 1e-3) / 1e12
+    value = job_tflops(flops["step"], ms, ws_n)
     in_bytes = sum(t.numel() * 2 for t in (x_h, W1_h, W2_h, dy_h))
     step_bytes = sum(kb.get(k, 0) * kstats[k]["launches"] / K for k in kstats)
     out = {
@@ -344,7 +353,7 @@ def run_ours(args):
         "kernels": kstats,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(ws_n * flops["step"] / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_tflops(flops["step"], e2e_ms, ws_n), 1), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "overlap": "h2d of step i+1 and d2h of step i-1 run during step i (3 streams)"},
         "gpu_launches": launches,
