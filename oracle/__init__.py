@@ -61,11 +61,11 @@ def _load():
                 getattr(lib, f).restype = d
                 getattr(lib, f).argtypes = [d]
             lib.oracle_swiglu_fwd.restype = i32
-            lib.oracle_swiglu_fwd.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, vp, i64, i32,
+            lib.oracle_swiglu_fwd.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, vp, i64, i32, i32,
                                               vp, vp, vp]
             lib.oracle_swiglu_bwd_rows.restype = i32
             lib.oracle_swiglu_bwd_rows.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, i64,
-                                                   i32, vp, vp, vp, vp]
+                                                   i32, i32, vp, vp, vp, vp]
             lib.oracle_swiglu_bwd_cols.restype = i32
             lib.oracle_swiglu_bwd_cols.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, i64,
                                                    i32, vp, vp]
@@ -127,8 +127,9 @@ def silu_prime(g: float) -> float:
     return float(_load().oracle_silu_prime(float(g)))
 
 
-def fwd(x, W1, W2, rows=None, round_intermediates: bool = True):
+def fwd(x, W1, W2, rows=None, round_intermediates: bool = True, residual: bool = False):
     """Forward for the selected token rows (all rows when ``rows`` is None).
+    ``residual``: the residual block y = x + MLP(x) (D == Dout).
 
     Returns (preact [n,2H], h [n,H], y [n,Dout]) as fp64 arrays.
     """
@@ -136,7 +137,7 @@ def fwd(x, W1, W2, rows=None, round_intermediates: bool = True):
     M, D = xb.shape
     H = w1b.shape[0] // 2
     Dout = w2b.shape[0]
-    if w1b.shape != (2 * H, D) or w2b.shape != (Dout, H):
+    if w1b.shape != (2 * H, D) or w2b.shape != (Dout, H) or (residual and D != Dout):
         raise ValueError("shape mismatch")
     ridx, n = _index(rows, M)
     preact = np.empty((n, 2 * H))
@@ -144,14 +145,14 @@ def fwd(x, W1, W2, rows=None, round_intermediates: bool = True):
     y = np.empty((n, Dout))
     rc = _load().oracle_swiglu_fwd(_ptr(xb), _ptr(w1b), _ptr(w2b), _kind(xb, w1b, w2b),
                                    M, D, H, Dout, _ptr(ridx), n,
-                                   int(round_intermediates), _ptr(preact), _ptr(h), _ptr(y))
+                                   int(round_intermediates), int(residual), _ptr(preact), _ptr(h), _ptr(y))
     if rc != 0:
         raise MemoryError("oracle_swiglu_fwd failed")
     return preact, h, y
 
 
-def bwd_rows(W1, W2, preact, dy, rows=None, round_intermediates: bool = True):
-    """Row-wise backward outputs for the selected token rows.
+def bwd_rows(W1, W2, preact, dy, rows=None, round_intermediates: bool = True, residual: bool = False):
+    """Row-wise backward outputs for the selected token rows (``residual``: dx += dy).
 
     Returns (grad_h [n,H], grad_preact [n,2H], h [n,H], dx [n,D]) as fp64 arrays.
     """
@@ -160,7 +161,7 @@ def bwd_rows(W1, W2, preact, dy, rows=None, round_intermediates: bool = True):
     H = H2 // 2
     Dout = w2b.shape[0]
     M = pb.shape[0]
-    if pb.shape != (M, 2 * H) or dyb.shape != (M, Dout) or w2b.shape != (Dout, H):
+    if pb.shape != (M, 2 * H) or dyb.shape != (M, Dout) or w2b.shape != (Dout, H) or (residual and D != Dout):
         raise ValueError("shape mismatch")
     ridx, n = _index(rows, M)
     gh = np.empty((n, H))
@@ -169,7 +170,7 @@ def bwd_rows(W1, W2, preact, dy, rows=None, round_intermediates: bool = True):
     dx = np.empty((n, D))
     rc = _load().oracle_swiglu_bwd_rows(_ptr(w1b), _ptr(w2b), _ptr(pb), _ptr(dyb),
                                         _kind(w1b, w2b, pb, dyb), M, D, H, Dout,
-                                        _ptr(ridx), n, int(round_intermediates),
+                                        _ptr(ridx), n, int(round_intermediates), int(residual),
                                         _ptr(gh), _ptr(gp), _ptr(h), _ptr(dx))
     if rc != 0:
         raise MemoryError("oracle_swiglu_bwd_rows failed")
@@ -200,8 +201,8 @@ def bwd_cols(x, W2, preact, dy, cols=None, round_intermediates: bool = True):
     return dW2c, dW1[:n], dW1[n:]
 
 
-def bwd_full(x, W1, W2, preact, dy, round_intermediates: bool = True):
+def bwd_full(x, W1, W2, preact, dy, round_intermediates: bool = True, residual: bool = False):
     """Whole backward on a small problem: (grad_h, grad_preact, h, dx, dW1 [2H,D], dW2 [Dout,H])."""
-    gh, gp, h, dx = bwd_rows(W1, W2, preact, dy, None, round_intermediates)
+    gh, gp, h, dx = bwd_rows(W1, W2, preact, dy, None, round_intermediates, residual)
     dW2c, dW1l, dW1g = bwd_cols(x, W2, preact, dy, None, round_intermediates)
     return gh, gp, h, dx, np.concatenate([dW1l, dW1g], axis=0), dW2c.T.copy()

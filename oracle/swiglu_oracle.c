@@ -39,6 +39,11 @@
  * round_mode = 0 keeps every intermediate in exact fp64 (used by the
  * finite-difference and autograd pins).
  *
+ * residual = 1 gives the residual block y = x + MLP(x) (requires D == Dout), the
+ * "Residual Add Epilogue" of the lesson "Transformer MLP, GEMM and operator fusion"
+ * (lincklin.cn, section 24: the down projection's output plus the block input); its
+ * backward adds dy to dx (the identity path), the weight gradients are unchanged.
+ *
  * Every loop is a plain sum over the contraction index in ascending order;
  * OpenMP only splits independent output rows/columns across threads.
  */
@@ -121,7 +126,7 @@ static double *to_f64(oracle_mat src, int64_t n) {
  */
 int oracle_swiglu_fwd(const void *x_p, const void *W1_p, const void *W2_p, int in_f64,
                       int64_t M, int64_t D, int64_t H, int64_t Dout,
-                      const int64_t *rows, int64_t nrows, int round_mode,
+                      const int64_t *rows, int64_t nrows, int round_mode, int residual,
                       double *preact_out, double *h_out, double *y_out) {
     (void)M;
     oracle_mat x = {x_p, in_f64};
@@ -155,7 +160,8 @@ int oracle_swiglu_fwd(const void *x_p, const void *W1_p, const void *W2_p, int i
             for (int64_t o = 0; o < Dout; ++o) {
                 double acc = 0.0;
                 for (int64_t j = 0; j < H; ++j) acc += hr[j] * w2[o * H + j];
-                y_out[i * Dout + o] = acc;
+                /* residual block: y = x + MLP(x) (needs D == Dout) */
+                y_out[i * Dout + o] = residual ? xr[o] + acc : acc;
             }
         }
         if (preact_out) memcpy(preact_out + i * 2 * H, pre, (size_t)(2 * H) * sizeof(double));
@@ -178,7 +184,7 @@ int oracle_swiglu_fwd(const void *x_p, const void *W1_p, const void *W2_p, int i
 int oracle_swiglu_bwd_rows(const void *W1_p, const void *W2_p,
                            const void *preact_p, const void *dy_p, int in_f64,
                            int64_t M, int64_t D, int64_t H, int64_t Dout,
-                           const int64_t *rows, int64_t nrows, int round_mode,
+                           const int64_t *rows, int64_t nrows, int round_mode, int residual,
                            double *grad_h_out, double *grad_preact_out,
                            double *h_out, double *dx_out) {
     (void)M;
@@ -220,6 +226,9 @@ int oracle_swiglu_bwd_rows(const void *W1_p, const void *W2_p,
             const double *w1r = w1 + r * D;
             for (int64_t d = 0; d < D; ++d) dxr[d] += g * w1r[d];
         }
+        /* residual block: the identity path adds dy to dx (needs D == Dout) */
+        if (residual)
+            for (int64_t d = 0; d < D; ++d) dxr[d] += at(dy, m * Dout + d);
         if (grad_h_out) memcpy(grad_h_out + i * H, gh, (size_t)H * sizeof(double));
         if (grad_preact_out) memcpy(grad_preact_out + i * 2 * H, gp, (size_t)(2 * H) * sizeof(double));
         if (dx_out) memcpy(dx_out + i * D, dxr, (size_t)D * sizeof(double));

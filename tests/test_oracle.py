@@ -273,3 +273,49 @@ def test_target_flops_and_activation_bytes():
     assert abs((s.M * 2 * s.H + s.M * s.Dout) * 2 / 2 ** 20 - mem["after_fwd_drop_h"]) < 1.5
     st = GOLDEN["stack4_memory_mib"]
     assert round(st["after_fwd_normal"] - st["after_fwd_drop_h"], 1) == 4 * mem["saved_by_drop_h"]
+
+
+# ----------------------------------------------------------------------------
+# residual block y = x + MLP(x)
+# ----------------------------------------------------------------------------
+
+def test_residual_chain_matches_torch_autograd_and_finite_differences():
+    M, D, H = 5, 8, 12
+    x, W1, W2, dy = (_rand64((M, D), 21), _rand64((2 * H, D), 22, D ** -0.5),
+                     _rand64((D, H), 23, H ** -0.5), _rand64((M, D), 24))
+    ref = _torch_chain(x, W1, W2, dy)          # MLP part only; the residual adds x and passes dy
+    _, _, y = oracle.fwd(x, W1, W2, round_intermediates=False, residual=True)
+    np.testing.assert_allclose(y, (ref["y"] + x).numpy(), rtol=1e-11, atol=1e-12)
+    preact, _, _ = oracle.fwd(x, W1, W2, round_intermediates=False)
+    _, _, _, dx, dW1, dW2 = oracle.bwd_full(x, W1, W2, torch.from_numpy(preact), dy,
+                                           round_intermediates=False, residual=True)
+    np.testing.assert_allclose(dx, (ref["dx"] + dy).numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dW1, ref["dW1"].numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dW2, ref["dW2"].numpy(), rtol=1e-11, atol=1e-12)
+    # finite differences of L = sum(dy * (x + MLP(x))) with respect to x
+    xn, w1n, w2n, dyn = x.numpy(), W1.numpy(), W2.numpy(), dy.numpy()
+    eps = 1e-6
+    fd = np.empty_like(xn)
+    for idx in np.ndindex(xn.shape):
+        a = xn.copy()
+        a[idx] += eps
+        lp = float((oracle.fwd(a, w1n, w2n, round_intermediates=False, residual=True)[2] * dyn).sum())
+        a[idx] -= 2 * eps
+        lm = float((oracle.fwd(a, w1n, w2n, round_intermediates=False, residual=True)[2] * dyn).sum())
+        fd[idx] = (lp - lm) / (2 * eps)
+    np.testing.assert_allclose(dx, fd, rtol=1e-6, atol=1e-8)
+
+
+def test_residual_with_zero_down_projection_is_the_identity():
+    g = torch.Generator().manual_seed(31)
+    M, D, H = 7, 16, 24
+    x = torch.randn(M, D, generator=g).to(torch.bfloat16)
+    dy = torch.randn(M, D, generator=g).to(torch.bfloat16)
+    W1 = torch.randn(2 * H, D, generator=g).mul(D ** -0.5).to(torch.bfloat16)
+    W2 = torch.zeros(D, H, dtype=torch.bfloat16)
+    _, _, y = oracle.fwd(x, W1, W2, residual=True)
+    np.testing.assert_array_equal(y, x.double().numpy())
+    preact = torch.from_numpy(oracle.fwd(x, W1, W2)[0]).to(torch.bfloat16)
+    _, gp, _, dx = oracle.bwd_rows(W1, W2, preact, dy, residual=True)
+    assert not gp.any()                                   # grad_h = dy @ 0 = 0
+    np.testing.assert_array_equal(dx, dy.double().numpy())
