@@ -50,6 +50,8 @@ def parse():
                     help="target: the block at the pages' target shape (the headline line); "
                          "prefill / decode: the 4096- and 16-token LLaMA-7B-shaped blocks; "
                          "stack4: four target blocks trained end to end (with memory)")
+    ap.add_argument("--residual", action="store_true",
+                    help="time the residual block y = x + MLP(x) (residual-add epilogues; D == Dout)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -225,8 +227,8 @@ def run_ours(args):
     ws_b = torch.empty(binding.swiglu_mlp_bwd_workspace_size(M, D, H, Do), dtype=torch.uint8, device=dev)
 
     def step():
-        binding.swiglu_mlp_fwd(x, W1, W2, preact, y, ws_f)
-        binding.swiglu_mlp_bwd(x, W1, W2, preact, dy, dx, dW1, dW2, ws_b)
+        binding.swiglu_mlp_fwd(x, W1, W2, preact, y, ws_f, residual=args.residual)
+        binding.swiglu_mlp_bwd(x, W1, W2, preact, dy, dx, dW1, dW2, ws_b, residual=args.residual)
 
     def barrier():
         if ws_n > 1:
@@ -282,21 +284,21 @@ def run_ours(args):
         # 16 tokens: every kernel streams its weights; the HBM roofline bounds it
         dom_gbs = kstats[dom]["hbm_gbs_compulsory"]
         roofline = {"kernel": dom, "bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(dom_gbs / pk["hbm_gbs"], 3), "traffic": measured_traffic(dom, wl),
+                    "frac": round(dom_gbs / pk["hbm_gbs"], 3), "traffic": measured_traffic(dom, wl if not args.residual else "residual"),
                     "peak_source": f"{pk_src} hbm_gbs"}
     else:
         dom_achieved = kstats[dom]["tflops"]
         roofline = {"kernel": dom, "bound": "tensor", "achieved": dom_achieved,
                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                     "frac": round(dom_achieved / pk["bf16_tflops_sustained"], 3),
-                    "traffic": measured_traffic(dom, wl),
+                    "traffic": measured_traffic(dom, wl if not args.residual else "residual"),
                     "peak_source": f"{pk_src} bf16_tflops_sustained (kernel timed inside a long step)"}
     fused = kstats.get("bwd_grad_h", {})
 
     # ---- end to end: pinned host inputs in, results out, every step; copies of
     # neighbouring steps overlap this step's compute (HostStepRunner)
     from bwd_gemm_epilogue_gb300.pipeline import HostStepRunner
-    runner = HostStepRunner(M, D, H, Do, dev)
+    runner = HostStepRunner(M, D, H, Do, dev, residual=args.residual)
     host_in = {k: t.pin_memory() for k, t in (("x", x_h), ("W1", W1_h), ("W2", W2_h), ("dy", dy_h))}
     host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory()
                 for k, t in (("y", y), ("dx", dx), ("dW1", dW1), ("dW2", dW2))}
@@ -327,8 +329,9 @@ def run_ours(args):
     in_bytes = sum(t.numel() * 2 for t in (x_h, W1_h, W2_h, dy_h))
     step_bytes = sum(kb.get(k, 0) * kstats[k]["launches"] / K for k in kstats)
     out = {
-        "metric": ("SwiGLU MLP fwd+bwd TFLOP/s (bf16, 11136x3584x14336); fused grad_preact us" if wl == "target"
-                   else f"SwiGLU MLP fwd+bwd TFLOP/s (bf16, {M}x{D}x{H}, {wl})"),
+        "metric": ("SwiGLU MLP fwd+bwd TFLOP/s (bf16, 11136x3584x14336); fused grad_preact us"
+                   if wl == "target" and not args.residual
+                   else f"SwiGLU MLP fwd+bwd TFLOP/s (bf16, {M}x{D}x{H}, {wl}{', residual' if args.residual else ''})"),
         "value": round(value, 1),
         "unit": "TFLOP/s",
         "n_gpus": ws_n,
@@ -338,10 +341,11 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": (round(value / ws_n / (flops["step"] / (PAGES_FULL_MS_B200 * 1e-3) / 1e12), 3)
-                        if wl == "target" else None),
+                        if wl == "target" and not args.residual else None),
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations/dy, N(0,1/fan_in) weights, bf16)",
-        "config": {"workload": f"SwiGLU MLP block fwd+bwd, M={M} D={D} H={H} Dout={Do}, drop-h, bf16",
+        "config": {"workload": (f"SwiGLU MLP {'residual block y = x + MLP(x)' if args.residual else 'block'} "
+                                f"fwd+bwd, M={M} D={D} H={H} Dout={Do}, drop-h, bf16"),
                    "M": M, "D": D, "H": H, "Dout": Do, "parallelism": f"replicas x{ws_n}",
                    "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB per step), no flush"},
         "step_hbm_gbs_compulsory": round(step_bytes / (ms * 1e-3) / 1e9, 1),

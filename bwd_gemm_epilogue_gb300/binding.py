@@ -36,6 +36,8 @@ SIGNATURES = {
     "swiglu_mlp_bwd_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
     "swiglu_mlp_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "swiglu_mlp_fwd_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "swiglu_mlp_bwd_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
     "swiglu_mlp_fused_grad_preact": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "swiglu_mlp_gemm_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
@@ -185,18 +187,19 @@ def _dims(x, W1, W2):
     return M, D, H, Dout
 
 
-def swiglu_mlp_fwd(x, W1, W2, preact=None, y=None, workspace=None):
-    """Forward; returns (preact [M,2H], y [M,Dout])."""
+def swiglu_mlp_fwd(x, W1, W2, preact=None, y=None, workspace=None, residual: bool = False):
+    """Forward; returns (preact [M,2H], y [M,Dout]).  residual: y = x + MLP(x)
+    (swiglu_mlp_fwd_residual; D == Dout)."""
     M, D, H, Dout = _dims(x, W1, W2)
     preact = _empty((M, 2 * H), x) if preact is None else preact
     y = _empty((M, Dout), x) if y is None else y
     need = swiglu_mlp_fwd_workspace_size(M, D, H, Dout)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    st = lib().swiglu_mlp_fwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), M, D, H, Dout,
-                              _ptr(workspace), workspace.numel() * workspace.element_size(),
-                              _stream(x.device))
-    _check(st, "swiglu_mlp_fwd")
+    fn = lib().swiglu_mlp_fwd_residual if residual else lib().swiglu_mlp_fwd
+    st = fn(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), M, D, H, Dout,
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(x.device))
+    _check(st, "swiglu_mlp_fwd_residual" if residual else "swiglu_mlp_fwd")
     return preact, y
 
 
@@ -216,8 +219,9 @@ def swiglu_mlp_fwd_noalloc(x, W1, W2, preact=None, y=None):
     return preact, y
 
 
-def swiglu_mlp_bwd(x, W1, W2, preact, dy, dx=None, dW1=None, dW2=None, workspace=None):
-    """Backward; returns (dx [M,D], dW1 [2H,D], dW2 [Dout,H])."""
+def swiglu_mlp_bwd(x, W1, W2, preact, dy, dx=None, dW1=None, dW2=None, workspace=None, residual: bool = False):
+    """Backward; returns (dx [M,D], dW1 [2H,D], dW2 [Dout,H]).  residual: dx += dy
+    (swiglu_mlp_bwd_residual; D == Dout)."""
     M, D, H, Dout = _dims(x, W1, W2)
     if tuple(preact.shape) != (M, 2 * H) or tuple(dy.shape) != (M, Dout):
         raise ValueError("preact / dy shape mismatch")
@@ -227,10 +231,10 @@ def swiglu_mlp_bwd(x, W1, W2, preact, dy, dx=None, dW1=None, dW2=None, workspace
     need = swiglu_mlp_bwd_workspace_size(M, D, H, Dout)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    st = lib().swiglu_mlp_bwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dW1),
-                              _ptr(dW2), M, D, H, Dout, _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _stream(x.device))
-    _check(st, "swiglu_mlp_bwd")
+    fn = lib().swiglu_mlp_bwd_residual if residual else lib().swiglu_mlp_bwd
+    st = fn(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dW1), _ptr(dW2),
+            M, D, H, Dout, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(x.device))
+    _check(st, "swiglu_mlp_bwd_residual" if residual else "swiglu_mlp_bwd")
     return dx, dW1, dW2
 
 
@@ -267,22 +271,24 @@ def swiglu_mlp_gemm_bf16(A, B, M: int, N: int, K: int, a_mn_major: bool, b_mn_ma
 
 class SwiGLUMLP(torch.autograd.Function):
     """autograd wrapper: forward saves (x, W1, W2, preact) and drops h; backward
-    calls swiglu_mlp_bwd.  Leading dimensions of x are flattened."""
+    calls swiglu_mlp_bwd.  Leading dimensions of x are flattened.  With residual
+    set it is the block y = x + MLP(x) (the residual entry points)."""
 
     @staticmethod
-    def forward(ctx, x, W1, W2):
+    def forward(ctx, x, W1, W2, residual=False):
         x2 = x.reshape(-1, x.shape[-1]).contiguous()
-        preact, y = swiglu_mlp_fwd(x2, W1.contiguous(), W2.contiguous())
+        preact, y = swiglu_mlp_fwd(x2, W1.contiguous(), W2.contiguous(), residual=residual)
         ctx.save_for_backward(x2, W1, W2, preact)
+        ctx.residual = residual
         return y.reshape(*x.shape[:-1], y.shape[-1])
 
     @staticmethod
     def backward(ctx, grad_y):
         x2, W1, W2, preact = ctx.saved_tensors
         dy = grad_y.reshape(-1, grad_y.shape[-1]).contiguous()
-        dx, dW1, dW2 = swiglu_mlp_bwd(x2, W1.contiguous(), W2.contiguous(), preact, dy)
-        return dx.reshape(*grad_y.shape[:-1], dx.shape[-1]), dW1, dW2
+        dx, dW1, dW2 = swiglu_mlp_bwd(x2, W1.contiguous(), W2.contiguous(), preact, dy, residual=ctx.residual)
+        return dx.reshape(*grad_y.shape[:-1], dx.shape[-1]), dW1, dW2, None
 
 
-def swiglu_mlp(x, W1, W2):
-    return SwiGLUMLP.apply(x, W1, W2)
+def swiglu_mlp(x, W1, W2, residual: bool = False):
+    return SwiGLUMLP.apply(x, W1, W2, residual)

@@ -31,6 +31,10 @@
 //                   accumulator columns [0,128) are `left` and [128,256) the matching
 //                   `gate`.  Stores preact (both halves, bf16) and
 //                   h = bf16(left * bf16(silu(gate))) computed from the bf16 preact.
+//   EPI_STORE_ADD   C = bf16(acc + R) for problems flagged `res`: R [M, N] is TMA-prefetched
+//                   by warp 2 like the backward's preact (the residual-add epilogue of the
+//                   "Transformer MLP, GEMM and operator fusion" lesson, section 24: the down
+//                   projection adds the block input; the backward's dx adds dy).
 //   EPI_SWIGLU_BWD  acc = grad_h[m0:, j0:j0+256] (dy @ W2), never written out.  With the
 //                   prefetched left/gate: dleft = grad_h * silu(gate),
 //                   dgate = grad_h * left * silu'(gate), silu' = sigma + silu*(1 - sigma),
@@ -55,7 +59,7 @@
 
 namespace swiglu {
 
-enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
+enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_STORE_ADD = 3 };
 
 constexpr int BM = 128;           // accumulator rows per CTA
 constexpr int BN = 256;           // accumulator columns
@@ -83,12 +87,13 @@ struct Problem {
     int band;         // n-tiles per raster band (L2 reuse)
     int k_blocks;
     int a_mn, b_mn;   // operand major-ness (1 = M- or N-contiguous)
+    int res;          // EPI_STORE_ADD: add the residual tensor (tensor map i0) to this problem's output
     int tile_begin;   // index of this problem's first tile in the launch
 };
 
 struct KernelArgs {
     CUtensorMap a[MAX_PROBLEMS], b[MAX_PROBLEMS], o0[MAX_PROBLEMS];
-    CUtensorMap o1, i0;   // SWIGLU epilogues: h output; preact input (backward)
+    CUtensorMap o1, i0;   // SWIGLU epilogues: h output; preact input (backward) / residual [M, N] (EPI_STORE_ADD)
     Problem prob[MAX_PROBLEMS];
     int num_problems;
     int num_tiles;
@@ -113,23 +118,25 @@ struct Cfg {
     // buffers get what is left (CTA-pair SWIGLU_BWD: 5 stages, 2 preact slots and
     // single-buffered output tiles measured 7% faster than 4 / 3 / 2).
     static constexpr int STAGES = CG == 1 ? (EPI == EPI_STORE ? 4 : 3) : (EPI == EPI_STORE ? 6 : 5);
+    static constexpr bool STORE_ONLY = EPI == EPI_STORE || EPI == EPI_STORE_ADD;   // one bf16 output
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_ROWS = BN / CG;                        // B rows (N) held by this CTA
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;             // what the leader's stage barrier waits for
-    static constexpr int NOUT = (EPI == EPI_STORE) ? 1 : 3;
+    static constexpr int NOUT = STORE_ONLY ? 1 : 3;
     // Store-only epilogues (64 registers) run two warps per TMEM lane quadrant, each
     // draining every other chunk, so twice the TMA stores are in flight; the SwiGLU
     // epilogues need too many registers for that and keep one warp per quadrant.
-    static constexpr int EPI_WARPS = (EPI == EPI_STORE) ? 8 : 4;
+    static constexpr int EPI_WARPS = STORE_ONLY ? 8 : 4;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     static constexpr int OUT_TILE = 32 * CHUNK * 2;               // one warp's 32x32 bf16 tile
     static constexpr int OUT_BUFS = (EPI == EPI_SWIGLU_BWD && CG == 2) ? 1 : 2;
     static constexpr int OUT_WARP_BYTES = OUT_BUFS * NOUT * OUT_TILE;
-    static constexpr int EIN_SLOTS = (EPI == EPI_SWIGLU_BWD) ? 2 : 0;
+    // epilogue-input slots: preact left + gate (SWIGLU_BWD) or the residual (STORE_ADD)
+    static constexpr int EIN_SLOTS = (EPI == EPI_SWIGLU_BWD || EPI == EPI_STORE_ADD) ? 2 : 0;
     static constexpr int EIN_HALF = BM * CHUNK * 2;               // 128 rows x 32 cols bf16
-    static constexpr int EIN_SLOT_BYTES = 2 * EIN_HALF;           // left + gate
+    static constexpr int EIN_SLOT_BYTES = (EPI == EPI_SWIGLU_BWD ? 2 : 1) * EIN_HALF;
     static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CHUNK : BN / CHUNK;
 
     static constexpr int OFF_A = 0;
@@ -350,8 +357,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 ptx::prefetch_tmap(&args.o0[q]);
             }
         }
-        if (EPI != EPI_STORE) ptx::prefetch_tmap(&args.o1);
-        if (EPI == EPI_SWIGLU_BWD) ptx::prefetch_tmap(&args.i0);
+        if (!C::STORE_ONLY) ptx::prefetch_tmap(&args.o1);
+        if (EPI == EPI_SWIGLU_BWD || EPI == EPI_STORE_ADD) ptx::prefetch_tmap(&args.i0);
     }
     if (warp == 1) {
         if (CG == 2) {
@@ -547,6 +554,43 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     if (last_parity[s] >= 0) drain_wait(ein_full_bar(s), (uint32_t)last_parity[s], tmo);
             }
         }
+        if (EPI == EPI_STORE_ADD && lane == 0) {
+            // the residual [M, N] tiles of the problems that carry one, 128 rows x 32 columns
+            // per chunk, in the order the epilogue warps consume them
+            int slot = 0;
+            uint32_t phase = 0;
+            int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
+            for (int s = 0; s < C::EIN_SLOTS; ++s) last_parity[s] = -1;
+            bool ok = true;
+            for (int it = t_first; it < t_end && ok; it += t_step) {
+                const int t = tile_at<SCHED>(args, it);
+                const int pi = SCHED ? problem_of(args, t) : 0;
+                const Problem pr = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
+                if (!pr.res) continue;
+                int tm, tn;
+                tile_coords(pr, t - pr.tile_begin, tm, tn);
+                const int m0 = tm * (BM * CG) + BM * (int)rank;
+                const int n0 = tn * BN;
+                for (int c = 0; c < C::CHUNKS; ++c) {
+                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, tmo, err, abort_flag, ERR_AUX)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = ein_full_bar(slot);
+                    ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
+                    last_parity[slot] = (int)phase;
+                    ptx::tma_load_2d(base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES, &args.i0, fb, n0 + c * CHUNK, m0);
+                    if (++slot == C::EIN_SLOTS) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < C::EIN_SLOTS; ++s)
+                    if (last_parity[s] >= 0) drain_wait(ein_full_bar(s), (uint32_t)last_parity[s], tmo);
+            }
+        }
         __syncwarp();
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
@@ -557,6 +601,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         const uint32_t out_base = base + C::OFF_OUT + (warp - EPI_WARP0) * C::OUT_WARP_BYTES;
         int ein_slot = 0;
         uint32_t ein_phase = 0;
+        int res_tiles = 0;   // EPI_STORE_ADD: residual tiles drained so far (slot bookkeeping)
         int ob = 0;
         int local = 0;
         bool ok = true;
@@ -604,8 +649,29 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     }
                 }
 
-                // epilogue inputs (backward): the saved preact left/gate for these 32 columns
+                // epilogue inputs (backward): the saved preact left/gate for these 32 columns;
+                // (residual store) the residual's 32 columns
                 uint32_t lft[16], gte[16];
+                if (EPI == EPI_STORE_ADD && pr.res) {
+                    constexpr int NSLOT = C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1;
+                    const int q = res_tiles * C::CHUNKS + c;
+                    const int slot = q % NSLOT;
+                    const bool in_ok = __all_sync(0xffffffffu, wait_bounded(ein_full_bar(slot),
+                                                                            (uint32_t)((q / NSLOT) & 1), tmo,
+                                                                            err, abort_flag, ERR_EPILOGUE));
+                    if (!in_ok) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t slot_base = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint4 r4 = ptx::lds128(slot_base + sw64_offset(row, q4));
+                        lft[4 * q4 + 0] = r4.x; lft[4 * q4 + 1] = r4.y; lft[4 * q4 + 2] = r4.z; lft[4 * q4 + 3] = r4.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ein_empty_bar(slot));
+                }
                 if (EPI == EPI_SWIGLU_BWD) {
                     const bool in_ok = __all_sync(
                         0xffffffffu, wait_bounded(ein_full_bar(ein_slot), ein_phase, tmo, err, abort_flag, ERR_EPILOGUE));
@@ -631,10 +697,16 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
 
                 // outputs for this chunk, packed bf16 pairs
                 uint32_t o0[16], o1[16], o2[16];
-                if (EPI == EPI_STORE) {
+                if (EPI == EPI_STORE || (EPI == EPI_STORE_ADD && !pr.res)) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         o0[i] = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+                } else if (EPI == EPI_STORE_ADD) {
+                    // residual add: C = acc + R, summed in fp32 and rounded once
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        o0[i] = pack_bf16(__uint_as_float(acc[2 * i]) + bf16_lo(lft[i]),
+                                          __uint_as_float(acc[2 * i + 1]) + bf16_hi(lft[i]));
                 } else if (EPI == EPI_SWIGLU_FWD) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -690,7 +762,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && rows_live) {
-                    if (EPI == EPI_STORE) {
+                    if (C::STORE_ONLY) {
                         const int n = tn * BN + c * CHUNK;
                         if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
                     } else {
@@ -706,6 +778,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 if (lane == 0) ptx::bulk_commit_group();
                 ob = (ob + 1) % C::OUT_BUFS;
             }
+            if (EPI == EPI_STORE_ADD && pr.res) ++res_tiles;
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
         ptx::tc_fence_before();

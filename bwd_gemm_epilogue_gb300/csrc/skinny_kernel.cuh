@@ -255,13 +255,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
 // element-wise finishing kernels (fp32 [N, ld] transposed sums -> bf16 outputs)
 // ---------------------------------------------------------------------------
 
-// out [M, N] bf16 = round(acc^T)
-__global__ void skinny_cast_kernel(const float* __restrict__ acc, int ld, __nv_bfloat16* __restrict__ out, int M,
-                                   int N) {
+// out [M, N] bf16 = round(acc^T (+ res)), res [M, N] bf16 optional (the residual block)
+__global__ void skinny_cast_kernel(const float* __restrict__ acc, int ld, const __nv_bfloat16* __restrict__ res,
+                                   __nv_bfloat16* __restrict__ out, int M, int N) {
     const long long total = (long long)M * N;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
         const int m = (int)(i / N), n = (int)(i % N);
-        out[i] = __float2bfloat16_rn(acc[(long long)n * ld + m]);
+        const float r = res ? __bfloat162float(res[i]) : 0.0f;
+        out[i] = __float2bfloat16_rn(acc[(long long)n * ld + m] + r);
     }
 }
 

@@ -158,6 +158,7 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     p.k_blocks = (int)((K + BK - 1) / BK);
     p.a_mn = a_mn ? 1 : 0;
     p.b_mn = b_mn ? 1 : 0;
+    p.res = 0;
     p.tile_begin = 0;
     return p;
 }
@@ -394,7 +395,8 @@ size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, SkinnyBwdWs* w, void* base
 
 // Forward for M <= 64 tokens.
 swiglu_status run_fwd_skinny(DeviceState* st, const void* x, const void* W1, const void* W2, void* preact, void* y,
-                             int64_t M, int64_t D, int64_t H, int64_t Dout, void* ws, cudaStream_t s) {
+                             int64_t M, int64_t D, int64_t H, int64_t Dout, void* ws, cudaStream_t s,
+                             bool residual) {
     SkinnyFwdWs w;
     skinny_fwd_ws(M, H, Dout, &w, ws);
     const int ld = (int)skinny_ld(M);
@@ -411,7 +413,8 @@ swiglu_status run_fwd_skinny(DeviceState* st, const void* x, const void* W1, con
     if (rc != SWIGLU_OK) return rc;
     const int g2 = elementwise_grid(st, (long long)M * Dout);
     return launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-        skinny_cast_kernel<<<g2, 256, 0, s>>>(w.yt, ld, static_cast<__nv_bfloat16*>(y), (int)M, (int)Dout);
+        skinny_cast_kernel<<<g2, 256, 0, s>>>(w.yt, ld, residual ? static_cast<const __nv_bfloat16*>(x) : nullptr,
+                                              static_cast<__nv_bfloat16*>(y), (int)M, (int)Dout);
         return cudaGetLastError();
     });
 }
@@ -461,38 +464,56 @@ struct GemmSpec {
     void* C;
     int64_t M, N, K;
     bool a_mn, b_mn;
+    const void* R = nullptr;   // optional residual [M, N] added to C
 };
 
-// Fill problem q of `a`: C [M,N] = A * B^T with either operand K-major or MN-major.
+// Fill problem q of `a`: C [M,N] = A * B^T (+ R) with either operand K-major or MN-major.
+// A residual goes through the launch's single residual map i0.
 bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg) {
     if (!encode_operand(&a.a[q], g.A, g.M, g.K, g.a_mn, BM)) return false;
     if (!encode_operand(&a.b[q], g.B, g.N, g.K, g.b_mn, BN / cg)) return false;
     if (!encode_out_2d(&a.o0[q], g.C, g.M, g.N)) return false;
     a.prob[q] = make_problem(g.M, g.N, g.K, (g.N + BN - 1) / BN, g.a_mn, g.b_mn, cg);
+    if (g.R) {
+        if (!encode_2d(&a.i0, g.R, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.N * 2, CHUNK, BM, CU_TENSOR_MAP_SWIZZLE_64B))
+            return false;
+        a.prob[q].res = 1;
+    }
     return true;
 }
 
-// One plain GEMM.
+// One plain GEMM, optionally with a residual added in its epilogue.
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
-                       int64_t K, bool a_mn, bool b_mn, cudaStream_t s) {
+                       int64_t K, bool a_mn, bool b_mn, cudaStream_t s, const void* R = nullptr) {
     const int cg = pick_cg(M);
     KernelArgs a;
     std::memset(&a, 0, sizeof a);
-    if (!add_problem(a, 0, GemmSpec{A, B, Cp, M, N, K, a_mn, b_mn}, cg))
-        return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
+    GemmSpec g{A, B, Cp, M, N, K, a_mn, b_mn};
+    g.R = R;
+    if (!add_problem(a, 0, g, cg)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
     a.num_problems = 1;
+    if (R) {
+        if (cg == 2) return launch<EPI_STORE_ADD, 2, false>(st, kind, a, s);
+        return launch<EPI_STORE_ADD, 1, false>(st, kind, a, s);
+    }
     if (cg == 2) return launch<EPI_STORE, 2, false>(st, kind, a, s);
     return launch<EPI_STORE, 1, false>(st, kind, a, s);
 }
 
 // Several independent plain GEMMs in one persistent launch, tiles balanced across
-// the CTA pairs by the host schedule (CTA-pair tiles; all M > 128).
+// the CTA pairs by the host schedule (CTA-pair tiles; all M > 128).  At most one of
+// them may carry a residual.
 swiglu_status run_gemm_group(DeviceState* st, int kind, const GemmSpec* g, int n, cudaStream_t s) {
     static thread_local ScheduledArgs a;   // ~26 KB: not on the stack
     std::memset(static_cast<KernelArgs*>(&a), 0, sizeof(KernelArgs));
-    for (int q = 0; q < n; ++q)
+    bool res = false;
+    for (int q = 0; q < n; ++q) {
+        if (g[q].R && res) return fail(SWIGLU_ERR_INVALID_ARG, "group: more than one residual");
+        res = res || g[q].R != nullptr;
         if (!add_problem(a, q, g[q], 2)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (group)");
+    }
     a.num_problems = n;
+    if (res) return launch<EPI_STORE_ADD, 2, true>(st, kind, a, s);
     return launch<EPI_STORE, 2, true>(st, kind, a, s);
 }
 
@@ -517,9 +538,9 @@ size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Do
     return round256((size_t)M * (size_t)H * 2) + round256((size_t)M * (size_t)H * 4);
 }
 
-swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2, void* preact, void* y, int64_t M,
-                             int64_t D, int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes,
-                             void* stream) {
+static swiglu_status fwd_impl(const void* x, const void* W1, const void* W2, void* preact, void* y, int64_t M,
+                              int64_t D, int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes,
+                              void* stream, bool residual) {
     if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
     if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
         return SWIGLU_ERR_UNSUPPORTED_SHAPE;
@@ -533,16 +554,30 @@ swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2, void
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_skinny(M)) return run_fwd_skinny(st, x, W1, W2, preact, y, M, D, H, Dout, workspace, s);
+    if (use_skinny(M)) return run_fwd_skinny(st, x, W1, W2, preact, y, M, D, H, Dout, workspace, s, residual);
     void* h = workspace;
     rc = run_fwd_preact(st, x, W1, preact, h, M, D, H, s);
     if (rc != SWIGLU_OK) return rc;
-    return run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h, W2, y, M, Dout, H, false, false, s);   // y = h @ W2^T
+    // y = h @ W2^T (+ x for the residual block, added in the epilogue)
+    return run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h, W2, y, M, Dout, H, false, false, s, residual ? x : nullptr);
 }
 
-swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
-                             void* dx, void* dW1, void* dW2, int64_t M, int64_t D, int64_t H, int64_t Dout,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2, void* preact, void* y, int64_t M,
+                             int64_t D, int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    return fwd_impl(x, W1, W2, preact, y, M, D, H, Dout, workspace, workspace_bytes, stream, false);
+}
+
+swiglu_status swiglu_mlp_fwd_residual(const void* x, const void* W1, const void* W2, void* preact, void* y,
+                                      int64_t M, int64_t D, int64_t H, int64_t Dout, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    if (D != Dout) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "residual block needs D == Dout");
+    return fwd_impl(x, W1, W2, preact, y, M, D, H, Dout, workspace, workspace_bytes, stream, true);
+}
+
+static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
+                              void* dx, void* dW1, void* dW2, int64_t M, int64_t D, int64_t H, int64_t Dout,
+                              void* workspace, size_t workspace_bytes, void* stream, bool residual) {
     if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
     if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
         return SWIGLU_ERR_UNSUPPORTED_SHAPE;
@@ -583,7 +618,8 @@ swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, cons
         if (rc != SWIGLU_OK) return rc;
         const int gc = elementwise_grid(st, (long long)M * D);
         rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-            skinny_cast_kernel<<<gc, 256, 0, s>>>(w.dxt, ld, static_cast<__nv_bfloat16*>(dx), (int)M, (int)D);
+            skinny_cast_kernel<<<gc, 256, 0, s>>>(w.dxt, ld, residual ? static_cast<const __nv_bfloat16*>(dy) : nullptr,
+                                                  static_cast<__nv_bfloat16*>(dx), (int)M, (int)D);
             return cudaGetLastError();
         });
         if (rc != SWIGLU_OK) return rc;
@@ -597,11 +633,12 @@ swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, cons
     }
     rc = run_fused_bwd(st, dy, W2, preact, grad_preact, h, M, H, Dout, s);
     if (rc != SWIGLU_OK) return rc;
-    const GemmSpec g[3] = {
+    GemmSpec g[3] = {
         {dy, h, dW2, Dout, H, M, true, true},                 // dW2 = dy^T @ h
-        {grad_preact, W1, dx, M, D, 2 * H, false, true},      // dx = grad_preact @ W1
+        {grad_preact, W1, dx, M, D, 2 * H, false, true},      // dx = grad_preact @ W1 (+ dy: residual block)
         {grad_preact, x, dW1, 2 * H, D, M, true, true},       // dW1 = grad_preact^T @ x (merged)
     };
+    if (residual) g[1].R = dy;
     int64_t pair_tiles = 0;   // tiles of the grouped launch (256-row CTA-pair tiles)
     for (const GemmSpec& q : g) pair_tiles += ((q.M + 2 * BM - 1) / (2 * BM)) * ((q.N + BN - 1) / BN);
     const bool grouped = !(g_debug_flags.load() & (DEBUG_UNGROUPED | DEBUG_FORCE_SINGLE_CTA)) && Dout > BM &&
@@ -609,9 +646,23 @@ swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, cons
     if (grouped) return run_gemm_group(st, SWIGLU_KERNEL_BWD_GEMMS, g, 3, s);
     rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, g[0].A, g[0].B, g[0].C, g[0].M, g[0].N, g[0].K, true, true, s);
     if (rc != SWIGLU_OK) return rc;
-    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DX, g[1].A, g[1].B, g[1].C, g[1].M, g[1].N, g[1].K, false, true, s);
+    rc = run_gemm(st, SWIGLU_KERNEL_BWD_DX, g[1].A, g[1].B, g[1].C, g[1].M, g[1].N, g[1].K, false, true, s, g[1].R);
     if (rc != SWIGLU_OK) return rc;
     return run_gemm(st, SWIGLU_KERNEL_BWD_DW1, g[2].A, g[2].B, g[2].C, g[2].M, g[2].N, g[2].K, true, true, s);
+}
+
+swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
+                             void* dx, void* dW1, void* dW2, int64_t M, int64_t D, int64_t H, int64_t Dout,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(x, W1, W2, preact, dy, dx, dW1, dW2, M, D, H, Dout, workspace, workspace_bytes, stream, false);
+}
+
+swiglu_status swiglu_mlp_bwd_residual(const void* x, const void* W1, const void* W2, const void* preact,
+                                      const void* dy, void* dx, void* dW1, void* dW2, int64_t M, int64_t D,
+                                      int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    if (D != Dout) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "residual block needs D == Dout");
+    return bwd_impl(x, W1, W2, preact, dy, dx, dW1, dW2, M, D, H, Dout, workspace, workspace_bytes, stream, true);
 }
 
 swiglu_status swiglu_mlp_fused_grad_preact(const void* dy, const void* W2, const void* preact, void* grad_preact,

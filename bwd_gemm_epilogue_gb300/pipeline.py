@@ -23,7 +23,7 @@ from . import binding
 
 
 class HostStepRunner:
-    def __init__(self, M: int, D: int, H: int, Dout: int, device=None):
+    def __init__(self, M: int, D: int, H: int, Dout: int, device=None, residual: bool = False):
         self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         self.shape = (M, D, H, Dout)
         bf = dict(dtype=torch.bfloat16, device=self.dev)
@@ -32,6 +32,7 @@ class HostStepRunner:
         self.out = [dict(y=torch.empty(M, Dout, **bf), dx=torch.empty(M, D, **bf),
                          dW1=torch.empty(2 * H, D, **bf), dW2=torch.empty(Dout, H, **bf)) for _ in range(2)]
         self.preact = torch.empty(M, 2 * H, **bf)
+        self.residual = residual      # residual block: y = x + MLP(x), dx += dy
         self.ws_f = torch.empty(max(16, binding.swiglu_mlp_fwd_workspace_size(M, D, H, Dout)),
                                 dtype=torch.uint8, device=self.dev)
         self.ws_b = torch.empty(max(16, binding.swiglu_mlp_bwd_workspace_size(M, D, H, Dout)),
@@ -69,9 +70,9 @@ class HostStepRunner:
             self.s_cmp.wait_event(self.h2d_done[b])
             if self._used[b]:
                 self.s_cmp.wait_event(self.d2h_done[b])
-            binding.swiglu_mlp_fwd(d["x"], d["W1"], d["W2"], self.preact, o["y"], self.ws_f)
+            binding.swiglu_mlp_fwd(d["x"], d["W1"], d["W2"], self.preact, o["y"], self.ws_f, residual=self.residual)
             binding.swiglu_mlp_bwd(d["x"], d["W1"], d["W2"], self.preact, d["dy"], o["dx"], o["dW1"], o["dW2"],
-                                   self.ws_b)
+                                   self.ws_b, residual=self.residual)
             self.cmp_done[b].record(self.s_cmp)
         self._used[b] = True
 

@@ -104,6 +104,29 @@ swiglu_status swiglu_mlp_bwd(const void* x, const void* W1, const void* W2,
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Residual block y = x + MLP(x) (requires D == Dout): the down projection adds the
+ * block input in its epilogue instead of writing MLP(x) and adding it in a separate
+ * pass ("Transformer MLP, GEMM and operator fusion" lesson, section 24, residual-add
+ * epilogue).  Same arguments, workspace and saved preact as swiglu_mlp_fwd.
+ * D != Dout returns SWIGLU_ERR_UNSUPPORTED_SHAPE.
+ */
+swiglu_status swiglu_mlp_fwd_residual(const void* x, const void* W1, const void* W2,
+                                      void* preact, void* y,
+                                      int64_t M, int64_t D, int64_t H, int64_t Dout,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of the residual block: as swiglu_mlp_bwd, with the identity path's dy
+ * added to dx in the dx GEMM's epilogue (dx = grad_preact @ W1 + dy); dW1 and dW2
+ * are unchanged.  Requires D == Dout.
+ */
+swiglu_status swiglu_mlp_bwd_residual(const void* x, const void* W1, const void* W2,
+                                      const void* preact, const void* dy,
+                                      void* dx, void* dW1, void* dW2,
+                                      int64_t M, int64_t D, int64_t H, int64_t Dout,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The fused segment alone: grad_h = dy @ W2 (never stored) and the SwiGLU
  * backward epilogue.  Optimization note, section 4; Drop-H report, fused kernel
  * pseudo-code.

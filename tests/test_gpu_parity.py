@@ -332,3 +332,95 @@ def test_few_token_block_matches_oracle(b, M, small_m_path):
     parity(dx, dx_ref, "dx")
     parity(dW1, dW1_ref, "dW1")
     parity(dW2, dW2_ref, "dW2")
+
+
+# ---------------------------------------------------------------------------- residual block y = x + MLP(x)
+
+RESIDUAL = [Shape(128, 256, 512, 256), Shape(300, 320, 392, 320), Shape(600, 264, 520, 264)]
+
+
+@pytest.mark.parametrize("s", RESIDUAL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}")
+def test_residual_forward_matches_oracle(b, cta_mode, s):
+    # the down projection's epilogue adds x before its single rounding
+    _, x, W1, W2, _ = workloads.make_block(s, seed=70, gate_sweep=True)
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2, residual=True)
+    preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2), residual=True)
+    ok_status(b)
+    parity(preact, p_ref, "preact")
+    parity(y, y_ref, "y (residual)")
+
+
+@pytest.mark.parametrize("s", RESIDUAL, ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}")
+def test_residual_backward_matches_oracle(b, bwd_mode, s):
+    # dx = grad_preact @ W1 + dy from the dx GEMM's epilogue; the other outputs are
+    # those of the plain block
+    _, x, W1, W2, dy = workloads.make_block(s, seed=71)
+    preact = workloads.make_preact(s, seed=71, gate_sweep=True)
+    _, gp_ref, h_ref, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, preact, dy, residual=True)
+    ws = torch.empty(b.swiglu_mlp_bwd_workspace_size(s.M, s.D, s.H, s.Dout), dtype=torch.uint8, device="cuda")
+    dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(preact), dev(dy), workspace=ws, residual=True)
+    ok_status(b)
+    h, gp = b.bwd_workspace_views(ws, s.M, s.H)
+    parity(gp, gp_ref, "grad_preact")
+    parity(h, h_ref, "h")
+    parity(dx, dx_ref, "dx (residual)")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
+
+
+@pytest.mark.parametrize("M", [1, 40])
+@pytest.mark.parametrize("small_m_path", [True, False])
+def test_residual_few_tokens(b, M, small_m_path):
+    s = Shape(M, 512, 1024, 512)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=72 + M)
+    pre_in = workloads.make_preact(s, seed=72 + M, gate_sweep=True)
+    b.swiglu_mlp_set_debug_flags(0 if small_m_path else 8)
+    try:
+        preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2), residual=True)
+        dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(pre_in), dev(dy), residual=True)
+        ok_status(b)
+    finally:
+        b.swiglu_mlp_set_debug_flags(0)
+    _, _, y_ref = oracle.fwd(x, W1, W2, residual=True)
+    parity(y, y_ref, "y (residual)")
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre_in, dy, residual=True)
+    parity(dx, dx_ref, "dx (residual)")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
+
+
+def test_residual_target_sampled(b):
+    # the full-size block (D == Dout) as a residual block, compared on sampled rows
+    s, x, W1, W2, dy = workloads.make_block("target")
+    preact_in = workloads.make_preact(s, workloads.CONFIGS["target"]["seed"])
+    xd, W1d, W2d, dyd, prd = dev(x), dev(W1), dev(W2), dev(dy), dev(preact_in)
+    _, y = b.swiglu_mlp_fwd(xd, W1d, W2d, residual=True)
+    dx, _, _ = b.swiglu_mlp_bwd(xd, W1d, W2d, prd, dyd, residual=True)
+    ok_status(b)
+    rows = _sample(s.M, 6, 3)
+    _, _, y_ref = oracle.fwd(x, W1, W2, rows=rows, residual=True)
+    parity(y[rows], y_ref, "y[rows] (residual)")
+    _, _, _, dx_ref = oracle.bwd_rows(W1, W2, preact_in, dy, rows=rows, residual=True)
+    parity(dx[rows], dx_ref, "dx[rows] (residual)")
+
+
+def test_residual_rejects_unequal_widths(b):
+    s = Shape(64, 128, 256, 192)
+    _, x, W1, W2, _ = workloads.make_block(s, seed=73)
+    with pytest.raises(RuntimeError, match="D == Dout"):
+        b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2), residual=True)
+
+
+def test_autograd_residual_block(b):
+    s = Shape(40, 64, 96, 64)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=74)
+    xg, w1g, w2g = (dev(t).requires_grad_(True) for t in (x, W1, W2))
+    y = b.swiglu_mlp(xg, w1g, w2g, residual=True)
+    y.backward(dev(dy))
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2, residual=True)
+    parity(y, y_ref, "y")
+    pre_gpu = torch.from_numpy(p_ref).to(torch.bfloat16)
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre_gpu, dy, residual=True)
+    parity(xg.grad, dx_ref, "dx")
+    parity(w1g.grad, dW1_ref, "dW1")
+    parity(w2g.grad, dW2_ref, "dW2")
