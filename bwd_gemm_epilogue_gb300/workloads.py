@@ -20,6 +20,22 @@ prefill/decode shapes; distributions: activations and dy ~ N(0, 1), weights
 The gate sweep of the tiny workload sets x[:, 0] = linspace(-20, 20, M) and
 makes W1's first gate row the unit vector e_0, so that preact[:, H] = x[:, 0]
 exactly and the sigmoid saturates at both ends.
+
+Mixture-of-experts workloads (tokens already grouped by expert; expert e owns
+rows [off_e, off_e + counts[e]); W1 [E, 2H, D], W2 [E, Dout, H]):
+
+  moe_tiny  E=4,  counts 32/120/8/64 (the per-expert token counts printed in
+            "Lesson 24: MLP, GEMM and operator fusion in the Transformer",
+            section 42), D=256, H=512, Dout=256                      seed 5
+  moe8      E=8,  T=16384 routed rows (8192 tokens, two experts each),
+            D=Dout=4096, H=14336 (Mixtral-8x7B expert shape)          seed 6
+  moe64     E=64, T=24576 routed rows (4096 tokens, six experts each),
+            D=Dout=2048, H=1408 (fine-grained experts), two experts
+            receive no tokens                                         seed 7
+
+Routed counts: expert probabilities uniform on the simplex (normalised
+exponential draws; the experts listed as empty get probability 0), T draws
+from them, counted per expert.
 """
 from __future__ import annotations
 
@@ -115,3 +131,33 @@ def make_stack(name: str = "stack4"):
     x, dy = make_activations(s, cfg["seed"])
     layers = [make_weights(s, 100 + l) for l in range(cfg["layers"])]
     return s, x, dy, layers
+
+
+MOE_CONFIGS = {
+    "moe_tiny": dict(E=4, counts=(32, 120, 8, 64), D=256, H=512, Dout=256, seed=5, empty=0),
+    "moe8": dict(E=8, T=16384, D=4096, H=14336, Dout=4096, seed=6, empty=0),
+    "moe64": dict(E=64, T=24576, D=2048, H=1408, Dout=2048, seed=7, empty=2),
+}
+_COUNTS = 5
+
+
+def moe_counts(T: int, E: int, seed: int, empty: int = 0) -> list:
+    """Per-expert row counts summing to T (see the module docstring); the last
+    `empty` experts receive none."""
+    g = _gen(seed, _COUNTS)
+    w = -torch.log(torch.rand(E, generator=g, dtype=torch.float64))
+    w[E - empty:] = 0.0
+    picks = torch.multinomial(w / w.sum(), T, replacement=True, generator=g)
+    return [int(v) for v in torch.bincount(picks, minlength=E)]
+
+
+def make_moe(name: str):
+    """counts, x [T, D], W1 [E, 2H, D], W2 [E, Dout, H], dy [T, Dout] for a named MoE workload."""
+    cfg = MOE_CONFIGS[name]
+    E, D, H, Dout, seed = cfg["E"], cfg["D"], cfg["H"], cfg["Dout"], cfg["seed"]
+    counts = list(cfg["counts"]) if "counts" in cfg else moe_counts(cfg["T"], E, seed, cfg["empty"])
+    s = Shape(sum(counts), D, H, Dout)
+    x, dy = make_activations(s, seed)
+    W1 = normal_bf16((E, 2 * H, D), D ** -0.5, seed, _W1)
+    W2 = normal_bf16((E, Dout, H), H ** -0.5, seed, _W2)
+    return counts, x, W1, W2, dy

@@ -18,8 +18,10 @@ Parity pins (tests/test_oracle.py): silu' against a central finite difference;
 the whole gradient chain against finite differences of L = sum(dy * y); the
 unrounded chain against torch fp64 autograd; bf16 rounding against torch's
 fp32->bf16 conversion and hand-worked ties; closed forms at g = 0, +-20;
-permutation weights, where every product reduces to a gather.  No function
-here is "parity unpinned".
+permutation weights, where every product reduces to a gather; for the
+mixture-of-experts functions, experts built as hidden-unit permutations and
+power-of-two scalings of one dense block, whose outputs are then known
+transforms of the dense block's.  No function here is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -206,3 +208,97 @@ def bwd_full(x, W1, W2, preact, dy, round_intermediates: bool = True, residual: 
     gh, gp, h, dx = bwd_rows(W1, W2, preact, dy, None, round_intermediates, residual)
     dW2c, dW1l, dW1g = bwd_cols(x, W2, preact, dy, None, round_intermediates)
     return gh, gp, h, dx, np.concatenate([dW1l, dW1g], axis=0), dW2c.T.copy()
+
+
+# ---------------------------------------------------------------------------- mixture of experts
+#
+# "Lesson 24: MLP, GEMM and operator fusion in the Transformer" (lincklin.cn), section 41
+# (each expert of an MoE layer is an MLP of its own; every token is routed to one
+# expert) and section 42 (the experts' GEMMs differ only in their row counts M_e).
+# Layout: the tokens arrive grouped by expert -- expert e owns rows
+# [off_e, off_e + counts[e]) of x, dy, preact, y and dx, with off_e the sum of the
+# counts before it -- and the weights are stacked per expert: W1 [E, 2H, D],
+# W2 [E, Dout, H].  Each expert's rows go through the block above with that
+# expert's weights; nothing else is computed.
+
+def expert_offsets(counts) -> np.ndarray:
+    """[E + 1] row offsets of the experts' segments."""
+    c = np.asarray(counts, dtype=np.int64)
+    if c.ndim != 1 or (c < 0).any():
+        raise ValueError("counts must be a 1-D array of non-negative ints")
+    return np.concatenate([[0], np.cumsum(c)])
+
+
+def _moe_shapes(W1, W2, counts):
+    w1b, w2b = _bits(W1), _bits(W2)
+    E, H2, D = w1b.shape
+    Dout, H = w2b.shape[1], w2b.shape[2]
+    off = expert_offsets(counts)
+    if w2b.shape[0] != E or H2 != 2 * H or off.size != E + 1:
+        raise ValueError("shape mismatch")
+    return w1b, w2b, off, E, D, H, Dout
+
+
+def moe_fwd(x, W1, W2, counts, round_intermediates: bool = True):
+    """Forward of every expert on its rows: (preact [T,2H], h [T,H], y [T,Dout])."""
+    xb = _bits(x)
+    w1b, w2b, off, E, D, H, Dout = _moe_shapes(W1, W2, counts)
+    T = xb.shape[0]
+    if off[-1] != T:
+        raise ValueError("counts do not sum to the number of rows")
+    preact, h, y = np.zeros((T, 2 * H)), np.zeros((T, H)), np.zeros((T, Dout))
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            preact[a:b], h[a:b], y[a:b] = fwd(xb[a:b], w1b[e], w2b[e], None, round_intermediates)
+    return preact, h, y
+
+
+def moe_bwd_full(x, W1, W2, preact, dy, counts, round_intermediates: bool = True):
+    """Backward of every expert on its rows:
+    (grad_h [T,H], grad_preact [T,2H], h [T,H], dx [T,D], dW1 [E,2H,D], dW2 [E,Dout,H]).
+    An expert that received no rows has zero weight gradients."""
+    xb, pb, dyb = _bits(x), _bits(preact), _bits(dy)
+    w1b, w2b, off, E, D, H, Dout = _moe_shapes(W1, W2, counts)
+    T = xb.shape[0]
+    if off[-1] != T:
+        raise ValueError("counts do not sum to the number of rows")
+    gh, gp, h, dx = np.zeros((T, H)), np.zeros((T, 2 * H)), np.zeros((T, H)), np.zeros((T, D))
+    dW1, dW2 = np.zeros((E, 2 * H, D)), np.zeros((E, Dout, H))
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            gh[a:b], gp[a:b], h[a:b], dx[a:b], dW1[e], dW2[e] = bwd_full(
+                xb[a:b], w1b[e], w2b[e], pb[a:b], dyb[a:b], round_intermediates)
+    return gh, gp, h, dx, dW1, dW2
+
+
+def moe_rows(x, W1, W2, preact, dy, counts, rows):
+    """Sampled token rows (global indices): (preact, y, grad_preact, h, dx) of those rows,
+    each computed by its own expert."""
+    xb, pb, dyb = _bits(x), _bits(preact), _bits(dy)
+    w1b, w2b, off, E, D, H, Dout = _moe_shapes(W1, W2, counts)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = [np.zeros((rows.size, n)) for n in (2 * H, Dout, 2 * H, H, D)]
+    for k, r in enumerate(rows):
+        e = int(np.searchsorted(off, r, side="right") - 1)
+        local = [r - off[e]]
+        seg = slice(off[e], off[e + 1])
+        p, _, yv = fwd(xb[seg], w1b[e], w2b[e], rows=local)
+        _, gpv, hv, dxv = bwd_rows(w1b[e], w2b[e], pb[seg], dyb[seg], rows=local)
+        for o, v in zip(out, (p, yv, gpv, hv, dxv)):
+            o[k] = v[0]
+    return tuple(out)
+
+
+def moe_cols(x, W2, preact, dy, counts, expert, cols):
+    """Expert `expert`'s weight gradients for the selected hidden indices, as bwd_cols."""
+    xb, pb, dyb = _bits(x), _bits(preact), _bits(dy)
+    w2b = _bits(W2)
+    off = expert_offsets(counts)
+    a, b = off[expert], off[expert + 1]
+    Dout, H = w2b.shape[1], w2b.shape[2]
+    n = len(cols)
+    if b == a:
+        return np.zeros((n, Dout)), np.zeros((n, xb.shape[1])), np.zeros((n, xb.shape[1]))
+    return bwd_cols(xb[a:b], w2b[expert], pb[a:b], dyb[a:b], cols=cols)

@@ -319,3 +319,95 @@ def test_residual_with_zero_down_projection_is_the_identity():
     _, gp, _, dx = oracle.bwd_rows(W1, W2, preact, dy, residual=True)
     assert not gp.any()                                   # grad_h = dy @ 0 = 0
     np.testing.assert_array_equal(dx, dy.double().numpy())
+
+
+# ----------------------------------------------------------------------------
+# mixture of experts: experts built from one dense block
+# ----------------------------------------------------------------------------
+
+def _expert_of(counts, t):
+    # the expert owning global row t, by walking the segments one by one
+    end = 0
+    for e, c in enumerate(counts):
+        end += c
+        if t < end:
+            return e
+    raise IndexError(t)
+
+
+def test_moe_experts_are_permuted_and_scaled_copies_of_one_block():
+    # Expert e gets W1[e] = the base W1 with its hidden units permuted by pi_e (the same
+    # permutation in the left and gate halves) and W2[e] = 2^e * base W2 with its columns
+    # permuted by pi_e.  Hidden-unit permutations leave an MLP's output unchanged and a
+    # power-of-two scale commutes with bf16 rounding, so for a token t of expert e:
+    #   preact_moe[t] = preact[t] with both halves permuted by pi_e,
+    #   y_moe[t] = 2^e y[t],  dx_moe[t] = 2^e dx[t]  (under dy),
+    # and summing the experts' gradients back through their permutations and scales gives
+    # the dense block's gradients over all tokens.  A wrong segment offset, a wrong
+    # expert's weights or a transposed slice breaks one of these.
+    E, D, H, Dout = 4, 24, 40, 16
+    counts = [9, 0, 14, 5]
+    T = sum(counts)
+    g = torch.Generator().manual_seed(77)
+    x = torch.randn(T, D, generator=g).to(torch.bfloat16)
+    dy = torch.randn(T, Dout, generator=g).to(torch.bfloat16)
+    W1 = (torch.randn(2 * H, D, generator=g) / D ** 0.5).to(torch.bfloat16)
+    W2 = (torch.randn(Dout, H, generator=g) / H ** 0.5).to(torch.bfloat16)
+    perms = [torch.randperm(H, generator=g) for _ in range(E)]
+    W1e = torch.stack([torch.cat([W1[:H][p], W1[H:][p]]) for p in perms])
+    W2e = torch.stack([W2[:, p] * 2.0 ** e for e, p in enumerate(perms)])
+
+    p_d, h_d, y_d = oracle.fwd(x, W1, W2)
+    p_m, h_m, y_m = oracle.moe_fwd(x, W1e, W2e, counts)
+    pre = torch.from_numpy(p_d).to(torch.bfloat16)
+    pre_m = torch.from_numpy(p_m).to(torch.bfloat16)
+    _, gp_d, _, dx_d, dW1_d, dW2_d = oracle.bwd_full(x, W1, W2, pre, dy)
+    _, gp_m, h2_m, dx_m, dW1_m, dW2_m = oracle.moe_bwd_full(x, W1e, W2e, pre_m, dy, counts)
+    for t in range(T):
+        e = _expert_of(counts, t)
+        p = perms[e].numpy()
+        np.testing.assert_array_equal(p_m[t, :H], p_d[t, :H][p])
+        np.testing.assert_array_equal(p_m[t, H:], p_d[t, H:][p])
+        np.testing.assert_array_equal(h_m[t], h_d[t][p])
+        np.testing.assert_array_equal(h2_m[t], h_d[t][p])
+        np.testing.assert_allclose(y_m[t], 2.0 ** e * y_d[t], rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(gp_m[t, :H], 2.0 ** e * gp_d[t, :H][p])
+        np.testing.assert_allclose(dx_m[t], 2.0 ** e * dx_d[t], rtol=1e-12, atol=1e-11)
+    dW1_sum = np.zeros_like(dW1_d)
+    dW2_sum = np.zeros_like(dW2_d)
+    for e, p in enumerate(perms):
+        p = p.numpy()
+        dW1_sum[p] += dW1_m[e][:H] / 2.0 ** e
+        dW1_sum[H + p] += dW1_m[e][H:] / 2.0 ** e
+        dW2_sum[:, p] += dW2_m[e]
+    np.testing.assert_allclose(dW1_sum, dW1_d, rtol=1e-12, atol=1e-11)
+    np.testing.assert_allclose(dW2_sum, dW2_d, rtol=1e-12, atol=1e-11)
+    assert not dW1_m[1].any() and not dW2_m[1].any()       # the expert with no tokens
+
+
+def test_moe_single_expert_is_the_dense_block_and_samples_agree():
+    s = workloads.Shape(21, 16, 24, 32)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=78)
+    p_d, _, y_d = oracle.fwd(x, W1, W2)
+    p_m, _, y_m = oracle.moe_fwd(x, W1[None], W2[None], [21])
+    np.testing.assert_array_equal(p_m, p_d)
+    np.testing.assert_array_equal(y_m, y_d)
+    # sampled rows / columns against the full computation, with three experts
+    counts = [8, 0, 13]
+    W1e = torch.stack([W1, W1.flip(0), -W1])
+    W2e = torch.stack([W2, W2.flip(1), W2 * 0.5])
+    pre = torch.from_numpy(oracle.moe_fwd(x, W1e, W2e, counts)[0]).to(torch.bfloat16)
+    full = oracle.moe_bwd_full(x, W1e, W2e, pre, dy, counts)
+    p_f, _, y_f = oracle.moe_fwd(x, W1e, W2e, counts)
+    rows = [0, 7, 8, 20]
+    p_r, y_r, gp_r, h_r, dx_r = oracle.moe_rows(x, W1e, W2e, pre, dy, counts, rows)
+    np.testing.assert_array_equal(p_r, p_f[rows])
+    np.testing.assert_array_equal(y_r, y_f[rows])
+    np.testing.assert_array_equal(gp_r, full[1][rows])
+    np.testing.assert_array_equal(dx_r, full[3][rows])
+    cols = [1, 23]
+    dW2c, dW1l, dW1g = oracle.moe_cols(x, W2e, pre, dy, counts, 2, cols)
+    np.testing.assert_array_equal(dW2c, full[5][2][:, cols].T)
+    np.testing.assert_array_equal(dW1l, full[4][2][cols])
+    np.testing.assert_array_equal(dW1g, full[4][2][[24 + c for c in cols]])
+    assert not oracle.moe_cols(x, W2e, pre, dy, counts, 1, cols)[1].any()
