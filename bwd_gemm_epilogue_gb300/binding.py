@@ -1,4 +1,5 @@
-"""ctypes binding of the C ABI in ``include/swiglu_mlp.h`` -- argument marshalling only.
+"""ctypes binding of the C ABI in ``include/swiglu_mlp.h`` and ``include/swiglu_moe.h``
+-- argument marshalling only.
 
 Each function has the name of the C entry point it calls and takes torch CUDA
 tensors (bf16, contiguous) for the pointer arguments; torch supplies device
@@ -29,7 +30,7 @@ STATUS_NAMES = {
     7: "SWIGLU_ERR_CUDA",
 }
 
-# Every symbol include/swiglu_mlp.h declares: name -> (restype, argtypes)
+# Every symbol include/swiglu_mlp.h and include/swiglu_moe.h declare: name -> (restype, argtypes)
 _vp, _i64, _i32, _u64, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
 SIGNATURES = {
     "swiglu_mlp_fwd_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
@@ -49,6 +50,11 @@ SIGNATURES = {
     "swiglu_mlp_trace_begin": (None, [_vp, _vp, _i32]),
     "swiglu_mlp_trace_end": (_i32, []),
     "swiglu_mlp_abi_version": (_i32, []),
+    "swiglu_moe_fwd_workspace_size": (_sz, [_vp, _i64, _i64, _i64, _i64]),
+    "swiglu_moe_bwd_workspace_size": (_sz, [_vp, _i64, _i64, _i64, _i64]),
+    "swiglu_moe_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "swiglu_moe_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz,
+                              _vp]),
 }
 
 KERNEL_KINDS = {1: "fwd_preact", 2: "fwd_down", 3: "bwd_grad_h", 4: "bwd_dW2", 5: "bwd_dx", 6: "bwd_dW1", 7: "gemm",
@@ -292,3 +298,67 @@ class SwiGLUMLP(torch.autograd.Function):
 
 def swiglu_mlp(x, W1, W2, residual: bool = False):
     return SwiGLUMLP.apply(x, W1, W2, residual)
+
+
+# ---------------------------------------------------------------------------- mixture of experts
+
+def _counts(counts):
+    """Host int64 array of the per-expert row counts (kept alive by the caller's frame)."""
+    vals = [int(v) for v in (counts.tolist() if hasattr(counts, "tolist") else counts)]
+    return (ctypes.c_int64 * len(vals))(*vals), len(vals), sum(vals)
+
+
+def _moe_dims(x, W1, W2):
+    T, D = x.shape
+    E, H2, D1 = W1.shape
+    E2, Dout, H = W2.shape
+    if D1 != D or H2 != 2 * H or E2 != E:
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)}, W1 {tuple(W1.shape)}, W2 {tuple(W2.shape)}")
+    return T, E, D, H, Dout
+
+
+def swiglu_moe_fwd_workspace_size(counts, D: int, H: int, Dout: int) -> int:
+    arr, E, _ = _counts(counts)
+    return int(lib().swiglu_moe_fwd_workspace_size(ctypes.cast(arr, _vp), E, D, H, Dout))
+
+
+def swiglu_moe_bwd_workspace_size(counts, D: int, H: int, Dout: int) -> int:
+    arr, E, _ = _counts(counts)
+    return int(lib().swiglu_moe_bwd_workspace_size(ctypes.cast(arr, _vp), E, D, H, Dout))
+
+
+def swiglu_moe_fwd(x, W1, W2, counts, preact=None, y=None, workspace=None):
+    """Forward of every expert on its rows (x grouped by expert, counts per expert);
+    returns (preact [T,2H], y [T,Dout])."""
+    T, E, D, H, Dout = _moe_dims(x, W1, W2)
+    arr, En, total = _counts(counts)
+    if En != E or total != T:
+        raise ValueError(f"counts: {En} experts summing to {total}, expected {E} and {T}")
+    preact = _empty((T, 2 * H), x) if preact is None else preact
+    y = _empty((T, Dout), x) if y is None else y
+    if workspace is None:
+        workspace = torch.empty(max(16, swiglu_moe_fwd_workspace_size(counts, D, H, Dout)), dtype=torch.uint8,
+                                device=x.device)
+    st = lib().swiglu_moe_fwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), ctypes.cast(arr, _vp), E, D, H,
+                              Dout, _ptr(workspace), workspace.numel(), _stream(x.device))
+    _check(st, "swiglu_moe_fwd")
+    return preact, y
+
+
+def swiglu_moe_bwd(x, W1, W2, preact, dy, counts, dx=None, dW1=None, dW2=None, workspace=None):
+    """Backward of every expert on its rows; returns (dx [T,D], dW1 [E,2H,D], dW2 [E,Dout,H])."""
+    T, E, D, H, Dout = _moe_dims(x, W1, W2)
+    arr, En, total = _counts(counts)
+    if En != E or total != T:
+        raise ValueError(f"counts: {En} experts summing to {total}, expected {E} and {T}")
+    dx = _empty((T, D), x) if dx is None else dx
+    dW1 = _empty((E, 2 * H, D), x) if dW1 is None else dW1
+    dW2 = _empty((E, Dout, H), x) if dW2 is None else dW2
+    if workspace is None:
+        workspace = torch.empty(max(16, swiglu_moe_bwd_workspace_size(counts, D, H, Dout)), dtype=torch.uint8,
+                                device=x.device)
+    st = lib().swiglu_moe_bwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dW1),
+                              _ptr(dW2), ctypes.cast(arr, _vp), E, D, H, Dout, _ptr(workspace),
+                              workspace.numel(), _stream(x.device))
+    _check(st, "swiglu_moe_bwd")
+    return dx, dW1, dW2

@@ -52,6 +52,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cstddef>
 #include <cstdint>
 #include <type_traits>
 
@@ -111,6 +112,33 @@ struct ScheduledArgs : KernelArgs {
     uint16_t sched[MAX_SCHED];
 };
 static_assert(sizeof(ScheduledArgs) <= 32764, "kernel parameter block limit");
+
+// Where a launch finds its problems and tile order:
+//   SRC_SINGLE  one problem in the parameter block, tiles round robin over the clusters;
+//   SRC_PARAMS  up to MAX_PROBLEMS problems and a host tile list in the parameter block;
+//   SRC_TABLE   any number of problems (the experts of an MoE layer, each with its own
+//               row count) in a table in global memory, written by the host before the
+//               launch, with the host tile list beside it.  Cluster c runs the entries
+//               sched[sched_off[c] .. sched_off[c + 1]), each problem << 20 | tile.
+constexpr int SRC_SINGLE = 0, SRC_PARAMS = 1, SRC_TABLE = 2;
+constexpr int TABLE_TILE_BITS = 20;
+struct alignas(128) TableEntry {
+    CUtensorMap a, b, o0;
+    CUtensorMap o1, i0;   // as in KernelArgs, per problem
+    Problem prob;
+};
+static_assert(sizeof(TableEntry) % 128 == 0 && offsetof(TableEntry, i0) % 64 == 0,
+              "tensor maps in the table stay 64-byte aligned");
+struct TableArgs {
+    const TableEntry* table;
+    const int* sched_off;
+    const int* sched;
+    int num_problems;
+    int num_tiles;
+    unsigned long long timeout_ns;
+    int* err;
+    int debug_flags;
+};
 
 template <int EPI, int CG>
 struct Cfg {
@@ -213,20 +241,59 @@ __device__ __forceinline__ const T* pick3(int pi, const T* p0, const T* p1, cons
 }
 
 // The tiles of cluster c: round robin over the launch, or the host's list.
-template <bool SCHED, class Args>
+template <int SRC, class Args>
 __device__ __forceinline__ int tiles_first(const Args& a, int c) {
-    if constexpr (SCHED) return a.sched_off[c];
+    if constexpr (SRC != SRC_SINGLE) return a.sched_off[c];
     else return c;
 }
-template <bool SCHED, class Args>
+template <int SRC, class Args>
 __device__ __forceinline__ int tiles_end(const Args& a, int c) {
-    if constexpr (SCHED) return a.sched_off[c + 1];
+    if constexpr (SRC != SRC_SINGLE) return a.sched_off[c + 1];
     else return a.num_tiles;
 }
-template <bool SCHED, class Args>
-__device__ __forceinline__ int tile_at(const Args& a, int i) {
-    if constexpr (SCHED) return a.sched[i];
-    else return i;
+
+// The problem of the launch's it-th tile (of this cluster's list), its index pi and
+// the tile's index lt within the problem.  Returned by value: the callers' asm
+// statements clobber memory, and parameter or table fields would be reloaded.
+template <int SRC, class Args>
+__device__ __forceinline__ Problem problem_at(const Args& a, int it, int& pi, int& lt) {
+    if constexpr (SRC == SRC_TABLE) {
+        const int v = __ldg(a.sched + it);
+        pi = v >> TABLE_TILE_BITS;
+        lt = v & ((1 << TABLE_TILE_BITS) - 1);
+        return a.table[pi].prob;
+    } else if constexpr (SRC == SRC_PARAMS) {
+        const int t = a.sched[it];
+        pi = problem_of(a, t);
+        const Problem pr = *pick3(pi, &a.prob[0], &a.prob[1], &a.prob[2]);
+        lt = t - pr.tile_begin;
+        return pr;
+    } else {
+        pi = 0;
+        lt = it;
+        return a.prob[0];
+    }
+}
+
+enum MapId { MAP_A, MAP_B, MAP_O0, MAP_O1, MAP_I0 };
+template <int SRC, int WHICH, class Args>
+__device__ __forceinline__ const CUtensorMap* map_of(const Args& a, int pi) {
+    if constexpr (SRC == SRC_TABLE) {
+        const TableEntry* e = a.table + pi;
+        if constexpr (WHICH == MAP_A) return &e->a;
+        else if constexpr (WHICH == MAP_B) return &e->b;
+        else if constexpr (WHICH == MAP_O0) return &e->o0;
+        else if constexpr (WHICH == MAP_O1) return &e->o1;
+        else return &e->i0;
+    } else {
+        if constexpr (WHICH == MAP_O1) return &a.o1;
+        else if constexpr (WHICH == MAP_I0) return &a.i0;
+        else {
+            const CUtensorMap* m = WHICH == MAP_A ? a.a : (WHICH == MAP_B ? a.b : a.o0);
+            if constexpr (SRC == SRC_PARAMS) return pick3(pi, &m[0], &m[1], &m[2]);
+            else return &m[0];
+        }
+    }
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (after recording `role` in the
@@ -298,10 +365,12 @@ __device__ __forceinline__ uint32_t sw64_offset(int r, int c) {
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int EPI, int CG, bool SCHED>
-using ArgsOf = typename std::conditional<SCHED, ScheduledArgs, KernelArgs>::type;
+template <int EPI, int CG, int SCHED>
+using ArgsOf = typename std::conditional<
+    SCHED == SRC_TABLE, TableArgs,
+    typename std::conditional<SCHED == SRC_PARAMS, ScheduledArgs, KernelArgs>::type>::type;
 
-template <int EPI, int CG, bool SCHED>
+template <int EPI, int CG, int SCHED>
 __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     gemm_kernel(const __grid_constant__ ArgsOf<EPI, CG, SCHED> args) {
     using C = Cfg<EPI, CG>;
@@ -349,16 +418,18 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
+        if constexpr (SCHED != SRC_TABLE) {
 #pragma unroll
-        for (int q = 0; q < MAX_PROBLEMS; ++q) {
-            if (q < args.num_problems) {
-                ptx::prefetch_tmap(&args.a[q]);
-                ptx::prefetch_tmap(&args.b[q]);
-                ptx::prefetch_tmap(&args.o0[q]);
+            for (int q = 0; q < MAX_PROBLEMS; ++q) {
+                if (q < args.num_problems) {
+                    ptx::prefetch_tmap(&args.a[q]);
+                    ptx::prefetch_tmap(&args.b[q]);
+                    ptx::prefetch_tmap(&args.o0[q]);
+                }
             }
+            if (!C::STORE_ONLY) ptx::prefetch_tmap(&args.o1);
+            if (EPI == EPI_SWIGLU_BWD || EPI == EPI_STORE_ADD) ptx::prefetch_tmap(&args.i0);
         }
-        if (!C::STORE_ONLY) ptx::prefetch_tmap(&args.o1);
-        if (EPI == EPI_SWIGLU_BWD || EPI == EPI_STORE_ADD) ptx::prefetch_tmap(&args.i0);
     }
     if (warp == 1) {
         if (CG == 2) {
@@ -385,17 +456,22 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
 #pragma unroll
             for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
             bool ok = true;
+            int seen_pi = -1;
             for (int it = t_first; it < t_end && ok; it += t_step) {
-                const int t = tile_at<SCHED>(args, it);
-                const int pi = SCHED ? problem_of(args, t) : 0;
-                const CUtensorMap* mA = SCHED ? pick3(pi, &args.a[0], &args.a[1], &args.a[2]) : &args.a[0];
-                const CUtensorMap* mB = SCHED ? pick3(pi, &args.b[0], &args.b[1], &args.b[2]) : &args.b[0];
+                int pi, lt;
                 // per-tile fields in registers: the asm statements below clobber memory
-                const Problem pr = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
+                const Problem pr = problem_at<SCHED>(args, it, pi, lt);
+                const CUtensorMap* mA = map_of<SCHED, MAP_A>(args, pi);
+                const CUtensorMap* mB = map_of<SCHED, MAP_B>(args, pi);
+                if (SCHED == SRC_TABLE && pi != seen_pi) {
+                    ptx::tmap_acquire(mA);
+                    ptx::tmap_acquire(mB);
+                    seen_pi = pi;
+                }
                 const int k_blocks = pr.k_blocks;
                 const bool a_mn = pr.a_mn != 0, b_mn = pr.b_mn != 0;
                 int tm, tn;
-                tile_coords(pr, t - pr.tile_begin, tm, tn);
+                tile_coords(pr, lt, tm, tn);
                 const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
@@ -461,8 +537,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             bool ok = true;
             int local = 0;
             for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
-                const int pi = SCHED ? problem_of(args, tile_at<SCHED>(args, it)) : 0;
-                const Problem& pq = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
+                int pi, lt;
+                const Problem pq = problem_at<SCHED>(args, it, pi, lt);
                 const int k_blocks = pq.k_blocks;
                 const bool a_mn = pq.a_mn != 0, b_mn = pq.b_mn != 0;
                 const uint32_t idesc = umma_idesc(a_mn, b_mn, CG);
@@ -525,11 +601,16 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
             for (int s = 0; s < C::EIN_SLOTS; ++s) last_parity[s] = -1;
             bool ok = true;
+            int seen_pi = -1;
             for (int it = t_first; it < t_end && ok; it += t_step) {
-                const int t = tile_at<SCHED>(args, it);
-                int tm, tn;
-                const Problem pr0 = args.prob[0];
-                tile_coords(pr0, t, tm, tn);
+                int pi, lt, tm, tn;
+                const Problem pr0 = problem_at<SCHED>(args, it, pi, lt);
+                tile_coords(pr0, lt, tm, tn);
+                const CUtensorMap* mI = map_of<SCHED, MAP_I0>(args, pi);
+                if (SCHED == SRC_TABLE && pi != seen_pi) {
+                    ptx::tmap_acquire(mI);
+                    seen_pi = pi;
+                }
                 const int m0 = tm * (BM * CG) + BM * (int)rank;
                 const int j0 = tn * BN;
                 for (int c = 0; c < C::CHUNKS; ++c) {
@@ -541,8 +622,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
                     last_parity[slot] = (int)phase;
                     const uint32_t dst = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
-                    ptx::tma_load_3d(dst, &args.i0, fb, j0 + c * CHUNK, 0, m0);
-                    ptx::tma_load_3d(dst + C::EIN_HALF, &args.i0, fb, j0 + c * CHUNK, 1, m0);
+                    ptx::tma_load_3d(dst, mI, fb, j0 + c * CHUNK, 0, m0);
+                    ptx::tma_load_3d(dst + C::EIN_HALF, mI, fb, j0 + c * CHUNK, 1, m0);
                     if (++slot == C::EIN_SLOTS) {
                         slot = 0;
                         phase ^= 1u;
@@ -562,13 +643,18 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
             for (int s = 0; s < C::EIN_SLOTS; ++s) last_parity[s] = -1;
             bool ok = true;
+            int seen_pi = -1;
             for (int it = t_first; it < t_end && ok; it += t_step) {
-                const int t = tile_at<SCHED>(args, it);
-                const int pi = SCHED ? problem_of(args, t) : 0;
-                const Problem pr = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
+                int pi, lt;
+                const Problem pr = problem_at<SCHED>(args, it, pi, lt);
                 if (!pr.res) continue;
+                const CUtensorMap* mI = map_of<SCHED, MAP_I0>(args, pi);
+                if (SCHED == SRC_TABLE && pi != seen_pi) {
+                    ptx::tmap_acquire(mI);
+                    seen_pi = pi;
+                }
                 int tm, tn;
-                tile_coords(pr, t - pr.tile_begin, tm, tn);
+                tile_coords(pr, lt, tm, tn);
                 const int m0 = tm * (BM * CG) + BM * (int)rank;
                 const int n0 = tn * BN;
                 for (int c = 0; c < C::CHUNKS; ++c) {
@@ -579,7 +665,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     const uint32_t fb = ein_full_bar(slot);
                     ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
                     last_parity[slot] = (int)phase;
-                    ptx::tma_load_2d(base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES, &args.i0, fb, n0 + c * CHUNK, m0);
+                    ptx::tma_load_2d(base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES, mI, fb, n0 + c * CHUNK, m0);
                     if (++slot == C::EIN_SLOTS) {
                         slot = 0;
                         phase ^= 1u;
@@ -605,15 +691,21 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         int ob = 0;
         int local = 0;
         bool ok = true;
+        int seen_pi = -1;
         for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
-            const int t = tile_at<SCHED>(args, it);
-            const int pi = SCHED ? problem_of(args, t) : 0;
+            int pi, lt;
             // registers (asm statements clobber memory)
-            const Problem pr = SCHED ? *pick3(pi, &args.prob[0], &args.prob[1], &args.prob[2]) : args.prob[0];
+            const Problem pr = problem_at<SCHED>(args, it, pi, lt);
             const int n_limit = pr.N;
-            const CUtensorMap* mO0 = SCHED ? pick3(pi, &args.o0[0], &args.o0[1], &args.o0[2]) : &args.o0[0];
+            const CUtensorMap* mO0 = map_of<SCHED, MAP_O0>(args, pi);
+            const CUtensorMap* mO1 = map_of<SCHED, MAP_O1>(args, pi);
+            if (SCHED == SRC_TABLE && pi != seen_pi && lane == 0) {
+                ptx::tmap_acquire(mO0);
+                if (!C::STORE_ONLY) ptx::tmap_acquire(mO1);
+            }
+            seen_pi = pi;
             int tm, tn;
-            tile_coords(pr, t - pr.tile_begin, tm, tn);
+            tile_coords(pr, lt, tm, tn);
             const int m0 = tm * (BM * CG) + BM * (int)rank;
             const int mrow0 = m0 + 32 * wq;     // first output row of this warp's slice
             const bool rows_live = mrow0 < pr.M;
@@ -771,7 +863,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         if (j < n_limit) {
                             ptx::tma_store_3d(mO0, ob_base, j, 0, mrow0);
                             ptx::tma_store_3d(mO0, ob_base + C::OUT_TILE, j, 1, mrow0);
-                            ptx::tma_store_2d(&args.o1, ob_base + 2 * C::OUT_TILE, j, mrow0);
+                            ptx::tma_store_2d(mO1, ob_base + 2 * C::OUT_TILE, j, mrow0);
                         }
                     }
                 }

@@ -18,6 +18,7 @@
 #include "gemm_kernel.cuh"
 #include "skinny_kernel.cuh"
 #include "swiglu_mlp.h"
+#include "swiglu_moe.h"
 
 namespace swiglu {
 namespace {
@@ -195,33 +196,54 @@ bool build_schedule(ScheduledArgs& a, int units) {
     return true;
 }
 
-// Launch one persistent grid over args' problems.  args' tensor maps and problems
-// are filled in by the caller; this sets the common fields and the grid.
-template <int EPI, int CG, bool SCHED>
-swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cudaStream_t stream) {
+// Persistent CTAs (CG == 1) or CTA pairs (CG == 2) of this kernel that fit on the
+// device at once; 0 on failure.
+template <int EPI, int CG, int SCHED>
+int cluster_slots(DeviceState* st) {
+    if (CG == 1) return st->num_sms;
+    static int max_clusters[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (max_clusters[dev] <= 0) {
+        auto kern = gemm_kernel<EPI, CG, SCHED>;
+        constexpr int smem = Cfg<EPI, CG>::SMEM_BYTES;
+        // the occupancy query sees the kernel's dynamic shared memory limit
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.blockDim = dim3(Cfg<EPI, CG>::THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.gridDim = dim3(2 * (st->num_sms / 2));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return 0;
+        max_clusters[dev] = n;
+    }
+    return max_clusters[dev];
+}
+
+// Launch `units` persistent clusters of the kernel over args (fields all filled in),
+// bracketed by the launch trace's events when one is open.
+template <int EPI, int CG, int SCHED>
+swiglu_status launch_grid(DeviceState* st, int kind, const ArgsOf<EPI, CG, SCHED>& args, int units,
+                          cudaStream_t stream) {
+    (void)st;
     auto kern = gemm_kernel<EPI, CG, SCHED>;
     constexpr int smem = Cfg<EPI, CG>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem)", e);
-    int tiles = 0;
-    for (int q = 0; q < args.num_problems; ++q) {
-        args.prob[q].tile_begin = tiles;
-        tiles += args.prob[q].tiles_m * args.prob[q].tiles_n;
-    }
-    args.num_tiles = tiles;
-    args.timeout_ns = g_timeout_ns.load();
-    args.err = st->err_word;
-    args.debug_flags = g_debug_flags.load();
-
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(Cfg<EPI, CG>::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
-    int slots = st->num_sms;   // persistent CTAs (CG == 1) or CTA pairs (CG == 2) that fit at once
     if (CG == 2) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -229,21 +251,6 @@ swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cu
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        static int max_clusters[kMaxDevices];
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (max_clusters[dev] <= 0) {
-            cfg.gridDim = dim3(2 * (st->num_sms / 2));
-            int n = 0;
-            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-            if (e != cudaSuccess || n <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters", e);
-            max_clusters[dev] = n;
-        }
-        slots = max_clusters[dev];
-    }
-    const int units = tiles < slots ? tiles : slots;
-    if constexpr (SCHED) {
-        if (!build_schedule(args, units)) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "tile schedule too large");
     }
     cfg.gridDim = dim3(units * CG);
     Trace& tr = g_trace;
@@ -261,6 +268,30 @@ swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cu
         if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventRecord(trace)", e);
     }
     return SWIGLU_OK;
+}
+
+// Launch one persistent grid over args' problems (parameter-block sources).  args'
+// tensor maps and problems are filled in by the caller; this sets the common
+// fields, the host schedule and the grid.
+template <int EPI, int CG, int SCHED>
+swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cudaStream_t stream) {
+    static_assert(SCHED != SRC_TABLE, "table launches go through launch_table");
+    int tiles = 0;
+    for (int q = 0; q < args.num_problems; ++q) {
+        args.prob[q].tile_begin = tiles;
+        tiles += args.prob[q].tiles_m * args.prob[q].tiles_n;
+    }
+    args.num_tiles = tiles;
+    args.timeout_ns = g_timeout_ns.load();
+    args.err = st->err_word;
+    args.debug_flags = g_debug_flags.load();
+    const int slots = cluster_slots<EPI, CG, SCHED>(st);
+    if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
+    const int units = tiles < slots ? tiles : slots;
+    if constexpr (SCHED == SRC_PARAMS) {
+        if (!build_schedule(args, units)) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "tile schedule too large");
+    }
+    return launch_grid<EPI, CG, SCHED>(st, kind, args, units, stream);
 }
 
 // ---------------------------------------------------------------- small-M (decode) path
@@ -436,8 +467,8 @@ swiglu_status run_fwd_preact(DeviceState* st, const void* x, const void* W1, voi
     if (!encode_out_2d(&a.o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
     a.num_problems = 1;
     a.prob[0] = make_problem(M, H, D, (H + BN / 2 - 1) / (BN / 2), false, false, cg);
-    if (cg == 2) return launch<EPI_SWIGLU_FWD, 2, false>(st, SWIGLU_KERNEL_FWD_PREACT, a, s);
-    return launch<EPI_SWIGLU_FWD, 1, false>(st, SWIGLU_KERNEL_FWD_PREACT, a, s);
+    if (cg == 2) return launch<EPI_SWIGLU_FWD, 2, SRC_SINGLE>(st, SWIGLU_KERNEL_FWD_PREACT, a, s);
+    return launch<EPI_SWIGLU_FWD, 1, SRC_SINGLE>(st, SWIGLU_KERNEL_FWD_PREACT, a, s);
 }
 
 // grad_h = dy @ W2 fused with the SwiGLU backward (writes grad_preact and h).
@@ -454,8 +485,8 @@ swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, con
     if (!encode_paired(&a.i0, preact, M, H, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
     a.num_problems = 1;
     a.prob[0] = make_problem(M, H, Dout, (H + BN - 1) / BN, false, true, cg);
-    if (cg == 2) return launch<EPI_SWIGLU_BWD, 2, false>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
-    return launch<EPI_SWIGLU_BWD, 1, false>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
+    if (cg == 2) return launch<EPI_SWIGLU_BWD, 2, SRC_SINGLE>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
+    return launch<EPI_SWIGLU_BWD, 1, SRC_SINGLE>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
 }
 
 struct GemmSpec {
@@ -493,11 +524,11 @@ swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, 
     if (!add_problem(a, 0, g, cg)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
     a.num_problems = 1;
     if (R) {
-        if (cg == 2) return launch<EPI_STORE_ADD, 2, false>(st, kind, a, s);
-        return launch<EPI_STORE_ADD, 1, false>(st, kind, a, s);
+        if (cg == 2) return launch<EPI_STORE_ADD, 2, SRC_SINGLE>(st, kind, a, s);
+        return launch<EPI_STORE_ADD, 1, SRC_SINGLE>(st, kind, a, s);
     }
-    if (cg == 2) return launch<EPI_STORE, 2, false>(st, kind, a, s);
-    return launch<EPI_STORE, 1, false>(st, kind, a, s);
+    if (cg == 2) return launch<EPI_STORE, 2, SRC_SINGLE>(st, kind, a, s);
+    return launch<EPI_STORE, 1, SRC_SINGLE>(st, kind, a, s);
 }
 
 // Several independent plain GEMMs in one persistent launch, tiles balanced across
@@ -513,8 +544,8 @@ swiglu_status run_gemm_group(DeviceState* st, int kind, const GemmSpec* g, int n
         if (!add_problem(a, q, g[q], 2)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (group)");
     }
     a.num_problems = n;
-    if (res) return launch<EPI_STORE_ADD, 2, true>(st, kind, a, s);
-    return launch<EPI_STORE, 2, true>(st, kind, a, s);
+    if (res) return launch<EPI_STORE_ADD, 2, SRC_PARAMS>(st, kind, a, s);
+    return launch<EPI_STORE, 2, SRC_PARAMS>(st, kind, a, s);
 }
 
 }  // namespace
@@ -824,3 +855,387 @@ extern "C" swiglu_status swiglu_mlp_fwd_noalloc(const void* x, const void* W1, c
     if (rc != SWIGLU_OK) return rc;
     return run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h, W2, y, M, Dout, H, false, false, s);
 }
+
+// ---------------------------------------------------------------------------
+// Mixture of experts ("Lesson 24: MLP, GEMM and operator fusion in the
+// Transformer", sections 41-43): every expert is a SwiGLU block of its own and
+// receives its own number of tokens.  Each step of the block runs as ONE
+// persistent launch over all experts' GEMMs (a grouped GEMM): the launch reads a
+// table of problems -- per expert its tensor maps, clipped to that expert's
+// rows, and sizes -- from global memory, and the clusters walk a host tile list
+// that balances the experts' tiles longest-first.
+// ---------------------------------------------------------------------------
+namespace swiglu {
+namespace {
+
+constexpr int kMaxUnits = 1024;          // bound on the clusters of one launch (table sizing)
+constexpr int kStageSlots = 8;
+
+// Pinned host slots the problem tables are copied from (a pageable source could
+// make cudaMemcpyAsync wait for the stream).  A slot is refilled only after the
+// copy enqueued from it kStageSlots tables earlier has completed.
+struct Staging {
+    uint8_t* host = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;
+};
+std::mutex g_stage_mutex;
+Staging g_stage[kMaxDevices][kStageSlots];
+int g_stage_next[kMaxDevices];
+
+swiglu_status stage_copy(void* dst, const std::vector<uint8_t>& img, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaGetDevice", e);
+    std::lock_guard<std::mutex> lock(g_stage_mutex);
+    Staging& sl = g_stage[dev][g_stage_next[dev]];
+    g_stage_next[dev] = (g_stage_next[dev] + 1) % kStageSlots;
+    if (sl.done) {
+        e = cudaEventSynchronize(sl.done);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventSynchronize(table staging)", e);
+    } else {
+        e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventCreate(table staging)", e);
+    }
+    if (sl.cap < img.size()) {
+        if (sl.host) cudaFreeHost(sl.host);
+        sl.host = nullptr;
+        sl.cap = 0;
+        const size_t cap = std::max(img.size(), size_t(1) << 18);
+        e = cudaHostAlloc(reinterpret_cast<void**>(&sl.host), cap, cudaHostAllocDefault);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaHostAlloc(table staging)", e);
+        sl.cap = cap;
+    }
+    std::memcpy(sl.host, img.data(), img.size());
+    e = cudaMemcpyAsync(dst, sl.host, img.size(), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemcpyAsync(problem table)", e);
+    e = cudaEventRecord(sl.done, s);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaEventRecord(table staging)", e);
+    return SWIGLU_OK;
+}
+
+// Device bytes of one launch's table: entries, cluster offsets, tile list, and
+// slack to start the entries on a 256-byte boundary (tensor maps in global memory
+// must be 64-byte aligned; the workspace is only 16-byte aligned).
+size_t table_bytes(size_t entries, size_t tiles) {
+    return 256 + round256(entries * sizeof(TableEntry)) + round256((kMaxUnits + 1) * sizeof(int)) +
+           round256(tiles * sizeof(int));
+}
+
+// One launch over the problems in `ents` (tensor maps and problems filled in),
+// its table written to dev_table (dev_bytes available) in stream order.
+template <int EPI, int CG>
+swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& ents, void* dev_table,
+                           size_t dev_bytes, cudaStream_t s) {
+    const int n = (int)ents.size();
+    if (n == 0) return SWIGLU_OK;
+    if (n >= (1 << (31 - TABLE_TILE_BITS))) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "too many problems");
+    long long tiles = 0;
+    for (TableEntry& e : ents) {
+        const long long t = (long long)e.prob.tiles_m * e.prob.tiles_n;
+        if (t >= (1 << TABLE_TILE_BITS)) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "too many tiles in one problem");
+        e.prob.tile_begin = (int)tiles;
+        tiles += t;
+    }
+    if (tiles == 0) return SWIGLU_OK;
+    if (table_bytes((size_t)n, (size_t)tiles) > dev_bytes) return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "problem table");
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(dev_table);
+    dev_table = reinterpret_cast<void*>((raw + 255) & ~uintptr_t(255));
+    const int slots = cluster_slots<EPI, CG, SRC_TABLE>(st);
+    if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
+    const int units = (int)std::min<long long>(tiles, std::min(slots, kMaxUnits));
+
+    // longest-processing-time: problems by decreasing k-blocks, each tile to the
+    // least-loaded cluster (a tile costs its k-blocks plus one for its epilogue)
+    std::vector<int> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int a, int b) { return ents[a].prob.k_blocks > ents[b].prob.k_blocks; });
+    std::vector<std::vector<int>> lists(units);
+    using Slot = std::pair<long long, int>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int u = 0; u < units; ++u) heap.push({0, u});
+    for (int pi : order) {
+        const Problem& p = ents[pi].prob;
+        const int nt = p.tiles_m * p.tiles_n;
+        for (int t = 0; t < nt; ++t) {
+            Slot sl = heap.top();
+            heap.pop();
+            lists[sl.second].push_back((pi << TABLE_TILE_BITS) | t);
+            heap.push({sl.first + p.k_blocks + 1, sl.second});
+        }
+    }
+    const size_t off_sched_off = round256((size_t)n * sizeof(TableEntry));
+    const size_t off_sched = off_sched_off + round256((kMaxUnits + 1) * sizeof(int));
+    std::vector<uint8_t> img(off_sched + (size_t)tiles * sizeof(int));
+    std::memcpy(img.data(), ents.data(), (size_t)n * sizeof(TableEntry));
+    int* so = reinterpret_cast<int*>(img.data() + off_sched_off);
+    int* sc = reinterpret_cast<int*>(img.data() + off_sched);
+    int pos = 0;
+    for (int u = 0; u < units; ++u) {
+        so[u] = pos;
+        for (int v : lists[u]) sc[pos++] = v;
+    }
+    so[units] = pos;
+    swiglu_status rc = stage_copy(dev_table, img, s);
+    if (rc != SWIGLU_OK) return rc;
+
+    TableArgs a;
+    std::memset(&a, 0, sizeof a);
+    uint8_t* d = static_cast<uint8_t*>(dev_table);
+    a.table = reinterpret_cast<const TableEntry*>(d);
+    a.sched_off = reinterpret_cast<const int*>(d + off_sched_off);
+    a.sched = reinterpret_cast<const int*>(d + off_sched);
+    a.num_problems = n;
+    a.num_tiles = (int)tiles;
+    a.timeout_ns = g_timeout_ns.load();
+    a.err = st->err_word;
+    a.debug_flags = g_debug_flags.load();
+    return launch_grid<EPI, CG, SRC_TABLE>(st, kind, a, units, s);
+}
+
+// Expert segments: off[e] .. off[e + 1] are expert e's rows.
+bool moe_offsets(const int64_t* counts, int64_t E, std::vector<int64_t>& off) {
+    if (!counts || E <= 0 || E > 682) return false;   // 3E problems of one launch fit the table's index bits
+    off.assign((size_t)E + 1, 0);
+    for (int64_t e = 0; e < E; ++e) {
+        if (counts[e] < 0 || counts[e] >= (int64_t(1) << 31)) return false;
+        off[e + 1] = off[e] + counts[e];
+    }
+    return off[E] < (int64_t(1) << 31);
+}
+
+// Row tiles of one expert: 256-row CTA-pair tiles unless they would waste more
+// than 15 % of the rows computed, in padding, over all experts (many small experts).
+int moe_pick_cg(const std::vector<int64_t>& off) {
+    if (g_debug_flags.load() & DEBUG_FORCE_SINGLE_CTA) return 1;
+    long long pad2 = 0, pad1 = 0;
+    for (size_t e = 0; e + 1 < off.size(); ++e) {
+        const long long m = off[e + 1] - off[e];
+        pad2 += (m + 2 * BM - 1) / (2 * BM) * (2 * BM);
+        pad1 += (m + BM - 1) / BM * BM;
+    }
+    return pad2 * 100 <= pad1 * 115 ? 2 : 1;
+}
+
+// Tile counts for the workspace bound (128-row tiles: never fewer than 256-row ones).
+long long moe_row_tiles(const std::vector<int64_t>& off, int64_t n_tiles) {
+    long long t = 0;
+    for (size_t e = 0; e + 1 < off.size(); ++e) t += (off[e + 1] - off[e] + BM - 1) / BM * n_tiles;
+    return t;
+}
+
+struct MoeDims {
+    int64_t E, D, H, Dout, T;
+};
+
+size_t moe_fwd_tables(const std::vector<int64_t>& off, const MoeDims& d, size_t* first) {
+    const size_t a = table_bytes((size_t)d.E, (size_t)moe_row_tiles(off, (d.H + BN / 2 - 1) / (BN / 2)));
+    const size_t b = table_bytes((size_t)d.E, (size_t)moe_row_tiles(off, (d.Dout + BN - 1) / BN));
+    if (first) *first = a;
+    return a + b;
+}
+
+size_t moe_bwd_tables(const std::vector<int64_t>& off, const MoeDims& d, size_t* first) {
+    const size_t a = table_bytes((size_t)d.E, (size_t)moe_row_tiles(off, (d.H + BN - 1) / BN));
+    const long long dw_tiles = d.E * (((d.Dout + BM - 1) / BM) * ((d.H + BN - 1) / BN) +
+                                      ((2 * d.H + BM - 1) / BM) * ((d.D + BN - 1) / BN));
+    const size_t b = table_bytes((size_t)(3 * d.E), (size_t)(moe_row_tiles(off, (d.D + BN - 1) / BN) + dw_tiles));
+    if (first) *first = a;
+    return a + b;
+}
+
+// Plain-GEMM entry: C [M,N] = A * B^T, either operand K-major or MN-major.
+bool fill_gemm(TableEntry& t, const GemmSpec& g, int cg) {
+    std::memset(&t, 0, sizeof t);
+    if (!encode_operand(&t.a, g.A, g.M, g.K, g.a_mn, BM)) return false;
+    if (!encode_operand(&t.b, g.B, g.N, g.K, g.b_mn, BN / cg)) return false;
+    if (!encode_out_2d(&t.o0, g.C, g.M, g.N)) return false;
+    t.prob = make_problem(g.M, g.N, g.K, (g.N + BN - 1) / BN, g.a_mn, g.b_mn, cg);
+    return true;
+}
+
+template <class T>
+const T* at_row(const void* base, int64_t row, int64_t width) {
+    return reinterpret_cast<const T*>(static_cast<const uint8_t*>(base) + row * width * 2);
+}
+template <class T>
+T* at_row(void* base, int64_t row, int64_t width) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + row * width * 2);
+}
+
+swiglu_status moe_check(const std::vector<int64_t>& off, const MoeDims& d) {
+    if (!dims_ok(d.D) || !dims_ok(d.H) || !dims_ok(d.Dout) || 2 * d.H >= (int64_t(1) << 31))
+        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    (void)off;
+    return SWIGLU_OK;
+}
+
+}  // namespace
+}  // namespace swiglu
+
+extern "C" {
+
+size_t swiglu_moe_fwd_workspace_size(const int64_t* counts, int64_t E, int64_t D, int64_t H, int64_t Dout) {
+    std::vector<int64_t> off;
+    if (!moe_offsets(counts, E, off) || H <= 0 || D <= 0 || Dout <= 0) return 0;
+    const MoeDims d{E, D, H, Dout, off[E]};
+    return round256((size_t)d.T * (size_t)H * 2) + moe_fwd_tables(off, d, nullptr);
+}
+
+size_t swiglu_moe_bwd_workspace_size(const int64_t* counts, int64_t E, int64_t D, int64_t H, int64_t Dout) {
+    std::vector<int64_t> off;
+    if (!moe_offsets(counts, E, off) || H <= 0 || D <= 0 || Dout <= 0) return 0;
+    const MoeDims d{E, D, H, Dout, off[E]};
+    return round256((size_t)d.T * (size_t)H * 2) + round256((size_t)d.T * (size_t)H * 4) +
+           moe_bwd_tables(off, d, nullptr);
+}
+
+swiglu_status swiglu_moe_fwd(const void* x, const void* W1, const void* W2, void* preact, void* y,
+                             const int64_t* counts, int64_t E, int64_t D, int64_t H, int64_t Dout,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    std::vector<int64_t> off;
+    if (!moe_offsets(counts, E, off) || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    const MoeDims d{E, D, H, Dout, off[E]};
+    swiglu_status rc = moe_check(off, d);
+    if (rc != SWIGLU_OK) return rc;
+    if (d.T == 0) return SWIGLU_OK;
+    if (!x || !W1 || !W2 || !preact || !y || !workspace) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(preact) || !aligned16(y) ||
+        !aligned16(workspace))
+        return SWIGLU_ERR_MISALIGNED;
+    if (workspace_bytes < swiglu_moe_fwd_workspace_size(counts, E, D, H, Dout))
+        return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+    DeviceState* st;
+    rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* h = static_cast<uint8_t*>(workspace);
+    size_t tab_a = 0;
+    const size_t tabs = moe_fwd_tables(off, d, &tab_a);
+    uint8_t* table_a = h + round256((size_t)d.T * (size_t)H * 2);
+    uint8_t* table_b = table_a + tab_a;
+    const int cg = moe_pick_cg(off);
+
+    std::vector<TableEntry> ents;
+    ents.reserve((size_t)E);
+    for (int64_t e = 0; e < E; ++e) {        // preact_e = x_e @ W1[e]^T, SwiGLU epilogue
+        const int64_t m = off[e + 1] - off[e];
+        if (m == 0) continue;
+        ents.emplace_back();
+        TableEntry& t = ents.back();
+        std::memset(&t, 0, sizeof t);
+        const void* w1 = at_row<uint8_t>(W1, e * 2 * H, D);
+        bool ok = encode_operand(&t.a, at_row<uint8_t>(x, off[e], D), m, D, false, BM);
+        ok = ok && encode_3d(&t.b, w1, (uint64_t)D, (uint64_t)H, 2, (uint64_t)D * 2, (uint64_t)H * D * 2, 64,
+                             BN / 2, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && encode_paired(&t.o0, at_row<uint8_t>(preact, off[e], 2 * H), m, H, 32);
+        ok = ok && encode_out_2d(&t.o1, at_row<uint8_t>(h, off[e], H), m, H);
+        if (!ok) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe fwd_preact)");
+        t.prob = make_problem(m, H, D, (H + BN / 2 - 1) / (BN / 2), false, false, cg);
+    }
+    rc = cg == 2 ? launch_table<EPI_SWIGLU_FWD, 2>(st, SWIGLU_KERNEL_FWD_PREACT, ents, table_a, tab_a, s)
+                 : launch_table<EPI_SWIGLU_FWD, 1>(st, SWIGLU_KERNEL_FWD_PREACT, ents, table_a, tab_a, s);
+    if (rc != SWIGLU_OK) return rc;
+    ents.clear();
+    for (int64_t e = 0; e < E; ++e) {        // y_e = h_e @ W2[e]^T
+        const int64_t m = off[e + 1] - off[e];
+        if (m == 0) continue;
+        ents.emplace_back();
+        const GemmSpec g{at_row<uint8_t>(h, off[e], H), at_row<uint8_t>(W2, e * Dout, H),
+                         at_row<uint8_t>(y, off[e], Dout), m, Dout, H, false, false};
+        if (!fill_gemm(ents.back(), g, cg)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe fwd_down)");
+    }
+    return cg == 2 ? launch_table<EPI_STORE, 2>(st, SWIGLU_KERNEL_FWD_DOWN, ents, table_b, tabs - tab_a, s)
+                   : launch_table<EPI_STORE, 1>(st, SWIGLU_KERNEL_FWD_DOWN, ents, table_b, tabs - tab_a, s);
+}
+
+swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
+                             void* dx, void* dW1, void* dW2, const int64_t* counts, int64_t E, int64_t D,
+                             int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes, void* stream) {
+    std::vector<int64_t> off;
+    if (!moe_offsets(counts, E, off) || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    const MoeDims d{E, D, H, Dout, off[E]};
+    swiglu_status rc = moe_check(off, d);
+    if (rc != SWIGLU_OK) return rc;
+    if (!W1 || !W2 || !dW1 || !dW2) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(dW1) || !aligned16(dW2)) return SWIGLU_ERR_MISALIGNED;
+    if (d.T > 0) {
+        if (!x || !preact || !dy || !dx || !workspace) return SWIGLU_ERR_INVALID_ARG;
+        if (!aligned16(x) || !aligned16(preact) || !aligned16(dy) || !aligned16(dx) || !aligned16(workspace))
+            return SWIGLU_ERR_MISALIGNED;
+        if (workspace_bytes < swiglu_moe_bwd_workspace_size(counts, E, D, H, Dout))
+            return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+    }
+    DeviceState* st;
+    rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // experts without tokens: zero weight gradients
+    for (int64_t e = 0; e < E; ++e) {
+        if (off[e + 1] != off[e]) continue;
+        cudaError_t ce = cudaMemsetAsync(at_row<uint8_t>(dW1, e * 2 * H, D), 0, (size_t)2 * H * D * 2, s);
+        if (ce == cudaSuccess) ce = cudaMemsetAsync(at_row<uint8_t>(dW2, e * Dout, H), 0, (size_t)Dout * H * 2, s);
+        if (ce != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync(empty expert)", ce);
+    }
+    if (d.T == 0) return SWIGLU_OK;
+    uint8_t* h = static_cast<uint8_t*>(workspace);
+    uint8_t* gp = h + round256((size_t)d.T * (size_t)H * 2);
+    size_t tab_a = 0;
+    const size_t tabs = moe_bwd_tables(off, d, &tab_a);
+    uint8_t* table_a = gp + round256((size_t)d.T * (size_t)H * 4);
+    uint8_t* table_b = table_a + tab_a;
+    const int cg = moe_pick_cg(off);
+
+    std::vector<TableEntry> ents;
+    ents.reserve((size_t)(3 * E));
+    for (int64_t e = 0; e < E; ++e) {        // grad_h_e = dy_e @ W2[e] fused with the SwiGLU backward
+        const int64_t m = off[e + 1] - off[e];
+        if (m == 0) continue;
+        ents.emplace_back();
+        TableEntry& t = ents.back();
+        std::memset(&t, 0, sizeof t);
+        bool ok = encode_operand(&t.a, at_row<uint8_t>(dy, off[e], Dout), m, Dout, false, BM);
+        ok = ok && encode_operand(&t.b, at_row<uint8_t>(W2, e * Dout, H), H, Dout, true, 0);
+        ok = ok && encode_paired(&t.o0, at_row<uint8_t>(gp, off[e], 2 * H), m, H, 32);
+        ok = ok && encode_out_2d(&t.o1, at_row<uint8_t>(h, off[e], H), m, H);
+        ok = ok && encode_paired(&t.i0, at_row<uint8_t>(preact, off[e], 2 * H), m, H, BM);
+        if (!ok) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe grad_h)");
+        t.prob = make_problem(m, H, Dout, (H + BN - 1) / BN, false, true, cg);
+    }
+    rc = cg == 2 ? launch_table<EPI_SWIGLU_BWD, 2>(st, SWIGLU_KERNEL_BWD_GRAD_H, ents, table_a, tab_a, s)
+                 : launch_table<EPI_SWIGLU_BWD, 1>(st, SWIGLU_KERNEL_BWD_GRAD_H, ents, table_a, tab_a, s);
+    if (rc != SWIGLU_OK) return rc;
+
+    // dW2[e] = dy_e^T @ h_e, dx_e = grad_preact_e @ W1[e], dW1[e] = grad_preact_e^T @ x_e:
+    // one launch over all experts (three with the ungrouped test hook)
+    const int cgw = (g_debug_flags.load() & DEBUG_FORCE_SINGLE_CTA) ? 1 : 2;
+    const bool grouped = !(g_debug_flags.load() & DEBUG_UNGROUPED);
+    const int kinds[3] = {SWIGLU_KERNEL_BWD_DW2, SWIGLU_KERNEL_BWD_DX, SWIGLU_KERNEL_BWD_DW1};
+    for (int part = grouped ? -1 : 0; part < (grouped ? 0 : 3); ++part) {
+        ents.clear();
+        for (int64_t e = 0; e < E; ++e) {
+            const int64_t m = off[e + 1] - off[e];
+            if (m == 0) continue;
+            const void* gpe = at_row<uint8_t>(gp, off[e], 2 * H);
+            const GemmSpec g[3] = {
+                {at_row<uint8_t>(dy, off[e], Dout), at_row<uint8_t>(h, off[e], H), at_row<uint8_t>(dW2, e * Dout, H),
+                 Dout, H, m, true, true},
+                {gpe, at_row<uint8_t>(W1, e * 2 * H, D), at_row<uint8_t>(dx, off[e], D), m, D, 2 * H, false, true},
+                {gpe, at_row<uint8_t>(x, off[e], D), at_row<uint8_t>(dW1, e * 2 * H, D), 2 * H, D, m, true, true},
+            };
+            for (int q = 0; q < 3; ++q) {
+                if (part >= 0 && q != part) continue;
+                ents.emplace_back();
+                if (!fill_gemm(ents.back(), g[q], cgw)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe bwd)");
+            }
+        }
+        const int kind = part < 0 ? SWIGLU_KERNEL_BWD_GEMMS : kinds[part];
+        rc = cgw == 2 ? launch_table<EPI_STORE, 2>(st, kind, ents, table_b, tabs - tab_a, s)
+                      : launch_table<EPI_STORE, 1>(st, kind, ents, table_b, tabs - tab_a, s);
+        if (rc != SWIGLU_OK) return rc;
+    }
+    return SWIGLU_OK;
+}
+
+}  // extern "C"

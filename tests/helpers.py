@@ -29,10 +29,14 @@ def parity(gpu, ref, name=""):
 
 
 def header_functions():
-    """Names of the functions include/swiglu_mlp.h declares."""
-    src = open(os.path.join(ROOT, "include", "swiglu_mlp.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(swiglu_mlp_\w+)\s*\(", src)))
+    """Names of the functions the headers under include/ declare."""
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(swiglu_(?:mlp|moe)_\w+)\s*\(", src))
+    return sorted(names)
 
 
 def ensure_library():

@@ -88,3 +88,42 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="build the CUDA library"):
         b.lib()
+
+
+# ---------------------------------------------------------------------------- mixture of experts
+
+def _counts(vals):
+    arr = (ctypes.c_int64 * len(vals))(*vals)
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def test_moe_workspace_sizes(lib):
+    c, keep = _counts([32, 120, 8, 64])
+    T, H = 224, 512
+    fwd = lib.swiglu_moe_fwd_workspace_size(c, 4, 256, H, 256)
+    bwd = lib.swiglu_moe_bwd_workspace_size(c, 4, 256, H, 256)
+    assert fwd >= T * H * 2 and bwd >= T * H * 2 + T * 2 * H * 2
+    c2, keep2 = _counts([32, 120, 8, 6400])
+    assert lib.swiglu_moe_fwd_workspace_size(c2, 4, 256, H, 256) > fwd      # more rows, more tiles
+    bad, keep3 = _counts([3, -1])
+    assert lib.swiglu_moe_fwd_workspace_size(bad, 2, 256, H, 256) == 0
+    assert lib.swiglu_moe_bwd_workspace_size(None, 2, 256, H, 256) == 0
+    assert lib.swiglu_moe_fwd_workspace_size(c, 0, 256, H, 256) == 0
+
+
+def test_moe_argument_errors(lib):
+    c, keep = _counts([32, 120, 8, 64])
+
+    def fwd(x=A16, ws=A16, wsb=BIG, D=256, H=512, Do=256, counts=c, E=4):
+        return lib.swiglu_moe_fwd(x, A16, A16, A16, A16, counts, E, D, H, Do, ws, wsb, None)
+
+    assert fwd(x=A16 + 8) == 3                 # misaligned
+    assert fwd(x=None) == 1                    # null input
+    assert fwd(D=100) == 2                     # D not a multiple of 8
+    assert fwd(wsb=64) == 4                    # workspace too small
+    assert fwd(counts=None) == 1
+    assert fwd(E=683) == 1                     # more experts than one launch's table indexes
+    big, keep2 = _counts([1 << 30, 1 << 30])
+    assert fwd(counts=big, E=2) == 1           # T >= 2^31
+    assert lib.swiglu_moe_bwd(A16, A16, A16, A16, A16, A16, A16, A16 + 4, c, 4, 256, 512, 256,
+                              A16, BIG, None) == 3
