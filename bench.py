@@ -46,10 +46,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["target", "prefill", "decode", "stack4"], default="target",
+    ap.add_argument("--workload", choices=["target", "prefill", "decode", "stack4", "moe8", "moe64"],
+                    default="target",
                     help="target: the block at the pages' target shape (the headline line); "
                          "prefill / decode: the 4096- and 16-token LLaMA-7B-shaped blocks; "
-                         "stack4: four target blocks trained end to end (with memory)")
+                         "stack4: four target blocks trained end to end (with memory); "
+                         "moe8 / moe64: mixture-of-experts layers, grouped launches over the experts")
     ap.add_argument("--residual", action="store_true",
                     help="time the residual block y = x + MLP(x) (residual-add epilogues; D == Dout)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -456,12 +458,115 @@ def run_stack(args):
         "gpu_launches_per_step": 4 * (2 + 2), "clocks": clk}), flush=True)
 
 
+def run_moe(args):
+    """A mixture-of-experts layer (tokens grouped by expert): forward + backward of
+    every expert, each step one grouped launch over all experts."""
+    import torch
+
+    from bwd_gemm_epilogue_gb300 import binding, ledger, workloads
+    from bwd_gemm_epilogue_gb300.pipeline import HostStepRunner
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = args.workload
+    counts, x_h, W1_h, W2_h, dy_h = workloads.make_moe(wl)
+    E, D, H, Do = W1_h.shape[0], x_h.shape[1], W2_h.shape[2], W2_h.shape[1]
+    T = sum(counts)
+    active = sum(1 for c in counts if c)
+    flops = ledger.gemm_flops(T, D, H, Do)       # every GEMM is linear in its row (or K) count
+    kb = ledger.kernel_bytes(T, D, H, Do, experts=active)
+    x, W1, W2, dy = (t.to(dev) for t in (x_h, W1_h, W2_h, dy_h))
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    preact, y, dx = torch.empty(T, 2 * H, **bf), torch.empty(T, Do, **bf), torch.empty(T, D, **bf)
+    dW1, dW2 = torch.empty(E, 2 * H, D, **bf), torch.empty(E, Do, H, **bf)
+    ws_f = torch.empty(binding.swiglu_moe_fwd_workspace_size(counts, D, H, Do), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(binding.swiglu_moe_bwd_workspace_size(counts, D, H, Do), dtype=torch.uint8, device=dev)
+
+    def step():
+        binding.swiglu_moe_fwd(x, W1, W2, counts, preact, y, ws_f)
+        binding.swiglu_moe_bwd(x, W1, W2, preact, dy, counts, dx, dW1, dW2, ws_b)
+
+    for _ in range(args.warmup):
+        step()
+    if binding.swiglu_mlp_device_status(dev) != 0:
+        raise RuntimeError("warm-up failed")
+    K = args.steps
+    trace = binding.LaunchTrace(8 * K)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with trace:
+        ev0.record()
+        for _ in range(K):
+            step()
+        ev1.record()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if binding.swiglu_mlp_device_status(dev) != 0:
+        raise RuntimeError("timed steps failed")
+    ms = ev0.elapsed_time(ev1) / K
+    per_kind = {}
+    for kind, kms in trace.records():
+        per_kind.setdefault(kind, []).append(kms)
+    total = sum(sum(v) for v in per_kind.values())
+    pk, pk_src = peaks()
+    kstats = {}
+    for kind, v in per_kind.items():
+        avg = sum(v) / len(v)
+        f_k = flops.get(kind, 0)
+        kstats[kind] = {"launches": len(v), "avg_us": round(avg * 1e3, 2),
+                        "tflops": round(f_k / (avg * 1e-3) / 1e12, 1),
+                        "frac_of_sustained_peak": round(f_k / (avg * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 3),
+                        "hbm_gbs_compulsory": round(kb.get(kind, 0) / (avg * 1e-3) / 1e9, 1),
+                        "share": round(sum(v) / total, 3)}
+    dom = max(kstats, key=lambda k: kstats[k]["share"])
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": kstats[dom]["tflops"],
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(kstats[dom]["tflops"] / pk["bf16_tflops_sustained"], 3), "traffic": None,
+                "peak_source": f"{pk_src} bf16_tflops_sustained (kernel timed inside a long step)"}
+
+    runner = HostStepRunner(T, D, H, Do, dev, counts=counts)
+    host_in = {k: t.pin_memory() for k, t in (("x", x_h), ("W1", W1_h), ("W2", W2_h), ("dy", dy_h))}
+    host_out = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                for k, t in (("y", y), ("dx", dx), ("dW1", dW1), ("dW2", dW2))}
+    bi, bo = runner.bytes_in(host_in), runner.bytes_out(host_out)
+    runner.run([host_in] * 2, [host_out] * 2)
+    runner.synchronize()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    runner.run([host_in] * args.e2e_steps, [host_out] * args.e2e_steps)
+    runner.synchronize()
+    torch.cuda.synchronize(dev)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+    if binding.swiglu_mlp_device_status(dev) != 0:
+        raise RuntimeError("e2e steps failed")
+    del runner
+    value = flops["step"] / (ms * 1e-3) / 1e12
+    cfg = workloads.MOE_CONFIGS[wl]
+    print(json.dumps({
+        "metric": f"SwiGLU MoE layer fwd+bwd TFLOP/s (bf16, {E} experts, {T} routed rows, D={D} H={H})",
+        "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded routed counts, N(0,1) activations/dy, N(0,1/fan_in) weights)",
+        "config": {"workload": f"{wl}: MoE SwiGLU layer, E={E} experts ({active} with rows), T={T} rows "
+                               f"grouped by expert, D={D} H={H} Dout={Do}",
+                   "E": E, "T": T, "D": D, "H": H, "Dout": Do, "seed": cfg["seed"],
+                   "rows_per_expert": {"min": min(counts), "max": max(counts)},
+                   "l2": "inputs larger than L2, no flush"},
+        "kernels": kstats, "roofline": roofline, "cpu_baseline": None,
+        "e2e": {"value": round(flops["step"] / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "gpu_launches": trace.count, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "stack4":
         run_stack(args)
+    elif args.workload in ("moe8", "moe64"):
+        run_moe(args)
     else:
         run_ours(args)
 

@@ -29,19 +29,22 @@ def gemm_flops(M: int, D: int, H: int, Dout: int) -> dict:
     return f
 
 
-def kernel_bytes(M: int, D: int, H: int, Dout: int) -> dict:
-    """Compulsory HBM bytes per launch of each kernel."""
+def kernel_bytes(M: int, D: int, H: int, Dout: int, experts: int = 1) -> dict:
+    """Compulsory HBM bytes per launch of each kernel.  `experts`: the number of
+    weight sets read (and weight gradients written) -- the experts that received
+    rows, for a mixture-of-experts layer with M rows in all."""
     b = BF16
+    E = experts
     k = {
         # x, W1 in; preact [M,2H] and h [M,H] out
-        "fwd_preact": b * (M * D + 2 * H * D + 2 * M * H + M * H),
+        "fwd_preact": b * (M * D + E * 2 * H * D + 2 * M * H + M * H),
         # h, W2 in; y out
-        "fwd_down": b * (M * H + Dout * H + M * Dout),
+        "fwd_down": b * (M * H + E * Dout * H + M * Dout),
         # dy, W2, preact in; grad_preact [M,2H] and h [M,H] out
-        "bwd_grad_h": b * (M * Dout + Dout * H + 2 * M * H + 2 * M * H + M * H),
-        "bwd_dW2": b * (M * Dout + M * H + Dout * H),
-        "bwd_dx": b * (2 * M * H + 2 * H * D + M * D),
-        "bwd_dW1": b * (2 * M * H + M * D + 2 * H * D),
+        "bwd_grad_h": b * (M * Dout + E * Dout * H + 2 * M * H + 2 * M * H + M * H),
+        "bwd_dW2": b * (M * Dout + M * H + E * Dout * H),
+        "bwd_dx": b * (2 * M * H + E * 2 * H * D + M * D),
+        "bwd_dW1": b * (2 * M * H + M * D + E * 2 * H * D),
     }
     k["bwd_gemms"] = k["bwd_dW2"] + k["bwd_dx"] + k["bwd_dW1"]
     return k

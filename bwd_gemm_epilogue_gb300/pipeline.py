@@ -7,7 +7,8 @@ host->device copy of step i+1 and the device->host copy of step i-1 run while
 step i computes:
 
     h2d stream      copy in (x, W1, W2, dy) of step i+1 into buffer (i+1) % 2
-    compute stream  swiglu_mlp_fwd + swiglu_mlp_bwd of step i on buffer i % 2
+    compute stream  swiglu_mlp_fwd + swiglu_mlp_bwd (or the MoE layer's
+                    swiglu_moe_fwd + swiglu_moe_bwd) of step i on buffer i % 2
     d2h stream      copy out (y, dx, dW1, dW2) of step i-1 from buffer (i-1) % 2
 
 Events order the reuse of each buffer: inputs of a buffer are overwritten only
@@ -23,20 +24,32 @@ from . import binding
 
 
 class HostStepRunner:
-    def __init__(self, M: int, D: int, H: int, Dout: int, device=None, residual: bool = False):
+    """counts: per-expert row counts for a mixture-of-experts layer (swiglu_moe_*;
+    W1 [E,2H,D], W2 [E,Dout,H] and their gradients per expert, M = sum(counts));
+    None for one block."""
+
+    def __init__(self, M: int, D: int, H: int, Dout: int, device=None, residual: bool = False, counts=None):
         self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         self.shape = (M, D, H, Dout)
+        self.counts = None if counts is None else [int(c) for c in counts]
+        if self.counts is not None and (sum(self.counts) != M or residual):
+            raise ValueError("counts must sum to M; the MoE layer has no residual variant")
+        E = () if counts is None else (len(self.counts),)
         bf = dict(dtype=torch.bfloat16, device=self.dev)
-        self.inp = [dict(x=torch.empty(M, D, **bf), W1=torch.empty(2 * H, D, **bf),
-                         W2=torch.empty(Dout, H, **bf), dy=torch.empty(M, Dout, **bf)) for _ in range(2)]
+        self.inp = [dict(x=torch.empty(M, D, **bf), W1=torch.empty(*E, 2 * H, D, **bf),
+                         W2=torch.empty(*E, Dout, H, **bf), dy=torch.empty(M, Dout, **bf)) for _ in range(2)]
         self.out = [dict(y=torch.empty(M, Dout, **bf), dx=torch.empty(M, D, **bf),
-                         dW1=torch.empty(2 * H, D, **bf), dW2=torch.empty(Dout, H, **bf)) for _ in range(2)]
+                         dW1=torch.empty(*E, 2 * H, D, **bf), dW2=torch.empty(*E, Dout, H, **bf)) for _ in range(2)]
         self.preact = torch.empty(M, 2 * H, **bf)
         self.residual = residual      # residual block: y = x + MLP(x), dx += dy
-        self.ws_f = torch.empty(max(16, binding.swiglu_mlp_fwd_workspace_size(M, D, H, Dout)),
-                                dtype=torch.uint8, device=self.dev)
-        self.ws_b = torch.empty(max(16, binding.swiglu_mlp_bwd_workspace_size(M, D, H, Dout)),
-                                dtype=torch.uint8, device=self.dev)
+        if self.counts is None:
+            fb = binding.swiglu_mlp_fwd_workspace_size(M, D, H, Dout)
+            bb = binding.swiglu_mlp_bwd_workspace_size(M, D, H, Dout)
+        else:
+            fb = binding.swiglu_moe_fwd_workspace_size(self.counts, D, H, Dout)
+            bb = binding.swiglu_moe_bwd_workspace_size(self.counts, D, H, Dout)
+        self.ws_f = torch.empty(max(16, fb), dtype=torch.uint8, device=self.dev)
+        self.ws_b = torch.empty(max(16, bb), dtype=torch.uint8, device=self.dev)
         self.s_h2d = torch.cuda.Stream(self.dev)
         self.s_cmp = torch.cuda.Stream(self.dev)
         self.s_d2h = torch.cuda.Stream(self.dev)
@@ -70,9 +83,15 @@ class HostStepRunner:
             self.s_cmp.wait_event(self.h2d_done[b])
             if self._used[b]:
                 self.s_cmp.wait_event(self.d2h_done[b])
-            binding.swiglu_mlp_fwd(d["x"], d["W1"], d["W2"], self.preact, o["y"], self.ws_f, residual=self.residual)
-            binding.swiglu_mlp_bwd(d["x"], d["W1"], d["W2"], self.preact, d["dy"], o["dx"], o["dW1"], o["dW2"],
-                                   self.ws_b, residual=self.residual)
+            if self.counts is None:
+                binding.swiglu_mlp_fwd(d["x"], d["W1"], d["W2"], self.preact, o["y"], self.ws_f,
+                                       residual=self.residual)
+                binding.swiglu_mlp_bwd(d["x"], d["W1"], d["W2"], self.preact, d["dy"], o["dx"], o["dW1"],
+                                       o["dW2"], self.ws_b, residual=self.residual)
+            else:
+                binding.swiglu_moe_fwd(d["x"], d["W1"], d["W2"], self.counts, self.preact, o["y"], self.ws_f)
+                binding.swiglu_moe_bwd(d["x"], d["W1"], d["W2"], self.preact, d["dy"], self.counts, o["dx"],
+                                       o["dW1"], o["dW2"], self.ws_b)
             self.cmp_done[b].record(self.s_cmp)
         self._used[b] = True
 
