@@ -161,3 +161,27 @@ def make_moe(name: str):
     W1 = normal_bf16((E, 2 * H, D), D ** -0.5, seed, _W1)
     W2 = normal_bf16((E, Dout, H), H ** -0.5, seed, _W2)
     return counts, x, W1, W2, dy
+
+
+def pow2_scale(t: torch.Tensor, fmax: float = 448.0) -> float:
+    """The smallest power of two s with max|t| / s <= fmax (per-tensor FP8 scale)."""
+    import math
+    amax = float(t.abs().max()) if t.numel() else 0.0
+    return 2.0 ** math.ceil(math.log2(amax / fmax)) if amax > 0 else 1.0
+
+
+def to_e4m3(t: torch.Tensor, s: float) -> torch.Tensor:
+    """t / s as FP8 E4M3 (torch's conversion: round to nearest even)."""
+    return (t.float() / s).to(torch.float8_e4m3fn)
+
+
+def make_fp8_block(s: Shape, seed: int, s_h: float = 1.0 / 32):
+    """FP8 inputs of the block: x8, W1_8, W2_8 (E4M3) and per-tensor power-of-two
+    scales {s_x, s_w1, s_w2, s_h}, from the same draws as make_block (x ~ N(0,1),
+    weights ~ N(0, 1/fan_in)).  s_h, the scale h is quantised with, is fixed: with
+    preact ~ N(0,1) a few of the largest h saturate at 448 * s_h = 14."""
+    x = torch.randn((s.M, s.D), generator=_gen(seed, _X), dtype=torch.float32)
+    W1 = torch.randn((2 * s.H, s.D), generator=_gen(seed, _W1), dtype=torch.float32) * s.D ** -0.5
+    W2 = torch.randn((s.Dout, s.H), generator=_gen(seed, _W2), dtype=torch.float32) * s.H ** -0.5
+    sc = {"s_x": pow2_scale(x), "s_w1": pow2_scale(W1), "s_w2": pow2_scale(W2), "s_h": float(s_h)}
+    return to_e4m3(x, sc["s_x"]), to_e4m3(W1, sc["s_w1"]), to_e4m3(W2, sc["s_w2"]), sc

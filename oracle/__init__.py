@@ -21,7 +21,11 @@ fp32->bf16 conversion and hand-worked ties; closed forms at g = 0, +-20;
 permutation weights, where every product reduces to a gather; for the
 mixture-of-experts functions, experts built as hidden-unit permutations and
 power-of-two scalings of one dense block, whose outputs are then known
-transforms of the dense block's.  No function here is "parity unpinned".
+transforms of the dense block's; for the FP8 forward, E4M3 decoding against
+torch's float8_e4m3fn, encoding against torch's rounding, hand-worked ties and
+saturation, and the FP8 forward against the bf16 oracle on the dequantised
+inputs and an fp64 matmul of the dequantised codes.  No function here is
+"parity unpinned".
 """
 from __future__ import annotations
 
@@ -73,6 +77,13 @@ def _load():
                                                    i32, vp, vp]
             lib.oracle_num_threads.restype = i32
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_e4m3_decode.restype = d
+            lib.oracle_e4m3_decode.argtypes = [i32]
+            lib.oracle_e4m3_encode.restype = i32
+            lib.oracle_e4m3_encode.argtypes = [d]
+            lib.oracle_swiglu_fwd_fp8.restype = i32
+            lib.oracle_swiglu_fwd_fp8.argtypes = [vp, vp, vp, d, d, d, d, i64, i64, i64, i64, vp, i64,
+                                                  vp, vp, vp, vp]
             _lib = lib
     return _lib
 
@@ -302,3 +313,56 @@ def moe_cols(x, W2, preact, dy, counts, expert, cols):
     if b == a:
         return np.zeros((n, Dout)), np.zeros((n, xb.shape[1])), np.zeros((n, xb.shape[1]))
     return bwd_cols(xb[a:b], w2b[expert], pb[a:b], dyb[a:b], cols=cols)
+
+
+# ---------------------------------------------------------------------------- FP8 forward
+#
+# "Lesson 24: MLP, GEMM and operator fusion in the Transformer" (lincklin.cn),
+# section 26 (the quantised GEMM epilogue, y = sat8(round(s * acc + b))) and
+# section 31 (8-bit weights for the weight-bound decode).  Formats and rounding
+# points are documented in swiglu_oracle.c.
+
+def e4m3_decode(code: int) -> float:
+    """Value of an FP8 E4M3 code (NaN for the NaN codes)."""
+    return float(_load().oracle_e4m3_decode(int(code)))
+
+
+def e4m3_encode(v: float) -> int:
+    """Nearest E4M3 code, ties to even, saturating at +-448."""
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+def _codes(a) -> np.ndarray:
+    """torch float8_e4m3fn / uint8 tensor or uint8 array -> contiguous uint8 codes."""
+    if hasattr(a, "dtype") and str(a.dtype) in ("torch.float8_e4m3fn", "torch.uint8"):
+        import torch
+        return a.detach().cpu().contiguous().view(torch.uint8).numpy()
+    arr = np.ascontiguousarray(a)
+    if arr.dtype != np.uint8:
+        raise TypeError(f"expected E4M3 codes (uint8), got {arr.dtype}")
+    return arr
+
+
+def fwd_fp8(x8, W1_8, W2_8, s_x: float, s_w1: float, s_w2: float, s_h: float, rows=None):
+    """FP8 forward for the selected token rows (all rows when ``rows`` is None).
+
+    Returns (preact [n,2H] bf16-rounded, h [n,H] before quantisation, h8 [n,H] E4M3
+    codes (uint8), y [n,Dout] unrounded), fp64 except h8.
+    """
+    xb, w1b, w2b = _codes(x8), _codes(W1_8), _codes(W2_8)
+    M, D = xb.shape
+    H = w1b.shape[0] // 2
+    Dout = w2b.shape[0]
+    if w1b.shape != (2 * H, D) or w2b.shape != (Dout, H):
+        raise ValueError("shape mismatch")
+    ridx, n = _index(rows, M)
+    preact = np.empty((n, 2 * H))
+    hpre = np.empty((n, H))
+    h8 = np.empty((n, H), dtype=np.uint8)
+    y = np.empty((n, Dout))
+    rc = _load().oracle_swiglu_fwd_fp8(_ptr(xb), _ptr(w1b), _ptr(w2b), float(s_x), float(s_w1), float(s_w2),
+                                       float(s_h), M, D, H, Dout, _ptr(ridx), n,
+                                       _ptr(preact), _ptr(hpre), _ptr(h8), _ptr(y))
+    if rc != 0:
+        raise MemoryError("oracle_swiglu_fwd_fp8 failed")
+    return preact, hpre, h8, y

@@ -309,3 +309,99 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 forward with a quantising epilogue.
+ *
+ * "Lesson 24: MLP, GEMM and operator fusion in the Transformer" (lincklin.cn),
+ * section 26 (quantised GEMM epilogue): the 8-bit GEMM accumulates in higher
+ * precision and the epilogue scales the accumulator, applies the activation,
+ * rounds and saturates to the 8-bit output format, y = sat8(round(s * acc + b));
+ * section 31: 8-bit weights halve the weight traffic of the bandwidth-bound
+ * decode step.
+ *
+ * The 8-bit format is FP8 E4M3 ("e4m3fn": 1 sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits; exponent field 0 is subnormal, (m / 8) * 2^-6; the code
+ * with all exponent and mantissa bits set is NaN; no infinities; the largest
+ * finite value is 1.75 * 2^8 = 448).
+ *
+ * The block in FP8 (per-tensor scales; the block has no bias, b = 0):
+ *   x = s_x * x8,  W1 = s_w1 * W1_8,  W2 = s_w2 * W2_8        (8-bit codes)
+ *   preact = s_x * s_w1 * (x8 @ W1_8^T)          accumulated exactly, stored bf16
+ *   h      = left * bf16(silu(gate))             from the bf16 preact, as in fp64
+ *   h8     = sat8(round(h / s_h))                the quantising epilogue
+ *   y      = s_h * s_w2 * (h8 @ W2_8^T)          returned unrounded
+ * Products of two E4M3 values are exact in fp64 and so are sums of up to 2^20 of
+ * them (their exponents span fewer than 36 bits), so both accumulations are
+ * exact here in any order.
+ * ------------------------------------------------------------------------ */
+
+double oracle_e4m3_decode(int code) {
+    int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);   /* (m/8) 2^-6 | (1 + m/8) 2^(e-7) */
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 code, ties to the even code (mantissa LSB 0); magnitudes beyond
+ * 448 saturate to +-448; NaN gives the NaN code. */
+int oracle_e4m3_encode(double v) {
+    if (isnan(v)) return 0x7F;
+    int sign = signbit(v) ? 0x80 : 0;
+    double a = fabs(v);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c < 0x7F; ++c) {       /* all non-negative finite codes, ascending */
+        double err = fabs(oracle_e4m3_decode(c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return sign | best;                    /* beyond 448 the nearest code is 448 itself */
+}
+
+int oracle_swiglu_fwd_fp8(const uint8_t *x8, const uint8_t *W1_8, const uint8_t *W2_8,
+                          double s_x, double s_w1, double s_w2, double s_h,
+                          int64_t M, int64_t D, int64_t H, int64_t Dout,
+                          const int64_t *rows, int64_t nrows,
+                          double *preact_out, double *hpre_out, uint8_t *h8_out, double *y_out) {
+    (void)M;
+    double lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = oracle_e4m3_decode(c);
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        double *pre = (double *)malloc((size_t)(2 * H > 0 ? 2 * H : 1) * sizeof(double));
+        double *hq = (double *)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
+        if (!pre || !hq) {
+            free(pre); free(hq);
+#pragma omp atomic write
+            fail = 1;
+            continue;
+        }
+        for (int64_t n = 0; n < 2 * H; ++n) {
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc += lut[x8[m * D + d]] * lut[W1_8[n * D + d]];
+            pre[n] = oracle_round_bf16(s_x * s_w1 * acc);
+        }
+        for (int64_t j = 0; j < H; ++j) {
+            double h = pre[j] * oracle_round_bf16(oracle_silu(pre[H + j]));
+            int code = oracle_e4m3_encode(h / s_h);
+            if (hpre_out) hpre_out[i * H + j] = h;
+            if (h8_out) h8_out[i * H + j] = (uint8_t)code;
+            hq[j] = lut[code];
+        }
+        if (y_out) {
+            for (int64_t o = 0; o < Dout; ++o) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < H; ++j) acc += hq[j] * lut[W2_8[o * H + j]];
+                y_out[i * Dout + o] = s_h * s_w2 * acc;
+            }
+        }
+        if (preact_out) memcpy(preact_out + i * 2 * H, pre, (size_t)(2 * H) * sizeof(double));
+        free(pre); free(hq);
+    }
+    return fail ? -1 : 0;
+}

@@ -411,3 +411,77 @@ def test_moe_single_expert_is_the_dense_block_and_samples_agree():
     np.testing.assert_array_equal(dW1l, full[4][2][cols])
     np.testing.assert_array_equal(dW1g, full[4][2][[24 + c for c in cols]])
     assert not oracle.moe_cols(x, W2e, pre, dy, counts, 1, cols)[1].any()
+
+
+# ----------------------------------------------------------------------------
+# FP8 E4M3 codes and the FP8 forward
+# ----------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_torch_and_the_format():
+    tv = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    ov = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    assert np.array_equal(np.isnan(ov), np.isnan(tv))
+    fin = ~np.isnan(ov)
+    np.testing.assert_array_equal(ov[fin], tv[fin])
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6 and oracle.e4m3_decode(0x38) == 1.0
+    assert np.isnan(oracle.e4m3_decode(0x7F)) and np.isnan(oracle.e4m3_decode(0xFF))
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    for c in range(256):
+        v = oracle.e4m3_decode(c)
+        if not math.isnan(v):
+            assert oracle.e4m3_encode(v) == c, c
+    enc = oracle.e4m3_encode
+    assert enc(2.0 ** -10) == 0x00             # half the smallest subnormal: tie -> even (0)
+    assert enc(3 * 2.0 ** -10) == 0x02         # tie between codes 1 and 2 -> 2
+    assert enc(2.0 ** -10 + 2.0 ** -30) == 0x01
+    assert enc(1.0625) == 0x38                 # tie between 1 and 1.125 -> 1 (even)
+    assert enc(1.1875) == 0x3A                 # tie between 1.125 and 1.25 -> 1.25
+    assert enc(449.0) == 0x7E and enc(464.0) == 0x7E and enc(1e9) == 0x7E and enc(-1e9) == 0xFE
+    assert enc(float("nan")) == 0x7F
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    g = torch.Generator().manual_seed(9)
+    v = torch.randn(3000, generator=g) * torch.exp2(torch.randint(-12, 8, (3000,), generator=g).float())
+    v = v.clamp(-440.0, 440.0)
+    # every midpoint between neighbouring positive codes, both signs
+    vals = torch.arange(0, 0x7E, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    mids = (vals[:-1] + vals[1:]) / 2
+    v = torch.cat([v, mids, -mids])
+    want = v.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(a)) for a in v.double().numpy()])
+    np.testing.assert_array_equal(got, want)
+
+
+def test_fp8_forward_against_the_bf16_oracle_and_fp64_matmul():
+    # Power-of-two scales make the dequantised inputs exact, so the FP8 forward's
+    # preact must equal the bf16 oracle's preact on the dequantised fp64 inputs; its h
+    # before quantisation, rounded to bf16, the bf16 oracle's h; its h8 the nearest
+    # E4M3 code of h / s_h (within half a code spacing, or saturated); and its y the
+    # fp64 product of the dequantised h8 and W2.
+    s = workloads.Shape(33, 48, 40, 24)
+    x8, W1_8, W2_8, sc = workloads.make_fp8_block(s, seed=90, s_h=1.0 / 256)   # saturates above 1.75
+    p8, hpre, h8, y8 = oracle.fwd_fp8(x8, W1_8, W2_8, **sc)
+    deq = lambda t, sv: torch.from_numpy(  # noqa: E731
+        np.array([oracle.e4m3_decode(c) for c in t.view(torch.uint8).flatten().tolist()]).reshape(t.shape) * sv)
+    x, W1, W2 = deq(x8, sc["s_x"]), deq(W1_8, sc["s_w1"]), deq(W2_8, sc["s_w2"])
+    p_ref, h_ref, _ = oracle.fwd(x, W1, W2)
+    np.testing.assert_array_equal(p8, p_ref)
+    np.testing.assert_array_equal(np.vectorize(oracle.round_bf16)(hpre), h_ref)
+    hq = np.vectorize(oracle.e4m3_decode)(h8.astype(np.int64))
+    q = hpre / sc["s_h"]
+    sat = np.abs(q) >= 448
+    assert sat.any() and (~sat).any()
+    np.testing.assert_array_equal(hq[sat], np.sign(q[sat]) * 448)
+    a = np.abs(q[~sat])
+    spacing = np.where(a < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -6))) - 3))
+    assert (np.abs(hq[~sat] - q[~sat]) <= spacing / 2).all()
+    y_ref = (hq * sc["s_h"]) @ W2.numpy().T
+    np.testing.assert_array_equal(y8, y_ref)
+    # row subsets agree with the full computation
+    r = oracle.fwd_fp8(x8, W1_8, W2_8, rows=[0, 17, 32], **sc)
+    np.testing.assert_array_equal(r[2], h8[[0, 17, 32]])
+    np.testing.assert_array_equal(r[3], y8[[0, 17, 32]])
