@@ -40,6 +40,8 @@ SIGNATURES = {
     "swiglu_mlp_fwd_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_bwd_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
+    "swiglu_mlp_fwd_fp8": (_i32, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                  _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
     "swiglu_mlp_fused_grad_preact": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "swiglu_mlp_gemm_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
     "swiglu_mlp_device_status": (_i32, [_vp]),
@@ -101,8 +103,8 @@ def _ptr(t: torch.Tensor | None):
         return None
     if not t.is_cuda:
         raise ValueError("tensor must live on a CUDA device")
-    if t.dtype != torch.bfloat16 and t.dtype != torch.uint8:
-        raise TypeError(f"expected bf16 (or a uint8 workspace), got {t.dtype}")
+    if t.dtype not in (torch.bfloat16, torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"expected bf16, FP8 E4M3 (or a uint8 workspace), got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
@@ -250,6 +252,26 @@ def bwd_workspace_views(workspace: torch.Tensor, M: int, H: int):
     h = workspace[: M * H * 2].view(torch.bfloat16).view(M, H)
     gp = workspace[off: off + M * 2 * H * 2].view(torch.bfloat16).view(M, 2 * H)
     return h, gp
+
+
+def swiglu_mlp_fwd_fp8(x8, W1_8, W2_8, s_x: float, s_w1: float, s_w2: float, s_h: float,
+                       preact=None, h8=None, y=None, store_preact: bool = True):
+    """FP8 forward (E4M3 operands, per-tensor scales); returns (preact [M,2H] bf16 or
+    None, h8 [M,H] E4M3, y [M,Dout] bf16)."""
+    M, D = x8.shape
+    H2, D1 = W1_8.shape
+    Dout, H = W2_8.shape
+    if D1 != D or H2 != 2 * H:
+        raise ValueError("shape mismatch")
+    if store_preact and preact is None:
+        preact = _empty((M, 2 * H), x8)
+    h8 = torch.empty(M, H, dtype=torch.float8_e4m3fn, device=x8.device) if h8 is None else h8
+    y = _empty((M, Dout), x8) if y is None else y
+    st = lib().swiglu_mlp_fwd_fp8(_ptr(x8), _ptr(W1_8), _ptr(W2_8), s_x, s_w1, s_w2, s_h,
+                                  _ptr(preact) if store_preact else None, _ptr(h8), _ptr(y), M, D, H, Dout,
+                                  _stream(x8.device))
+    _check(st, "swiglu_mlp_fwd_fp8")
+    return (preact if store_preact else None), h8, y
 
 
 def swiglu_mlp_fused_grad_preact(dy, W2, preact, grad_preact=None, h=None):

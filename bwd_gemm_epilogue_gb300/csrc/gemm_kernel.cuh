@@ -62,6 +62,11 @@ namespace swiglu {
 
 enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_STORE_ADD = 3 };
 
+// Operand type of the MMAs: bf16 (kind::f16) or FP8 E4M3 (kind::f8f6f4).  Both fill a
+// 128-byte swizzle row per k-block -- 64 bf16 or 128 FP8 values -- so the stage
+// layout, descriptors and 32-byte k-steps are the same.
+enum OperandType : int { OP_BF16 = 0, OP_E4M3 = 1 };
+
 constexpr int BM = 128;           // accumulator rows per CTA
 constexpr int BN = 256;           // accumulator columns
 constexpr int BK = 64;            // one 128-byte swizzle row of bf16
@@ -90,6 +95,7 @@ struct Problem {
     int a_mn, b_mn;   // operand major-ness (1 = M- or N-contiguous)
     int res;          // EPI_STORE_ADD: add the residual tensor (tensor map i0) to this problem's output
     int tile_begin;   // index of this problem's first tile in the launch
+    int no_o0;        // EPI_SWIGLU_FWD: do not store preact (o0), only h
 };
 
 struct KernelArgs {
@@ -101,6 +107,8 @@ struct KernelArgs {
     unsigned long long timeout_ns;
     int* err;         // device error word
     int debug_flags;
+    float scale_acc;  // OP_E4M3: the accumulator's scale (product of the operands' scales)
+    float scale_out;  // OP_E4M3 SwiGLU forward: 1 / the scale h is quantised with
 };
 
 // A launch with an explicit per-cluster tile list (longest tiles first, balanced on
@@ -200,10 +208,10 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor, kind::f16: bf16 A/B, fp32 D, M = 128 * CG, N = 256.
-__host__ __device__ constexpr uint32_t umma_idesc(bool a_mn_major, bool b_mn_major, int cg) {
+__host__ __device__ constexpr uint32_t umma_idesc(bool a_mn_major, bool b_mn_major, int cg, bool e4m3 = false) {
     return (1u << 4)                          // D format f32
-           | (1u << 7)                        // A format bf16
-           | (1u << 10)                       // B format bf16
+           | ((e4m3 ? 0u : 1u) << 7)          // A format: bf16 (kind::f16) or E4M3 (kind::f8f6f4)
+           | ((e4m3 ? 0u : 1u) << 10)         // B format likewise
            | ((a_mn_major ? 1u : 0u) << 15)   // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
            | ((uint32_t)(BN >> 3) << 17)      // N >> 3
@@ -370,10 +378,13 @@ using ArgsOf = typename std::conditional<
     SCHED == SRC_TABLE, TableArgs,
     typename std::conditional<SCHED == SRC_PARAMS, ScheduledArgs, KernelArgs>::type>::type;
 
-template <int EPI, int CG, int SCHED>
+template <int EPI, int CG, int SCHED, int OP = OP_BF16>
 __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     gemm_kernel(const __grid_constant__ ArgsOf<EPI, CG, SCHED> args) {
     using C = Cfg<EPI, CG>;
+    static_assert(OP == OP_BF16 || ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) && SCHED == SRC_SINGLE),
+                  "FP8 operands: forward kernels, one problem per launch");
+    constexpr int BKE = OP == OP_E4M3 ? 2 * BK : BK;   // k values per 128-byte k-block
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -424,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 if (q < args.num_problems) {
                     ptx::prefetch_tmap(&args.a[q]);
                     ptx::prefetch_tmap(&args.b[q]);
-                    ptx::prefetch_tmap(&args.o0[q]);
+                    if (!args.prob[q].no_o0) ptx::prefetch_tmap(&args.o0[q]);
                 }
             }
             if (!C::STORE_ONLY) ptx::prefetch_tmap(&args.o1);
@@ -483,7 +494,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     const uint32_t fb = CG == 2 ? full_bar_leader + 8u * stage : fb_local;
                     if (leader) ptx::mbar_arrive_expect_tx(fb_local, C::TX_BYTES);
                     last_parity[stage] = (int)phase;
-                    const int k0 = kb * BK;
+                    const int k0 = kb * BKE;
                     const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
                     const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
                     auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
@@ -541,7 +552,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 const Problem pq = problem_at<SCHED>(args, it, pi, lt);
                 const int k_blocks = pq.k_blocks;
                 const bool a_mn = pq.a_mn != 0, b_mn = pq.b_mn != 0;
-                const uint32_t idesc = umma_idesc(a_mn, b_mn, CG);
+                const uint32_t idesc = umma_idesc(a_mn, b_mn, CG, OP == OP_E4M3);
                 // Descriptors of stage 0, k = 0; a stage and a 16-k step only move the start
                 // address (low 14 bits, in 16-byte units, no carry below 256 KB).
                 // K-major: the next 16 k sit 32 bytes further along each 128-B row;
@@ -572,8 +583,14 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         const uint64_t ad = ad0 + (uint64_t)(k * a_kstep);
                         const uint64_t bd = bd0 + (uint64_t)(k * b_kstep);
-                        if (CG == 2) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                        else ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        const uint32_t acc_flag = (kb | k) != 0 ? 1u : 0u;
+                        if (OP == OP_E4M3) {
+                            if (CG == 2) ptx::mma_e4m3_pair(d_tmem, ad, bd, idesc, acc_flag);
+                            else ptx::mma_e4m3(d_tmem, ad, bd, idesc, acc_flag);
+                        } else {
+                            if (CG == 2) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc_flag);
+                            else ptx::mma_bf16(d_tmem, ad, bd, idesc, acc_flag);
+                        }
                     }
                     if (CG == 2) ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
                     else ptx::mma_commit(empty_bar(stage));
@@ -787,8 +804,18 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     }
                 }
 
-                // outputs for this chunk, packed bf16 pairs
+                // outputs for this chunk, packed bf16 pairs (the FP8 forward's h: 4 codes a word)
                 uint32_t o0[16], o1[16], o2[16];
+                if (OP == OP_E4M3) {
+                    // FP8 operands: the accumulator carries the product of the operands' scales
+                    float sa = 1.0f;
+                    if constexpr (OP == OP_E4M3) sa = args.scale_acc;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        acc[i] = __float_as_uint(__uint_as_float(acc[i]) * sa);
+                        if (EPI == EPI_SWIGLU_FWD) acc2[i] = __float_as_uint(__uint_as_float(acc2[i]) * sa);
+                    }
+                }
                 if (EPI == EPI_STORE || (EPI == EPI_STORE_ADD && !pr.res)) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -814,7 +841,15 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                             const float silu = g * sigmoid_mufu(g);
                             hv[e] = l * round_bf16(silu);
                         }
-                        o2[i] = pack_bf16(hv[0], hv[1]);
+                        if (OP == OP_E4M3) {
+                            // the quantising epilogue: h8 = sat8(round(h / s_h)), two codes per 16 bits
+                            float so = 1.0f;
+                            if constexpr (OP == OP_E4M3) so = args.scale_out;
+                            const uint32_t q2 = ptx::cvt_e4m3x2(hv[0] * so, hv[1] * so);
+                            o2[i >> 1] = (i & 1) ? (o2[i >> 1] | (q2 << 16)) : q2;
+                        } else {
+                            o2[i] = pack_bf16(hv[0], hv[1]);
+                        }
                     }
                 } else {
 #pragma unroll
@@ -846,6 +881,12 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 for (int o = 0; o < C::NOUT; ++o) {
                     const uint32_t* src = (o == 0) ? o0 : (o == 1) ? o1 : o2;
                     const uint32_t tile = ob_base + o * C::OUT_TILE;
+                    if (OP == OP_E4M3 && o == 2) {
+                        // the FP8 h tile: 32 rows of 32 bytes, unswizzled
+                        ptx::sts128(tile + lane * 32, make_uint4(src[0], src[1], src[2], src[3]));
+                        ptx::sts128(tile + lane * 32 + 16, make_uint4(src[4], src[5], src[6], src[7]));
+                        continue;
+                    }
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         ptx::sts128(tile + sw64_offset(lane, q),
@@ -861,8 +902,10 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         const int jw = (EPI == EPI_SWIGLU_FWD) ? BN / 2 : BN;
                         const int j = tn * jw + c * CHUNK;
                         if (j < n_limit) {
-                            ptx::tma_store_3d(mO0, ob_base, j, 0, mrow0);
-                            ptx::tma_store_3d(mO0, ob_base + C::OUT_TILE, j, 1, mrow0);
+                            if (!pr.no_o0) {
+                                ptx::tma_store_3d(mO0, ob_base, j, 0, mrow0);
+                                ptx::tma_store_3d(mO0, ob_base + C::OUT_TILE, j, 1, mrow0);
+                            }
                             ptx::tma_store_2d(mO1, ob_base + 2 * C::OUT_TILE, j, mrow0);
                         }
                     }

@@ -10,6 +10,7 @@
 #include <queue>
 #include <utility>
 #include <vector>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -99,23 +100,25 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows, row
 // pitch `row_bytes`.
 bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+    return g_encode(m, dtype, 2, const_cast<void*>(ptr), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_bytes,
-               uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz) {
+               uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle swz,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {s1_bytes, s2_bytes};
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t estr[3] = {1, 1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+    return g_encode(m, dtype, 3, const_cast<void*>(ptr), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -161,6 +164,7 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     p.b_mn = b_mn ? 1 : 0;
     p.res = 0;
     p.tile_begin = 0;
+    p.no_o0 = 0;
     return p;
 }
 
@@ -198,14 +202,14 @@ bool build_schedule(ScheduledArgs& a, int units) {
 
 // Persistent CTAs (CG == 1) or CTA pairs (CG == 2) of this kernel that fit on the
 // device at once; 0 on failure.
-template <int EPI, int CG, int SCHED>
+template <int EPI, int CG, int SCHED, int OP = OP_BF16>
 int cluster_slots(DeviceState* st) {
     if (CG == 1) return st->num_sms;
     static int max_clusters[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
     if (max_clusters[dev] <= 0) {
-        auto kern = gemm_kernel<EPI, CG, SCHED>;
+        auto kern = gemm_kernel<EPI, CG, SCHED, OP>;
         constexpr int smem = Cfg<EPI, CG>::SMEM_BYTES;
         // the occupancy query sees the kernel's dynamic shared memory limit
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
@@ -230,11 +234,11 @@ int cluster_slots(DeviceState* st) {
 
 // Launch `units` persistent clusters of the kernel over args (fields all filled in),
 // bracketed by the launch trace's events when one is open.
-template <int EPI, int CG, int SCHED>
+template <int EPI, int CG, int SCHED, int OP = OP_BF16>
 swiglu_status launch_grid(DeviceState* st, int kind, const ArgsOf<EPI, CG, SCHED>& args, int units,
                           cudaStream_t stream) {
     (void)st;
-    auto kern = gemm_kernel<EPI, CG, SCHED>;
+    auto kern = gemm_kernel<EPI, CG, SCHED, OP>;
     constexpr int smem = Cfg<EPI, CG>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(max dynamic smem)", e);
@@ -273,7 +277,7 @@ swiglu_status launch_grid(DeviceState* st, int kind, const ArgsOf<EPI, CG, SCHED
 // Launch one persistent grid over args' problems (parameter-block sources).  args'
 // tensor maps and problems are filled in by the caller; this sets the common
 // fields, the host schedule and the grid.
-template <int EPI, int CG, int SCHED>
+template <int EPI, int CG, int SCHED, int OP = OP_BF16>
 swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cudaStream_t stream) {
     static_assert(SCHED != SRC_TABLE, "table launches go through launch_table");
     int tiles = 0;
@@ -285,13 +289,13 @@ swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cu
     args.timeout_ns = g_timeout_ns.load();
     args.err = st->err_word;
     args.debug_flags = g_debug_flags.load();
-    const int slots = cluster_slots<EPI, CG, SCHED>(st);
+    const int slots = cluster_slots<EPI, CG, SCHED, OP>(st);
     if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
     const int units = tiles < slots ? tiles : slots;
     if constexpr (SCHED == SRC_PARAMS) {
         if (!build_schedule(args, units)) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "tile schedule too large");
     }
-    return launch_grid<EPI, CG, SCHED>(st, kind, args, units, stream);
+    return launch_grid<EPI, CG, SCHED, OP>(st, kind, args, units, stream);
 }
 
 // ---------------------------------------------------------------- small-M (decode) path
@@ -1239,3 +1243,79 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// FP8 forward ("Lesson 24: MLP, GEMM and operator fusion in the Transformer",
+// section 26, the quantised GEMM epilogue; section 31, 8-bit weights): both
+// products on FP8 E4M3 operands (tcgen05 kind::f8f6f4), fp32 accumulators, the
+// first GEMM's epilogue scaling the accumulator, applying the SwiGLU and writing
+// h quantised to E4M3; the second GEMM's epilogue scaling to bf16 y.
+// ---------------------------------------------------------------------------
+namespace swiglu {
+namespace {
+
+swiglu_status run_fwd_fp8(DeviceState* st, const void* x8, const void* W1_8, const void* W2_8, float s_x,
+                          float s_w1, float s_w2, float s_h, void* preact, void* h8, void* y, int64_t M,
+                          int64_t D, int64_t H, int64_t Dout, cudaStream_t s) {
+    constexpr CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const int cg = pick_cg(M);
+    KernelArgs a;
+    std::memset(&a, 0, sizeof a);
+    // x8 [M, D] and W1_8 [2H, D] as (k, j, half), 128 k values (bytes) per box row
+    bool ok = encode_2d(&a.a[0], x8, (uint64_t)D, (uint64_t)M, (uint64_t)D, 2 * BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, U8);
+    ok = ok && encode_3d(&a.b[0], W1_8, (uint64_t)D, (uint64_t)H, 2, (uint64_t)D, (uint64_t)H * D, 2 * BK, BN / 2, 1,
+                         CU_TENSOR_MAP_SWIZZLE_128B, U8);
+    if (preact) ok = ok && encode_paired(&a.o0[0], preact, M, H, 32);
+    // h8 [M, H]: 32-byte rows of this warp's 32 columns, unswizzled
+    ok = ok && encode_2d(&a.o1, h8, (uint64_t)H, (uint64_t)M, (uint64_t)H, CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_NONE, U8);
+    if (!ok) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (fp8 fwd_preact)");
+    a.num_problems = 1;
+    a.prob[0] = make_problem(M, H, D, (H + BN / 2 - 1) / (BN / 2), false, false, cg);
+    a.prob[0].k_blocks = (int)((D + 2 * BK - 1) / (2 * BK));
+    a.prob[0].no_o0 = preact ? 0 : 1;
+    a.scale_acc = s_x * s_w1;
+    a.scale_out = 1.0f / s_h;
+    swiglu_status rc = cg == 2
+        ? launch<EPI_SWIGLU_FWD, 2, SRC_SINGLE, OP_E4M3>(st, SWIGLU_KERNEL_FWD_PREACT, a, s)
+        : launch<EPI_SWIGLU_FWD, 1, SRC_SINGLE, OP_E4M3>(st, SWIGLU_KERNEL_FWD_PREACT, a, s);
+    if (rc != SWIGLU_OK) return rc;
+
+    // y = (s_h s_w2) * (h8 @ W2_8^T)
+    KernelArgs b;
+    std::memset(&b, 0, sizeof b);
+    ok = encode_2d(&b.a[0], h8, (uint64_t)H, (uint64_t)M, (uint64_t)H, 2 * BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, U8);
+    ok = ok && encode_2d(&b.b[0], W2_8, (uint64_t)H, (uint64_t)Dout, (uint64_t)H, 2 * BK, BN / cg,
+                         CU_TENSOR_MAP_SWIZZLE_128B, U8);
+    ok = ok && encode_out_2d(&b.o0[0], y, M, Dout);
+    if (!ok) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (fp8 fwd_down)");
+    b.num_problems = 1;
+    b.prob[0] = make_problem(M, Dout, H, (Dout + BN - 1) / BN, false, false, cg);
+    b.prob[0].k_blocks = (int)((H + 2 * BK - 1) / (2 * BK));
+    b.scale_acc = s_h * s_w2;
+    return cg == 2 ? launch<EPI_STORE, 2, SRC_SINGLE, OP_E4M3>(st, SWIGLU_KERNEL_FWD_DOWN, b, s)
+                   : launch<EPI_STORE, 1, SRC_SINGLE, OP_E4M3>(st, SWIGLU_KERNEL_FWD_DOWN, b, s);
+}
+
+}  // namespace
+}  // namespace swiglu
+
+extern "C" swiglu_status swiglu_mlp_fwd_fp8(const void* x8, const void* W1_8, const void* W2_8, float s_x,
+                                            float s_w1, float s_w2, float s_h, void* preact, void* h8, void* y,
+                                            int64_t M, int64_t D, int64_t H, int64_t Dout, void* stream) {
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (D % 16 || H % 16 || !dims_ok(Dout) || D >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31) ||
+        M >= (int64_t(1) << 31))
+        return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "fp8 forward: D and H multiples of 16, Dout of 8");
+    if (!(s_x > 0.0f) || !(s_w1 > 0.0f) || !(s_w2 > 0.0f) || !(s_h > 0.0f) || !std::isfinite(1.0f / s_h))
+        return fail(SWIGLU_ERR_INVALID_ARG, "fp8 forward: scales must be positive and finite");
+    if (M == 0) return SWIGLU_OK;
+    if (!x8 || !W1_8 || !W2_8 || !h8 || !y) return SWIGLU_ERR_INVALID_ARG;
+    if (!aligned16(x8) || !aligned16(W1_8) || !aligned16(W2_8) || !aligned16(h8) || !aligned16(y) ||
+        (preact && !aligned16(preact)))
+        return SWIGLU_ERR_MISALIGNED;
+    DeviceState* st;
+    swiglu_status rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    return run_fwd_fp8(st, x8, W1_8, W2_8, s_x, s_w1, s_w2, s_h, preact, h8, y, M, D, H, Dout,
+                       static_cast<cudaStream_t>(stream));
+}

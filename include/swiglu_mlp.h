@@ -127,6 +127,28 @@ swiglu_status swiglu_mlp_bwd_residual(const void* x, const void* W1, const void*
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 forward with a quantising epilogue ("Lesson 24: MLP, GEMM and operator
+ * fusion in the Transformer", lincklin.cn, section 26: the 8-bit GEMM's epilogue
+ * scales the accumulator, applies the activation, rounds and saturates to the
+ * 8-bit output; section 31: 8-bit weights halve the weight traffic).
+ *   x8 [M,D], W1_8 [2H,D], W2_8 [Dout,H]  FP8 E4M3 codes (one byte each), with
+ *                                         per-tensor scales: x = s_x * x8, ...
+ *   preact [M,2H]  optional bf16 output (NULL: not stored) =
+ *                  bf16(s_x * s_w1 * (x8 @ W1_8^T))
+ *   h8 [M,H]       E4M3 output: sat8(round(h / s_h)), h = left * bf16(silu(gate))
+ *                  from the bf16-rounded preact; round to nearest even, finite
+ *                  values beyond +-448 saturate to +-448
+ *   y [M,Dout]     bf16 output: s_h * s_w2 * (h8 @ W2_8^T)
+ * Both products run on the FP8 tensor cores with fp32 accumulators.  Needs D and H
+ * multiples of 16 (16-byte rows of FP8), Dout a multiple of 8, positive finite
+ * scales (SWIGLU_ERR_INVALID_ARG otherwise); no workspace (h8 is the caller's).
+ */
+swiglu_status swiglu_mlp_fwd_fp8(const void* x8, const void* W1_8, const void* W2_8,
+                                 float s_x, float s_w1, float s_w2, float s_h,
+                                 void* preact, void* h8, void* y,
+                                 int64_t M, int64_t D, int64_t H, int64_t Dout, void* stream);
+
+/*
  * The fused segment alone: grad_h = dy @ W2 (never stored) and the SwiGLU
  * backward epilogue.  Optimization note, section 4; Drop-H report, fused kernel
  * pseudo-code.

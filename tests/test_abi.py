@@ -127,3 +127,14 @@ def test_moe_argument_errors(lib):
     assert fwd(counts=big, E=2) == 1           # T >= 2^31
     assert lib.swiglu_moe_bwd(A16, A16, A16, A16, A16, A16, A16, A16 + 4, c, 4, 256, 512, 256,
                               A16, BIG, None) == 3
+
+
+def test_fp8_forward_argument_errors(lib):
+    def f(D=256, H=512, Do=256, sh=1.0, x=A16, h8=A16):
+        return lib.swiglu_mlp_fwd_fp8(x, A16, A16, 1.0, 1.0, 1.0, sh, None, h8, A16, 128, D, H, Do, None)
+
+    assert f(D=264) == 2                       # D not a multiple of 16
+    assert f(H=520) == 2                       # H not a multiple of 16
+    assert f(sh=0.0) == 1 and f(sh=-1.0) == 1  # scales must be positive
+    assert f(x=None) == 1
+    assert f(h8=A16 + 8) == 3
