@@ -46,12 +46,15 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["target", "prefill", "decode", "stack4", "moe8", "moe64"],
+    ap.add_argument("--workload", choices=["target", "prefill", "decode", "stack4", "moe8", "moe64",
+                                           "fp8_target", "fp8_prefill", "fp8_decode"],
                     default="target",
                     help="target: the block at the pages' target shape (the headline line); "
                          "prefill / decode: the 4096- and 16-token LLaMA-7B-shaped blocks; "
                          "stack4: four target blocks trained end to end (with memory); "
-                         "moe8 / moe64: mixture-of-experts layers, grouped launches over the experts")
+                         "moe8 / moe64: mixture-of-experts layers, grouped launches over the experts; "
+                         "fp8_*: the FP8 forward (E4M3, quantising epilogue) at the target / prefill / "
+                         "decode shapes, with the bf16 forward timed beside it")
     ap.add_argument("--residual", action="store_true",
                     help="time the residual block y = x + MLP(x) (residual-add epilogues; D == Dout)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -559,6 +562,89 @@ def run_moe(args):
         "gpu_launches": trace.count, "clocks": clk}), flush=True)
 
 
+def run_fp8(args):
+    """The FP8 forward (E4M3 operands, h quantised in the first GEMM's epilogue) at one
+    of the block shapes, with the bf16 forward of the same shape timed beside it."""
+    import torch
+
+    from bwd_gemm_epilogue_gb300 import binding, ledger, workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    base = args.workload[len("fp8_"):]
+    cfg = workloads.CONFIGS[base]
+    s = cfg["shape"]
+    M, D, H, Do = s.M, s.D, s.H, s.Dout
+    x8_h, W1_h, W2_h, sc = workloads.make_fp8_block(s, cfg["seed"])
+    x8, W1_8, W2_8 = (t.to(dev) for t in (x8_h, W1_h, W2_h))
+    h8 = torch.empty(M, H, dtype=torch.float8_e4m3fn, device=dev)
+    y = torch.empty(M, Do, dtype=torch.bfloat16, device=dev)
+    flops = ledger.gemm_flops(M, D, H, Do)
+
+    def fp8_step():
+        binding.swiglu_mlp_fwd_fp8(x8, W1_8, W2_8, h8=h8, y=y, store_preact=False, **sc)
+
+    # the bf16 forward of the same shape, for comparison
+    _, xb_h, W1b_h, W2b_h, _ = workloads.make_block(base)
+    xb, W1b, W2b = (t.to(dev) for t in (xb_h, W1b_h, W2b_h))
+    pre_b = torch.empty(M, 2 * H, dtype=torch.bfloat16, device=dev)
+    ws_f = torch.empty(max(16, binding.swiglu_mlp_fwd_workspace_size(M, D, H, Do)), dtype=torch.uint8, device=dev)
+
+    def bf16_step():
+        binding.swiglu_mlp_fwd(xb, W1b, W2b, pre_b, y, ws_f)
+
+    def timed(step, K):
+        for _ in range(args.warmup):
+            step()
+        tr = binding.LaunchTrace(4 * K)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with tr:
+            e0.record()
+            for _ in range(K):
+                step()
+            e1.record()
+        torch.cuda.synchronize(dev)
+        if binding.swiglu_mlp_device_status(dev) != 0:
+            raise RuntimeError("fp8 forward steps failed")
+        per = {}
+        for kind, kms in tr.records():
+            per.setdefault(kind, []).append(kms)
+        return e0.elapsed_time(e1) / K, {k: sum(v) / len(v) for k, v in per.items()}, tr.count
+
+    K = args.steps
+    clocks = ClockSampler(dev.index)
+    ms8, k8, launches = timed(fp8_step, K)
+    clk = clocks.stop()
+    msb, kbf, _ = timed(bf16_step, K)
+    pk, pk_src = peaks()
+    peak8 = 2.0 * pk["bf16_tflops_sustained"]
+    kstats = {k: {"avg_us": round(v * 1e3, 2), "tflops": round(flops.get(k, 0) / (v * 1e-3) / 1e12, 1),
+                  "frac_of_fp8_peak": round(flops.get(k, 0) / (v * 1e-3) / 1e12 / peak8, 3)} for k, v in k8.items()}
+    dom = max((k for k in k8 if k in flops), key=lambda k: k8[k])
+    kb8 = {"fwd_preact": M * D + 2 * H * D + M * H, "fwd_down": M * H + Do * H + 2 * M * Do}   # FP8 bytes
+    value = flops["fwd"] / (ms8 * 1e-3) / 1e12
+    if base == "decode":
+        gbs = kb8[dom] / (k8[dom] * 1e-3) / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / pk["hbm_gbs"], 3), "traffic": None, "peak_source": f"{pk_src} hbm_gbs"}
+    else:
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": kstats[dom]["tflops"], "peak": round(peak8, 1),
+                    "unit": "TFLOP/s", "frac": kstats[dom]["frac_of_fp8_peak"], "traffic": None,
+                    "peak_source": f"{pk_src} bf16_tflops_sustained x 2 (nominal FP8 / bf16 dense ratio)"}
+    print(json.dumps({
+        "metric": f"SwiGLU MLP FP8 forward TFLOP/s (E4M3, {M}x{D}x{H})",
+        "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms8, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3", "data": "synthetic (the bf16 workload's draws quantised to E4M3, power-of-two scales)",
+        "config": {"workload": f"{args.workload}: FP8 forward x8 @ W1_8^T (+SwiGLU, h quantised), h8 @ W2_8^T, "
+                               f"M={M} D={D} H={H} Dout={Do}, preact not stored", "scales": sc},
+        "kernels": kstats, "roofline": roofline, "cpu_baseline": None,
+        "bf16_forward_ms": round(msb, 4), "speedup_vs_bf16_forward": round(msb / ms8, 3),
+        "bf16_kernels_us": {k: round(v * 1e3, 2) for k, v in kbf.items()},
+        "gpu_launches": launches, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -567,6 +653,8 @@ def main():
         run_stack(args)
     elif args.workload in ("moe8", "moe64"):
         run_moe(args)
+    elif args.workload.startswith("fp8_"):
+        run_fp8(args)
     else:
         run_ours(args)
 

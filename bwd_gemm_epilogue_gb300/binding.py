@@ -40,8 +40,9 @@ SIGNATURES = {
     "swiglu_mlp_fwd_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_bwd_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_fwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
+    "swiglu_mlp_fwd_fp8_workspace_size": (_sz, [_i64, _i64, _i64, _i64]),
     "swiglu_mlp_fwd_fp8": (_i32, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
-                                  _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
+                                  _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "swiglu_mlp_fused_grad_preact": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "swiglu_mlp_gemm_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
     "swiglu_mlp_device_status": (_i32, [_vp]),
@@ -254,8 +255,12 @@ def bwd_workspace_views(workspace: torch.Tensor, M: int, H: int):
     return h, gp
 
 
+def swiglu_mlp_fwd_fp8_workspace_size(M: int, D: int, H: int, Dout: int) -> int:
+    return int(lib().swiglu_mlp_fwd_fp8_workspace_size(M, D, H, Dout))
+
+
 def swiglu_mlp_fwd_fp8(x8, W1_8, W2_8, s_x: float, s_w1: float, s_w2: float, s_h: float,
-                       preact=None, h8=None, y=None, store_preact: bool = True):
+                       preact=None, h8=None, y=None, store_preact: bool = True, workspace=None):
     """FP8 forward (E4M3 operands, per-tensor scales); returns (preact [M,2H] bf16 or
     None, h8 [M,H] E4M3, y [M,Dout] bf16)."""
     M, D = x8.shape
@@ -267,8 +272,12 @@ def swiglu_mlp_fwd_fp8(x8, W1_8, W2_8, s_x: float, s_w1: float, s_w2: float, s_h
         preact = _empty((M, 2 * H), x8)
     h8 = torch.empty(M, H, dtype=torch.float8_e4m3fn, device=x8.device) if h8 is None else h8
     y = _empty((M, Dout), x8) if y is None else y
+    if workspace is None:
+        n = swiglu_mlp_fwd_fp8_workspace_size(M, D, H, Dout)
+        workspace = torch.empty(n, dtype=torch.uint8, device=x8.device) if n else None
     st = lib().swiglu_mlp_fwd_fp8(_ptr(x8), _ptr(W1_8), _ptr(W2_8), s_x, s_w1, s_w2, s_h,
                                   _ptr(preact) if store_preact else None, _ptr(h8), _ptr(y), M, D, H, Dout,
+                                  _ptr(workspace), 0 if workspace is None else workspace.numel(),
                                   _stream(x8.device))
     _check(st, "swiglu_mlp_fwd_fp8")
     return (preact if store_preact else None), h8, y

@@ -53,7 +53,11 @@ struct SkinnyArgs {
     int debug_flags;
 };
 
+// OP: bf16 operands (kind::f16) or FP8 E4M3 operands (kind::f8f6f4, 128 k values per
+// 128-byte k-block; K-major weights only).  The fp32 sums are unscaled.
+template <int OP = OP_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __grid_constant__ SkinnyArgs args) {
+    constexpr int BKE = OP == OP_E4M3 ? 2 * BK : BK;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -128,7 +132,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
                     const uint32_t fb = full_bar(stage);
                     ptx::mbar_arrive_expect_tx(fb, tx);
                     last_parity[stage] = (int)phase;
-                    const int k0 = kb * BK;
+                    const int k0 = kb * BKE;
                     const uint32_t sA = base + stage * SK_A_BYTES;
                     const uint32_t sB = base + SK_OFF_B + stage * SK_B_BYTES;
                     if (w_mn) {
@@ -152,7 +156,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
     } else if (warp == 1) {
         if (lane == 0) {
             const bool w_mn = args.w_mn != 0;
-            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((w_mn ? 1u : 0u) << 15) |
+            const uint32_t fmt = OP == OP_E4M3 ? 0u : 1u;   // E4M3 or bf16
+            const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((w_mn ? 1u : 0u) << 15) |
                                    ((uint32_t)(n_mma >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
             int stage = 0;
             uint32_t phase = 0;
@@ -182,7 +187,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
                         const uint64_t ad = w_mn ? umma_desc_sw128(sA + k * 2048, 8192, 1024)
                                                  : umma_desc_sw128(sA + k * 32, 16, 1024);
                         const uint64_t bd = umma_desc_sw128(sB + k * 32, 16, 1024);
-                        ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        if (OP == OP_E4M3) ptx::mma_e4m3(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        else ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit(empty_bar(stage));
                     if (++stage == SK_STAGES) {
@@ -255,14 +261,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
 // element-wise finishing kernels (fp32 [N, ld] transposed sums -> bf16 outputs)
 // ---------------------------------------------------------------------------
 
-// out [M, N] bf16 = round(acc^T (+ res)), res [M, N] bf16 optional (the residual block)
+// out [M, N] bf16 = round(scale * acc^T (+ res)), res [M, N] bf16 optional (the
+// residual block); scale is 1 except for FP8 sums
 __global__ void skinny_cast_kernel(const float* __restrict__ acc, int ld, const __nv_bfloat16* __restrict__ res,
-                                   __nv_bfloat16* __restrict__ out, int M, int N) {
+                                   __nv_bfloat16* __restrict__ out, int M, int N, float scale = 1.0f) {
     const long long total = (long long)M * N;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
         const int m = (int)(i / N), n = (int)(i % N);
         const float r = res ? __bfloat162float(res[i]) : 0.0f;
-        out[i] = __float2bfloat16_rn(acc[(long long)n * ld + m] + r);
+        out[i] = __float2bfloat16_rn(scale * acc[(long long)n * ld + m] + r);
+    }
+}
+
+// FP8 SwiGLU forward from the unscaled fp32 sums preact^T [2H, ld]: preact [M, 2H]
+// (optional, bf16 of scale_acc * sum) and h8 [M, H] = E4M3(h * inv_s_h), h from the
+// bf16 preact as in the bf16 kernels; codes round to nearest even and saturate.
+__global__ void skinny_swiglu_fwd_fp8_kernel(const float* __restrict__ acc, int ld, float scale_acc, float inv_s_h,
+                                             __nv_bfloat16* __restrict__ preact, uint8_t* __restrict__ h8, int M,
+                                             int H) {
+    const long long total = (long long)M * H;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+        const int m = (int)(i / H), j = (int)(i % H);
+        const __nv_bfloat16 lb = __float2bfloat16_rn(scale_acc * acc[(long long)j * ld + m]);
+        const __nv_bfloat16 gb = __float2bfloat16_rn(scale_acc * acc[(long long)(H + j) * ld + m]);
+        if (preact) {
+            preact[(long long)m * 2 * H + j] = lb;
+            preact[(long long)m * 2 * H + H + j] = gb;
+        }
+        const float g = __bfloat162float(gb);
+        const float hv = __bfloat162float(lb) * round_bf16(g * sigmoid_mufu(g));
+        h8[i] = (uint8_t)(ptx::cvt_e4m3x2(hv * inv_s_h, 0.0f) & 0xFFu);
     }
 }
 

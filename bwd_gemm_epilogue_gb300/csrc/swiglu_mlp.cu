@@ -329,14 +329,24 @@ swiglu_status launch_traced(int kind, cudaStream_t stream, F&& do_launch) {
 // acc [N, ld] fp32 = W * X^T with W [N, K] (w_mn = 0) or [K, N] (w_mn = 1) and X [M, K];
 // split over K so the work units cover the SMs.  acc is zeroed here first.
 swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, const void* X, float* acc, int64_t N,
-                         int64_t K, int64_t M, cudaStream_t s) {
+                         int64_t K, int64_t M, cudaStream_t s, bool fp8 = false) {
     const int64_t ld = skinny_ld(M);
     cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)N * ld * 4, s);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync(skinny accumulator)", e);
     static thread_local SkinnyArgs a;
     std::memset(&a, 0, sizeof a);
-    if (!encode_operand(&a.w, W, N, K, w_mn, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny w)");
-    if (!encode_operand(&a.x, X, M, K, false, (uint32_t)ld)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny x)");
+    if (fp8) {
+        // E4M3 operands, K-major: 128 k values (bytes) per box row
+        constexpr CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        if (w_mn || !encode_2d(&a.w, W, (uint64_t)K, (uint64_t)N, (uint64_t)K, 2 * BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, U8))
+            return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny fp8 w)");
+        if (!encode_2d(&a.x, X, (uint64_t)K, (uint64_t)M, (uint64_t)K, 2 * BK, (uint32_t)ld, CU_TENSOR_MAP_SWIZZLE_128B, U8))
+            return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny fp8 x)");
+    } else {
+        if (!encode_operand(&a.w, W, N, K, w_mn, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny w)");
+        if (!encode_operand(&a.x, X, M, K, false, (uint32_t)ld))
+            return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny x)");
+    }
     {
         cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)N};
         cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
@@ -352,7 +362,7 @@ swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, co
     a.n_mma = (int)ld;
     a.w_mn = w_mn ? 1 : 0;
     a.n_tiles = (int)((N + BM - 1) / BM);
-    a.k_blocks = (int)((K + BK - 1) / BK);
+    a.k_blocks = (int)((K + (fp8 ? 2 * BK : BK) - 1) / (fp8 ? 2 * BK : BK));
     // Split count: the fewest splits whose makespan ceil(tiles * s / SMs) / s (in
     // whole-K tiles) is within 2% of the best over s = 1..32 with >= 2 k-blocks per
     // split (fewer splits, less fp32 reduce traffic and per-unit overhead).
@@ -369,12 +379,13 @@ swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, co
     a.timeout_ns = g_timeout_ns.load();
     a.err = st->err_word;
     a.debug_flags = g_debug_flags.load();
-    e = cudaFuncSetAttribute(skinny_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES);
+    auto kern = fp8 ? skinny_gemm_kernel<OP_E4M3> : skinny_gemm_kernel<OP_BF16>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(skinny smem)", e);
     const int units = a.n_tiles * a.splits;
     const int grid = units < st->num_sms ? units : st->num_sms;
     return launch_traced(kind, s, [&]() {
-        skinny_gemm_kernel<<<grid, NUM_THREADS, SK_SMEM_BYTES, s>>>(a);
+        kern<<<grid, NUM_THREADS, SK_SMEM_BYTES, s>>>(a);
         return cudaGetLastError();
     });
 }
@@ -1254,9 +1265,52 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
 namespace swiglu {
 namespace {
 
+// Workspace of the FP8 forward: for M <= 64 the fp32 sums preact^T [2H, M16] and
+// y^T [Dout, M16] (M16 = M rounded up to 16); nothing otherwise.
+size_t fp8_fwd_ws(int64_t M, int64_t H, int64_t Dout, float** pt, float** yt, void* base) {
+    if (!use_skinny(M)) return 0;
+    const size_t ld = (size_t)skinny_ld(M);
+    const size_t a = round256((size_t)2 * H * ld * 4);
+    if (base) {
+        *pt = static_cast<float*>(base);
+        *yt = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + a);
+    }
+    return a + round256((size_t)Dout * ld * 4);
+}
+
+// M <= 64 tokens: weight-streaming FP8 products (transposed, split over K) and
+// element-wise kernels that scale, apply the SwiGLU, quantise h and cast y.
+swiglu_status run_fwd_fp8_skinny(DeviceState* st, const void* x8, const void* W1_8, const void* W2_8, float s_x,
+                                 float s_w1, float s_w2, float s_h, void* preact, void* h8, void* y, int64_t M,
+                                 int64_t D, int64_t H, int64_t Dout, void* ws, cudaStream_t s) {
+    float *pt = nullptr, *yt = nullptr;
+    fp8_fwd_ws(M, H, Dout, &pt, &yt, ws);
+    const int ld = (int)skinny_ld(M);
+    swiglu_status rc = run_skinny(st, SWIGLU_KERNEL_FWD_PREACT, W1_8, false, x8, pt, 2 * H, D, M, s, true);
+    if (rc != SWIGLU_OK) return rc;
+    const int g = elementwise_grid(st, (long long)M * H);
+    rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
+        skinny_swiglu_fwd_fp8_kernel<<<g, 256, 0, s>>>(pt, ld, s_x * s_w1, 1.0f / s_h,
+                                                        static_cast<__nv_bfloat16*>(preact),
+                                                        static_cast<uint8_t*>(h8), (int)M, (int)H);
+        return cudaGetLastError();
+    });
+    if (rc != SWIGLU_OK) return rc;
+    rc = run_skinny(st, SWIGLU_KERNEL_FWD_DOWN, W2_8, false, h8, yt, Dout, H, M, s, true);
+    if (rc != SWIGLU_OK) return rc;
+    const int g2 = elementwise_grid(st, (long long)M * Dout);
+    return launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
+        skinny_cast_kernel<<<g2, 256, 0, s>>>(yt, ld, nullptr, static_cast<__nv_bfloat16*>(y), (int)M, (int)Dout,
+                                              s_h * s_w2);
+        return cudaGetLastError();
+    });
+}
+
 swiglu_status run_fwd_fp8(DeviceState* st, const void* x8, const void* W1_8, const void* W2_8, float s_x,
                           float s_w1, float s_w2, float s_h, void* preact, void* h8, void* y, int64_t M,
-                          int64_t D, int64_t H, int64_t Dout, cudaStream_t s) {
+                          int64_t D, int64_t H, int64_t Dout, void* ws, cudaStream_t s) {
+    if (use_skinny(M))
+        return run_fwd_fp8_skinny(st, x8, W1_8, W2_8, s_x, s_w1, s_w2, s_h, preact, h8, y, M, D, H, Dout, ws, s);
     constexpr CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const int cg = pick_cg(M);
     KernelArgs a;
@@ -1299,9 +1353,16 @@ swiglu_status run_fwd_fp8(DeviceState* st, const void* x8, const void* W1_8, con
 }  // namespace
 }  // namespace swiglu
 
+extern "C" size_t swiglu_mlp_fwd_fp8_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
+    (void)D;
+    if (M <= 0 || H <= 0 || Dout <= 0) return 0;
+    return fp8_fwd_ws(M, H, Dout, nullptr, nullptr, nullptr);
+}
+
 extern "C" swiglu_status swiglu_mlp_fwd_fp8(const void* x8, const void* W1_8, const void* W2_8, float s_x,
                                             float s_w1, float s_w2, float s_h, void* preact, void* h8, void* y,
-                                            int64_t M, int64_t D, int64_t H, int64_t Dout, void* stream) {
+                                            int64_t M, int64_t D, int64_t H, int64_t Dout, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
     if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
     if (D % 16 || H % 16 || !dims_ok(Dout) || D >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31) ||
         M >= (int64_t(1) << 31))
@@ -1311,11 +1372,13 @@ extern "C" swiglu_status swiglu_mlp_fwd_fp8(const void* x8, const void* W1_8, co
     if (M == 0) return SWIGLU_OK;
     if (!x8 || !W1_8 || !W2_8 || !h8 || !y) return SWIGLU_ERR_INVALID_ARG;
     if (!aligned16(x8) || !aligned16(W1_8) || !aligned16(W2_8) || !aligned16(h8) || !aligned16(y) ||
-        (preact && !aligned16(preact)))
+        (preact && !aligned16(preact)) || (workspace && !aligned16(workspace)))
         return SWIGLU_ERR_MISALIGNED;
+    const size_t need = swiglu_mlp_fwd_fp8_workspace_size(M, D, H, Dout);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
     DeviceState* st;
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
-    return run_fwd_fp8(st, x8, W1_8, W2_8, s_x, s_w1, s_w2, s_h, preact, h8, y, M, D, H, Dout,
+    return run_fwd_fp8(st, x8, W1_8, W2_8, s_x, s_w1, s_w2, s_h, preact, h8, y, M, D, H, Dout, workspace,
                        static_cast<cudaStream_t>(stream));
 }

@@ -141,12 +141,18 @@ swiglu_status swiglu_mlp_bwd_residual(const void* x, const void* W1, const void*
  *   y [M,Dout]     bf16 output: s_h * s_w2 * (h8 @ W2_8^T)
  * Both products run on the FP8 tensor cores with fp32 accumulators.  Needs D and H
  * multiples of 16 (16-byte rows of FP8), Dout a multiple of 8, positive finite
- * scales (SWIGLU_ERR_INVALID_ARG otherwise); no workspace (h8 is the caller's).
+ * scales (SWIGLU_ERR_INVALID_ARG otherwise).  For M <= 64 tokens (decode) the
+ * products stream the FP8 weights transposed and split over K, as in the bf16
+ * forward, into fp32 sums held in the workspace; element-wise kernels scale them,
+ * apply the SwiGLU, quantise h and cast y.  Larger M needs no workspace.
  */
+size_t swiglu_mlp_fwd_fp8_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
+
 swiglu_status swiglu_mlp_fwd_fp8(const void* x8, const void* W1_8, const void* W2_8,
                                  float s_x, float s_w1, float s_w2, float s_h,
                                  void* preact, void* h8, void* y,
-                                 int64_t M, int64_t D, int64_t H, int64_t Dout, void* stream);
+                                 int64_t M, int64_t D, int64_t H, int64_t Dout,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The fused segment alone: grad_h = dy @ W2 (never stored) and the SwiGLU

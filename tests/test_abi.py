@@ -131,10 +131,15 @@ def test_moe_argument_errors(lib):
 
 def test_fp8_forward_argument_errors(lib):
     def f(D=256, H=512, Do=256, sh=1.0, x=A16, h8=A16):
-        return lib.swiglu_mlp_fwd_fp8(x, A16, A16, 1.0, 1.0, 1.0, sh, None, h8, A16, 128, D, H, Do, None)
+        return lib.swiglu_mlp_fwd_fp8(x, A16, A16, 1.0, 1.0, 1.0, sh, None, h8, A16, 128, D, H, Do, None, 0, None)
 
     assert f(D=264) == 2                       # D not a multiple of 16
     assert f(H=520) == 2                       # H not a multiple of 16
     assert f(sh=0.0) == 1 and f(sh=-1.0) == 1  # scales must be positive
     assert f(x=None) == 1
     assert f(h8=A16 + 8) == 3
+    # few tokens need fp32 workspace sums
+    assert lib.swiglu_mlp_fwd_fp8_workspace_size(16, 4096, 11008, 4096) == 2 * 11008 * 16 * 4 + 4096 * 16 * 4
+    assert lib.swiglu_mlp_fwd_fp8_workspace_size(65, 4096, 11008, 4096) == 0
+    assert lib.swiglu_mlp_fwd_fp8(A16, A16, A16, 1.0, 1.0, 1.0, 1.0, None, A16, A16, 16, 256, 512, 256,
+                                  None, 0, None) == 4

@@ -90,3 +90,22 @@ def test_fp8_forward_full_size_sampled(b):
     parity(preact[rows], p_ref, "preact[rows]")
     check_codes(h8[rows], hpre, h8_ref, sc["s_h"], "h8[rows]")
     parity(y[rows], y_ref, "y[rows]")
+
+
+@pytest.mark.parametrize("M", [1, 16, 40, 64])
+@pytest.mark.parametrize("small_m_path", [True, False])
+def test_fp8_few_tokens(b, M, small_m_path):
+    # M <= 64: the FP8 weights stream through the transposed, K-split kernels (the
+    # decode path); test hook bit 3 keeps the 128/256-row tile kernels for comparison
+    s = Shape(M, 512, 1024, 768)
+    x8, W1_8, W2_8, sc = workloads.make_fp8_block(s, seed=93 + M, s_h=1.0 / 128)
+    p_ref, hpre, h8_ref, y_ref = oracle.fwd_fp8(x8, W1_8, W2_8, **sc)
+    b.swiglu_mlp_set_debug_flags(0 if small_m_path else 8)
+    try:
+        preact, h8, y = b.swiglu_mlp_fwd_fp8(x8.cuda(), W1_8.cuda(), W2_8.cuda(), **sc)
+        assert b.swiglu_mlp_device_status() == 0
+    finally:
+        b.swiglu_mlp_set_debug_flags(0)
+    parity(preact, p_ref, "preact")
+    check_codes(h8, hpre, h8_ref, sc["s_h"], "h8")
+    parity(y, y_ref, "y")
