@@ -204,6 +204,54 @@ def peaks():
 
 # ----------------------------------------------------------------------------- our arm
 
+def eager_comparison(step, x, W1, W2, dy, step_flops, dev, blocks: int = 4, n: int = 10):
+    """The pages' unfused drop-h step on the same GPU: torch.matmul (cuBLAS) for the five
+    GEMMs and eager element-wise kernels for the SwiGLU forward/backward, grad_h written to
+    and read back from HBM.  Timed in alternating blocks with this library's step (context
+    for the fused path, not a product path)."""
+    import torch
+    import torch.nn.functional as F
+
+    H = W2.shape[1]
+
+    def eager_step():
+        pre = x @ W1.t()
+        left, gate = pre[:, :H], pre[:, H:]
+        h = left * F.silu(gate)
+        _ = h @ W2.t()
+        gh = dy @ W2
+        sig = torch.sigmoid(gate)
+        silu = gate * sig
+        gp = torch.cat([gh * silu, gh * left * (sig + silu * (1 - sig))], dim=1)
+        h2 = left * silu
+        _ = gp @ W1
+        _ = gp.t() @ x
+        _ = dy.t() @ h2
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(3):
+        eager_step()
+        step()
+    torch.cuda.synchronize(dev)
+    ours, base = [], []
+    for b in range(blocks):
+        for name in (("ours", "eager") if b % 2 == 0 else ("eager", "ours")):
+            (ours if name == "ours" else base).append(timed(step if name == "ours" else eager_step))
+    o, e = statistics.median(ours), statistics.median(base)
+    return {"ms_per_step": round(e, 4), "tflops": round(step_flops / (e * 1e-3) / 1e12, 1),
+            "ours_ms_per_step_same_blocks": round(o, 4), "speedup": round(e / o, 3),
+            "what": "torch.matmul (cuBLAS) GEMMs + eager element-wise SwiGLU forward/backward (grad_h through HBM), "
+                    "the pages' unfused drop-h step, alternating blocks of 10 steps with this library's step"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -324,6 +372,10 @@ def run_ours(args):
         raise RuntimeError(f"e2e steps failed: {binding.swiglu_mlp_strerror(st)}")
     del runner
 
+    eager = None
+    if rank == 0 and ws_n == 1 and wl in ("target", "prefill") and not args.residual:
+        eager = eager_comparison(step, x, W1, W2, dy, flops["step"], dev)
+
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         pre_h = preact.cpu()
@@ -367,6 +419,7 @@ def run_ours(args):
                 "overlap": "h2d of step i+1 and d2h of step i-1 run during step i (3 streams)"},
         "gpu_launches": launches,
         "clocks": clk,
+        "cublas_eager_comparison": eager,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)

@@ -50,6 +50,7 @@ SIGNATURES = {
     "swiglu_mlp_last_error_detail": (ctypes.c_char_p, []),
     "swiglu_mlp_set_wait_timeout_ns": (None, [_u64]),
     "swiglu_mlp_set_debug_flags": (None, [_i32]),
+    "swiglu_mlp_set_raster_band": (None, [_i32]),
     "swiglu_mlp_trace_begin": (None, [_vp, _vp, _i32]),
     "swiglu_mlp_trace_end": (_i32, []),
     "swiglu_mlp_abi_version": (_i32, []),
@@ -144,6 +145,10 @@ def swiglu_mlp_set_wait_timeout_ns(ns: int) -> None:
 
 def swiglu_mlp_set_debug_flags(flags: int) -> None:
     lib().swiglu_mlp_set_debug_flags(int(flags))
+
+
+def swiglu_mlp_set_raster_band(n_tiles: int) -> None:
+    lib().swiglu_mlp_set_raster_band(int(n_tiles))
 
 
 def swiglu_mlp_abi_version() -> int:

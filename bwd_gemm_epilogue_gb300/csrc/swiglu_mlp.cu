@@ -30,6 +30,7 @@ __device__ int g_err_word;   // device error word: ERR_* bits of roles that gave
 
 std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
 std::atomic<int> g_debug_flags{0};
+std::atomic<int> g_raster_band{0};   // 0: the default band of 8 tiles
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -158,7 +159,8 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     p.K = (int)K;
     p.tiles_m = (int)((M + BM * cg - 1) / (BM * cg));
     p.tiles_n = (int)tiles_n;
-    p.band = p.tiles_n < 8 ? p.tiles_n : 8;
+    const int band = g_raster_band.load() > 0 ? g_raster_band.load() : 8;
+    p.band = p.tiles_n < band ? p.tiles_n : band;
     p.k_blocks = (int)((K + BK - 1) / BK);
     p.a_mn = a_mn ? 1 : 0;
     p.b_mn = b_mn ? 1 : 0;
@@ -782,6 +784,8 @@ const char* swiglu_mlp_last_error_detail(void) { return g_detail; }
 void swiglu_mlp_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
 void swiglu_mlp_set_debug_flags(int flags) { g_debug_flags.store(flags); }
+
+void swiglu_mlp_set_raster_band(int n_tiles) { g_raster_band.store(n_tiles > 0 ? n_tiles : 0); }
 
 void swiglu_mlp_trace_begin(void** events, int* kinds, int capacity) {
     Trace& tr = g_trace;

@@ -228,6 +228,12 @@ void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
  * to test each path.) */
 void swiglu_mlp_set_debug_flags(int flags);
 
+/* Tuning knob, process-wide: the width, in 256-column tiles, of the bands the tile
+ * kernels walk their output in (all rows of a band before the next band, so a band's
+ * B slabs stay in L2 while the A slabs stream past).  0 (the default) = 8.  Any
+ * value >= 1 computes the same result. */
+void swiglu_mlp_set_raster_band(int n_tiles);
+
 /* Kernel kinds reported by the launch trace. */
 typedef enum {
     SWIGLU_KERNEL_FWD_PREACT = 1,   /* x @ W1^T + SwiGLU forward epilogue */

@@ -424,3 +424,25 @@ def test_autograd_residual_block(b):
     parity(xg.grad, dx_ref, "dx")
     parity(w1g.grad, dW1_ref, "dW1")
     parity(w2g.grad, dW2_ref, "dW2")
+
+
+@pytest.mark.parametrize("band", [1, 3])
+def test_raster_band_setting_keeps_results(b, band):
+    # the tile walk order is a tuning knob: any band width computes the same block
+    s = Shape(600, 264, 520, 264)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=75)
+    pre_in = workloads.make_preact(s, seed=75, gate_sweep=True)
+    b.swiglu_mlp_set_raster_band(band)
+    try:
+        preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2))
+        dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(pre_in), dev(dy))
+        ok_status(b)
+    finally:
+        b.swiglu_mlp_set_raster_band(0)
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2)
+    parity(preact, p_ref, "preact")
+    parity(y, y_ref, "y")
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre_in, dy)
+    parity(dx, dx_ref, "dx")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
