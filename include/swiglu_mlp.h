@@ -224,8 +224,9 @@ void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
  * Bit 1: every GEMM uses single-CTA 128-row tiles instead of CTA-pair 256-row
  * tiles.  Bit 2: the backward launches dW2, dx and dW1 separately instead of as
  * one grouped launch.  Bit 3: M <= 64 keeps the 128-row tile path instead of the
- * small-M path.  (Every setting computes the same result; the bits exist
- * to test each path.) */
+ * small-M path.  Bit 4: MoE launches keep CTA-pair tiles even when 128-row tiles
+ * would compute fewer padded rows.  (Every setting computes the same result; the
+ * bits exist to test each path.) */
 void swiglu_mlp_set_debug_flags(int flags);
 
 /* Tuning knob, process-wide: the width, in 256-column tiles, of the bands the tile
