@@ -204,6 +204,35 @@ def peaks():
 
 # ----------------------------------------------------------------------------- our arm
 
+def graph_replay_timing(step, dev, K: int, step_flops: float):
+    """The same step captured once into a CUDA graph and replayed K times: the launch
+    gaps between the step's short kernels go away (the decode step is launch-bound)."""
+    import torch
+
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            step()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / K
+    return {"ms_per_step": round(ms, 4), "tflops": round(step_flops / (ms * 1e-3) / 1e12, 1),
+            "what": "one fwd+bwd step captured into a CUDA graph, replayed back to back"}
+
+
 def eager_comparison(step, x, W1, W2, dy, step_flops, dev, blocks: int = 4, n: int = 10):
     """The pages' unfused drop-h step on the same GPU: torch.matmul (cuBLAS) for the five
     GEMMs and eager element-wise kernels for the SwiGLU forward/backward, grad_h written to
@@ -372,6 +401,10 @@ def run_ours(args):
         raise RuntimeError(f"e2e steps failed: {binding.swiglu_mlp_strerror(st)}")
     del runner
 
+    graph = None
+    if wl == "decode":
+        graph = graph_replay_timing(step, dev, K, flops["step"])
+
     eager = None
     if rank == 0 and ws_n == 1 and wl in ("target", "prefill") and not args.residual:
         eager = eager_comparison(step, x, W1, W2, dy, flops["step"], dev)
@@ -420,6 +453,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk,
         "cublas_eager_comparison": eager,
+        "cuda_graph": graph,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -511,6 +545,9 @@ def run_stack(args):
         "data": "synthetic", "config": {"workload": "stack4: 4 SwiGLU blocks, M=11136 D=Dout=3584 H=14336"},
         "saved_activation_mib": round(st.saved_activation_bytes() / 2 ** 20, 1),
         "saved_activation_note": "x_0..x_4 and preact_1..4 kept for the backward (h dropped)",
+        "bwd_peak_mib": round(st.backward_peak_bytes() / 2 ** 20, 1),
+        "bwd_peak_note": "saved activations + one layer's backward workspace (h, grad_preact) + dx ping-pong "
+                         "+ all four layers' dW1/dW2; weights, x and dy excluded",
         "gpu_launches_per_step": 4 * (2 + 2), "clocks": clk}), flush=True)
 
 

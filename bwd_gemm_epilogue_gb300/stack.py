@@ -59,3 +59,11 @@ class SwiGLUStack:
         input (x_0 .. x_{L-1}), every preact, and the output."""
         t = self.acts + self.preacts
         return sum(a.numel() * a.element_size() for a in t)
+
+    def backward_peak_bytes(self) -> int:
+        """Device memory held at the backward's peak beyond the weights, x and dy (the
+        caller's): the saved activations, the backward workspace (h and grad_preact of
+        one layer), the dx ping-pong buffers and every layer's weight gradients.  The
+        forward's workspace (h) is idle during the backward and not counted."""
+        extra = [self.ws_b] + self.dacts + [g for pair in self.grads for g in pair]
+        return self.saved_activation_bytes() + sum(a.numel() * a.element_size() for a in extra)

@@ -446,3 +446,67 @@ def test_raster_band_setting_keeps_results(b, band):
     parity(dx, dx_ref, "dx")
     parity(dW1, dW1_ref, "dW1")
     parity(dW2, dW2_ref, "dW2")
+
+
+def test_fused_epilogue_special_values(b):
+    # gate at 0, +-1e4, +-1e30, +-inf and NaN; left at 0, 1, -2 and tiny values.  Large
+    # finite gates saturate sigma (silu -> g or -0, silu' -> 1 or 0); infinities and NaN
+    # give the inf / NaN pattern the definitions give (silu(-inf) = -inf * 0 = NaN,
+    # silu'(+inf) = 1 + inf * 0 = NaN), which the oracle reproduces in fp64.
+    s = Shape(128, 64, 256, 128)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=6)
+    vals = torch.tensor([0.0, 1e4, -1e4, 1e30, -1e30, float("inf"), float("-inf"), float("nan"), 0.5, -3.0])
+    lefts = torch.tensor([0.0, 1.0, -2.0, 1e-20])
+    gate = vals.repeat(s.M * s.H // vals.numel() + 1)[: s.M * s.H].reshape(s.M, s.H)
+    left = lefts.repeat(s.M * s.H // lefts.numel() + 1)[: s.M * s.H].reshape(s.M, s.H)
+    preact = torch.cat([left, gate], dim=1).to(torch.bfloat16)
+    _, gp_ref, h_ref, _ = oracle.bwd_rows(W1, W2, preact, dy)
+    gp, h = b.swiglu_mlp_fused_grad_preact(dev(dy), dev(W2), dev(preact))
+    ok_status(b)
+    for name, got, ref in (("grad_preact", gp, gp_ref), ("h", h, h_ref)):
+        g = got.float().cpu().double().numpy()
+        np.testing.assert_array_equal(np.isnan(g), np.isnan(ref), err_msg=f"{name}: NaN pattern")
+        np.testing.assert_array_equal(np.isposinf(g), np.isposinf(ref), err_msg=f"{name}: +inf pattern")
+        np.testing.assert_array_equal(np.isneginf(g), np.isneginf(ref), err_msg=f"{name}: -inf pattern")
+        fin = np.isfinite(ref)
+        assert fin.mean() > 0.5
+        big = fin & (np.abs(ref) >= 1e6)                   # the 1e30-scale entries, on their own
+        for part, sel in (("finite", fin & ~big), ("huge", big)):
+            parity(torch.from_numpy(np.where(sel, g, 0.0)), np.where(sel, ref, 0.0), f"{name} ({part} entries)")
+
+
+@pytest.mark.parametrize("M", [16, 300])
+def test_cuda_graph_replay_matches_direct_calls(b, M):
+    # the block's calls enqueue only kernels and memsets on the caller's stream, so a
+    # step can be captured into a CUDA graph; replays give the direct calls' bits
+    s = Shape(M, 256, 512, 256)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=76)
+    x, W1, W2, dy = dev(x), dev(W1), dev(W2), dev(dy)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    preact, y, dx = torch.empty(M, 1024, **bf), torch.empty(M, 256, **bf), torch.empty(M, 256, **bf)
+    dW1, dW2 = torch.empty(1024, 256, **bf), torch.empty(256, 512, **bf)
+    wsf = torch.empty(b.swiglu_mlp_fwd_workspace_size(M, 256, 512, 256), dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(b.swiglu_mlp_bwd_workspace_size(M, 256, 512, 256), dtype=torch.uint8, device="cuda")
+
+    def step():
+        b.swiglu_mlp_fwd(x, W1, W2, preact, y, wsf)
+        b.swiglu_mlp_bwd(x, W1, W2, preact, dy, dx, dW1, dW2, wsb)
+
+    step()
+    ok_status(b)
+    ref = [t.clone() for t in (preact, y, dx, dW1, dW2)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        step()
+    for t in (preact, y, dx, dW1, dW2):
+        t.zero_()
+    g.replay()
+    g.replay()
+    ok_status(b)
+    for name, got, want in zip(("preact", "y", "dx", "dW1", "dW2"), (preact, y, dx, dW1, dW2), ref):
+        assert torch.equal(got, want), name

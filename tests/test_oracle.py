@@ -485,3 +485,19 @@ def test_fp8_forward_against_the_bf16_oracle_and_fp64_matmul():
     r = oracle.fwd_fp8(x8, W1_8, W2_8, rows=[0, 17, 32], **sc)
     np.testing.assert_array_equal(r[2], h8[[0, 17, 32]])
     np.testing.assert_array_equal(r[3], y8[[0, 17, 32]])
+
+
+def test_identity_down_projection_passes_dy_through():
+    # W2 = I (H = Dout): grad_h = dy @ W2 = dy exactly, so the backward's grad_preact is
+    # [dy * silu(gate) | dy * left * silu'(gate)] element by element
+    s = workloads.Shape(12, 16, 24, 24)
+    _, x, W1, _, dy = workloads.make_block(s, seed=79)
+    W2 = torch.eye(24).to(torch.bfloat16)
+    preact = workloads.make_preact(s, seed=79)
+    gh, gp, _, _ = oracle.bwd_rows(W1, W2, preact, dy)
+    np.testing.assert_array_equal(gh, dy.double().numpy())
+    p = preact.double().numpy()
+    left, gate = p[:, :24], p[:, 24:]
+    sg = 1.0 / (1.0 + np.exp(-gate))
+    want_l = np.vectorize(oracle.round_bf16)(dy.double().numpy() * gate * sg)
+    np.testing.assert_allclose(gp[:, :24], want_l, rtol=0, atol=0)
