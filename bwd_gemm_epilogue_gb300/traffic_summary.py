@@ -5,7 +5,7 @@
 The CSV comes from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,
 gpu__time_duration.sum --csv --log-file dram.csv python bench.py ...` over launches of
 the target step.  Launches are mapped to kernel kinds by their template arguments
-(gemm_kernel<EPI, CG, SCHED>), averaged per kind, and written with a hash of the
+(gemm_kernel<EPI, CG, SCHED, OP>, bf16 operands), averaged per kind, and written with a hash of the
 kernel sources: bench.py reports a kind's traffic only while the sources still hash
 the same (a changed kernel invalidates its counters).
 """
@@ -36,10 +36,10 @@ def summarize(path: str) -> dict:
     for r in rows[hi + 1:]:
         if len(r) <= vi:
             continue
-        m = re.search(r"gemm_kernel<(\d+), (\d+), (\d+)>", r[ki])
-        if not m or m.groups() not in KINDS:
+        m = re.search(r"gemm_kernel<(\d+), (\d+), (\d+)(?:, (\d+))?>", r[ki])
+        if not m or m.group(4) not in (None, "0") or m.groups()[:3] not in KINDS:
             continue
-        d = per_launch.setdefault(r[ii], {"kind": KINDS[m.groups()]})
+        d = per_launch.setdefault(r[ii], {"kind": KINDS[m.groups()[:3]]})
         d[r[mi]] = float(r[vi].replace(",", "")) * scale.get(r[ui], 1)
     acc = {}
     for d in per_launch.values():
