@@ -154,8 +154,13 @@ struct Cfg {
     // buffers get what is left (CTA-pair SWIGLU_BWD: 5 stages, 2 preact slots and
     // single-buffered output tiles measured 7% faster than 4 / 3 / 2; single-CTA
     // SWIGLU_FWD: 4 stages and single-buffered outputs 11% faster than 3 / 2).
+    // The fused backward drains 16-column chunks (x16 TMEM loads, 32-byte staging rows):
+    // its preact slots and output tiles then take half the space, which buys a sixth
+    // operand stage for CTA pairs (a fourth for single CTAs).
+    static constexpr int CK = EPI == EPI_SWIGLU_BWD ? 16 : CHUNK;   // epilogue columns per chunk
     static constexpr int STAGES =
-        CG == 1 ? ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) ? 4 : 3) : (EPI == EPI_STORE ? 6 : 5);
+        CG == 1 ? ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) ? 4 : 3)
+                : ((EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD) ? 6 : 5);
     static constexpr bool STORE_ONLY = EPI == EPI_STORE || EPI == EPI_STORE_ADD;   // one bf16 output
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_ROWS = BN / CG;                        // B rows (N) held by this CTA
@@ -168,15 +173,15 @@ struct Cfg {
     // epilogues need too many registers for that and keep one warp per quadrant.
     static constexpr int EPI_WARPS = STORE_ONLY ? 8 : 4;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
-    static constexpr int OUT_TILE = 32 * CHUNK * 2;               // one warp's 32x32 bf16 tile
+    static constexpr int OUT_TILE = 32 * CK * 2;                  // one warp's 32 x CK bf16 tile
     static constexpr int OUT_BUFS =
-        ((EPI == EPI_SWIGLU_BWD && CG == 2) || (EPI == EPI_SWIGLU_FWD && CG == 1)) ? 1 : 2;
+        (EPI == EPI_SWIGLU_BWD || (EPI == EPI_SWIGLU_FWD && CG == 1)) ? 1 : 2;
     static constexpr int OUT_WARP_BYTES = OUT_BUFS * NOUT * OUT_TILE;
     // epilogue-input slots: preact left + gate (SWIGLU_BWD) or the residual (STORE_ADD)
     static constexpr int EIN_SLOTS = (EPI == EPI_SWIGLU_BWD || EPI == EPI_STORE_ADD) ? 2 : 0;
-    static constexpr int EIN_HALF = BM * CHUNK * 2;               // 128 rows x 32 cols bf16
+    static constexpr int EIN_HALF = BM * CK * 2;                  // 128 rows x CK cols bf16
     static constexpr int EIN_SLOT_BYTES = (EPI == EPI_SWIGLU_BWD ? 2 : 1) * EIN_HALF;
-    static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CHUNK : BN / CHUNK;
+    static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CK : BN / CK;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -370,6 +375,17 @@ __device__ __forceinline__ float sigmoid_mufu(float g) {
 // 16-byte unit `c` (0..3) of row `r` in a [rows][64 B] tile with 64-byte swizzle.
 __device__ __forceinline__ uint32_t sw64_offset(int r, int c) {
     return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// 16-byte unit `c` (0..1) of row `r` in a [rows][32 B] tile with 32-byte swizzle.
+__device__ __forceinline__ uint32_t sw32_offset(int r, int c) {
+    return (uint32_t)(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
+}
+
+// Unit `c` of row `r` in a staging tile of CK bf16 columns (64- or 32-byte rows).
+template <int CK>
+__device__ __forceinline__ uint32_t stage_offset(int r, int c) {
+    return CK == 32 ? sw64_offset(r, c) : sw32_offset(r, c);
 }
 
 // ---------------------------------------------------------------------------
@@ -642,8 +658,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
                     last_parity[slot] = (int)phase;
                     const uint32_t dst = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
-                    ptx::tma_load_3d(dst, mI, fb, j0 + c * CHUNK, 0, m0);
-                    ptx::tma_load_3d(dst + C::EIN_HALF, mI, fb, j0 + c * CHUNK, 1, m0);
+                    ptx::tma_load_3d(dst, mI, fb, j0 + c * C::CK, 0, m0);
+                    ptx::tma_load_3d(dst + C::EIN_HALF, mI, fb, j0 + c * C::CK, 1, m0);
                     if (++slot == C::EIN_SLOTS) {
                         slot = 0;
                         phase ^= 1u;
@@ -747,6 +763,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 if (EPI == EPI_SWIGLU_FWD) {
                     ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
                     ptx::tmem_ld_32x32b_x32(t_row + BN / 2 + c * CHUNK, acc2);
+                } else if (C::CK == 16) {
+                    ptx::tmem_ld_32x32b_x16(t_row + c * C::CK, *reinterpret_cast<uint32_t(*)[16]>(acc));
                 } else {
                     ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
                 }
@@ -793,9 +811,9 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     }
                     const uint32_t slot_base = base + C::OFF_EIN + ein_slot * C::EIN_SLOT_BYTES;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 l4 = ptx::lds128(slot_base + sw64_offset(row, q));
-                        const uint4 g4 = ptx::lds128(slot_base + C::EIN_HALF + sw64_offset(row, q));
+                    for (int q = 0; q < C::CK / 8; ++q) {
+                        const uint4 l4 = ptx::lds128(slot_base + stage_offset<C::CK>(row, q));
+                        const uint4 g4 = ptx::lds128(slot_base + C::EIN_HALF + stage_offset<C::CK>(row, q));
                         lft[4 * q + 0] = l4.x; lft[4 * q + 1] = l4.y; lft[4 * q + 2] = l4.z; lft[4 * q + 3] = l4.w;
                         gte[4 * q + 0] = g4.x; gte[4 * q + 1] = g4.y; gte[4 * q + 2] = g4.z; gte[4 * q + 3] = g4.w;
                     }
@@ -856,7 +874,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < C::CK / 2; ++i) {
                         float dl[2], dg[2], hv[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
@@ -891,8 +909,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         continue;
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        ptx::sts128(tile + sw64_offset(lane, q),
+                    for (int q = 0; q < C::CK / 8; ++q)
+                        ptx::sts128(tile + stage_offset<C::CK>(lane, q),
                                     make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]));
                 }
                 ptx::fence_proxy_async_smem();
@@ -903,7 +921,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
                     } else {
                         const int jw = (EPI == EPI_SWIGLU_FWD) ? BN / 2 : BN;
-                        const int j = tn * jw + c * CHUNK;
+                        const int j = tn * jw + c * C::CK;
                         if (j < n_limit) {
                             if (!pr.no_o0) {
                                 ptx::tma_store_3d(mO0, ob_base, j, 0, mrow0);

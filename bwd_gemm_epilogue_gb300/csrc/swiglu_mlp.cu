@@ -130,14 +130,22 @@ bool encode_operand(CUtensorMap* m, const void* ptr, int64_t mn, int64_t k, bool
     return encode_2d(m, ptr, (uint64_t)k, (uint64_t)mn, (uint64_t)k * 2, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// [M, 2H] tensor seen as (j, half, m): element (j, half, m) = base[m*2H + half*H + j].
-bool encode_paired(CUtensorMap* m, const void* ptr, int64_t M, int64_t H, uint32_t box_rows) {
-    return encode_3d(m, ptr, (uint64_t)H, 2, (uint64_t)M, (uint64_t)H * 2, (uint64_t)H * 4, CHUNK, 1, box_rows,
-                     CU_TENSOR_MAP_SWIZZLE_64B);
+// Epilogue tiles are `box_cols` bf16 wide: 32 columns (64-byte rows, 64-byte swizzle) or
+// the fused backward's 16 (32-byte rows, 32-byte swizzle).
+CUtensorMapSwizzle epi_swizzle(uint32_t box_cols) {
+    return box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
 }
 
-bool encode_out_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
-    return encode_2d(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols * 2, CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+// [M, 2H] tensor seen as (j, half, m): element (j, half, m) = base[m*2H + half*H + j].
+bool encode_paired(CUtensorMap* m, const void* ptr, int64_t M, int64_t H, uint32_t box_rows,
+                   uint32_t box_cols = CHUNK) {
+    return encode_3d(m, ptr, (uint64_t)H, 2, (uint64_t)M, (uint64_t)H * 2, (uint64_t)H * 4, box_cols, 1, box_rows,
+                     epi_swizzle(box_cols));
+}
+
+bool encode_out_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, uint32_t box_cols = CHUNK) {
+    return encode_2d(m, ptr, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols * 2, box_cols, 32,
+                     epi_swizzle(box_cols));
 }
 
 // Host-only test hook bit: run every GEMM with single-CTA tiles.
@@ -497,9 +505,11 @@ swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, con
     if (!encode_operand(&a.a[0], dy, M, Dout, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
     // B(n = j, k = o) = W2[o, j]: MN-major
     if (!encode_operand(&a.b[0], W2, H, Dout, true, 0)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
-    if (!encode_paired(&a.o0[0], grad_preact, M, H, 32)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
-    if (!encode_out_2d(&a.o1, h, M, H)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
-    if (!encode_paired(&a.i0, preact, M, H, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
+    constexpr uint32_t ck = Cfg<EPI_SWIGLU_BWD, 2>::CK;
+    static_assert(ck == Cfg<EPI_SWIGLU_BWD, 1>::CK, "one chunk width for both tile sizes");
+    if (!encode_paired(&a.o0[0], grad_preact, M, H, 32, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
+    if (!encode_out_2d(&a.o1, h, M, H, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
+    if (!encode_paired(&a.i0, preact, M, H, BM, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
     a.num_problems = 1;
     a.prob[0] = make_problem(M, H, Dout, (H + BN - 1) / BN, false, true, cg);
     if (cg == 2) return launch<EPI_SWIGLU_BWD, 2, SRC_SINGLE>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
@@ -1222,9 +1232,10 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
         std::memset(&t, 0, sizeof t);
         bool ok = encode_operand(&t.a, at_row<uint8_t>(dy, off[e], Dout), m, Dout, false, BM);
         ok = ok && encode_operand(&t.b, at_row<uint8_t>(W2, e * Dout, H), H, Dout, true, 0);
-        ok = ok && encode_paired(&t.o0, at_row<uint8_t>(gp, off[e], 2 * H), m, H, 32);
-        ok = ok && encode_out_2d(&t.o1, at_row<uint8_t>(h, off[e], H), m, H);
-        ok = ok && encode_paired(&t.i0, at_row<uint8_t>(preact, off[e], 2 * H), m, H, BM);
+        constexpr uint32_t ck = Cfg<EPI_SWIGLU_BWD, 2>::CK;
+        ok = ok && encode_paired(&t.o0, at_row<uint8_t>(gp, off[e], 2 * H), m, H, 32, ck);
+        ok = ok && encode_out_2d(&t.o1, at_row<uint8_t>(h, off[e], H), m, H, ck);
+        ok = ok && encode_paired(&t.i0, at_row<uint8_t>(preact, off[e], 2 * H), m, H, BM, ck);
         if (!ok) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe grad_h)");
         t.prob = make_problem(m, H, Dout, (H + BN - 1) / BN, false, true, cg);
     }
