@@ -8,9 +8,12 @@
 //   C^T [N, M] += W [N, K-slice] * X [M, K-slice]^T
 //
 // with the weight W as the 128-row tcgen05 A operand (K-major, or MN-major when W
-// is stored transposed) and the tokens X as an N = 16..64 B operand.  The K range
-// is split so that (N / 128) x splits work units cover the SMs; every unit adds its
-// 128 x M fp32 partial into a zero-initialised fp32 buffer with a TMA reduce-add.
+// is stored transposed) and the tokens X as an N = 16..64 B operand.  The work --
+// (N / 128) weight tiles x K / 64 k-blocks -- is dealt out evenly ("stream-K"): CTA b
+// of G streams the k-blocks [b * total / G, (b + 1) * total / G) of the tile-major
+// sequence, so every SM reads the same share of the weights.  Each piece of a tile a
+// CTA covers adds its 128 x M fp32 partial into a zero-initialised fp32 buffer with a
+// TMA reduce-add.
 // Element-wise kernels then round and transpose the fp32 sums into the bf16 outputs
 // and apply the SwiGLU forward or backward -- for M tokens grad_h is M x H fp32
 // (0.7 MB at decode sizes), so it is written once to global memory and read once
@@ -47,7 +50,7 @@ struct SkinnyArgs {
     int N, K;
     int n_mma;          // tokens rounded up to a multiple of 16 (MMA N)
     int w_mn;           // weight stored [K, N] (N contiguous)
-    int n_tiles, splits, kb_per_split, k_blocks;
+    int n_tiles, k_blocks;
     unsigned long long timeout_ns;
     int* err;
     int debug_flags;
@@ -67,7 +70,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
     const unsigned long long tmo = args.timeout_ns;
     int* const err = args.err;
     const int n_mma = args.n_mma;
-    const int units = args.n_tiles * args.splits;
+    // this CTA's share of the tile-major (tile, k-block) sequence
+    const long long total = (long long)args.n_tiles * args.k_blocks;
+    const long long share_lo = total * blockIdx.x / gridDim.x;
+    const long long share_hi = total * (blockIdx.x + 1) / gridDim.x;
 
     const uint32_t bar0 = base + SK_OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -103,13 +109,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    // work unit u: weight rows [128 * (u % n_tiles), +128), k-blocks of split u / n_tiles
-    auto unit_range = [&](int u, int& n0, int& kb0, int& kb1) {
-        const int tile = u % args.n_tiles;
-        const int split = u / args.n_tiles;
+    // piece at position pos of the share: weight rows [128 * tile, +128), k-blocks
+    // [kb0, kb1) -- up to the end of the tile or of the share; pos advances by kb1 - kb0
+    auto piece = [&](long long pos, int& n0, int& kb0, int& kb1) {
+        const int tile = (int)(pos / args.k_blocks);
         n0 = tile * BM;
-        kb0 = split * args.kb_per_split;
-        kb1 = min(args.k_blocks, kb0 + args.kb_per_split);
+        kb0 = (int)(pos - (long long)tile * args.k_blocks);
+        kb1 = (int)min((long long)args.k_blocks, kb0 + (share_hi - pos));
     };
 
     if (warp == 0) {
@@ -121,9 +127,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
             const uint32_t tx = SK_A_BYTES + (uint32_t)n_mma * BK * 2;
             const bool w_mn = args.w_mn != 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                int n0, kb0, kb1;
-                unit_range(u, n0, kb0, kb1);
+            int n0, kb0, kb1;
+            for (long long pos = share_lo; pos < share_hi && ok; pos += kb1 - kb0) {
+                piece(pos, n0, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
                         ok = false;
@@ -163,9 +169,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
-                int n0, kb0, kb1;
-                unit_range(u, n0, kb0, kb1);
+            int n0, kb0, kb1;
+            for (long long pos = share_lo; pos < share_hi && ok; pos += kb1 - kb0, ++local) {
+                piece(pos, n0, kb0, kb1);
                 const int ab = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
                 if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, tmo, err, abort_flag, ERR_MMA)) {
@@ -210,9 +216,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
         const uint32_t out_tile = base + SK_OFF_OUT + wq * SK_OUT_WARP;
         int local = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
-            int n0, kb0, kb1;
-            unit_range(u, n0, kb0, kb1);
+        int n0, kb0, kb1;
+        for (long long pos = share_lo; pos < share_hi && ok; pos += kb1 - kb0, ++local) {
+            piece(pos, n0, kb0, kb1);
             const int ab = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             const bool got = __all_sync(0xffffffffu,

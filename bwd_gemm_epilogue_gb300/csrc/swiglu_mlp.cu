@@ -337,7 +337,8 @@ swiglu_status launch_traced(int kind, cudaStream_t stream, F&& do_launch) {
 }
 
 // acc [N, ld] fp32 = W * X^T with W [N, K] (w_mn = 0) or [K, N] (w_mn = 1) and X [M, K];
-// split over K so the work units cover the SMs.  acc is zeroed here first.
+// the k-blocks of all weight tiles dealt out evenly over the SMs (each CTA reduce-adds
+// the partial sums of the pieces it covers).  acc is zeroed here first.
 swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, const void* X, float* acc, int64_t N,
                          int64_t K, int64_t M, cudaStream_t s, bool fp8 = false) {
     const int64_t ld = skinny_ld(M);
@@ -373,27 +374,15 @@ swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, co
     a.w_mn = w_mn ? 1 : 0;
     a.n_tiles = (int)((N + BM - 1) / BM);
     a.k_blocks = (int)((K + (fp8 ? 2 * BK : BK) - 1) / (fp8 ? 2 * BK : BK));
-    // Split count: the fewest splits whose makespan ceil(tiles * s / SMs) / s (in
-    // whole-K tiles) is within 2% of the best over s = 1..32 with >= 2 k-blocks per
-    // split (fewer splits, less fp32 reduce traffic and per-unit overhead).
-    auto span_of = [&](int sp) {
-        const long long units = (long long)a.n_tiles * sp;
-        return (double)((units + st->num_sms - 1) / st->num_sms) / sp;
-    };
-    double best = span_of(1);
-    for (int sp = 2; sp <= 32 && sp * 2 <= a.k_blocks; ++sp) best = span_of(sp) < best ? span_of(sp) : best;
-    int splits = 1;
-    while (span_of(splits) > best * 1.02) ++splits;
-    a.kb_per_split = (a.k_blocks + splits - 1) / splits;
-    a.splits = (a.k_blocks + a.kb_per_split - 1) / a.kb_per_split;   // every split non-empty
     a.timeout_ns = g_timeout_ns.load();
     a.err = st->err_word;
     a.debug_flags = g_debug_flags.load();
     auto kern = fp8 ? skinny_gemm_kernel<OP_E4M3> : skinny_gemm_kernel<OP_BF16>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(skinny smem)", e);
-    const int units = a.n_tiles * a.splits;
-    const int grid = units < st->num_sms ? units : st->num_sms;
+    // stream-K: every CTA streams an equal share of the n_tiles x k_blocks k-blocks
+    const long long total = (long long)a.n_tiles * a.k_blocks;
+    const int grid = (int)(total < st->num_sms ? total : st->num_sms);
     return launch_traced(kind, s, [&]() {
         kern<<<grid, NUM_THREADS, SK_SMEM_BYTES, s>>>(a);
         return cudaGetLastError();

@@ -76,7 +76,9 @@ size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Do
  * h = bf16(left * bf16(silu(gate))), then y = h @ W2^T.  For M <= 64 tokens
  * (decode) the two products run transposed with the weights as the 128-row MMA
  * operand, split over K into fp32 workspace sums, and small element-wise kernels
- * apply the SwiGLU and round to bf16.
+ * apply the SwiGLU and round to bf16.  The split sums are added in an order that
+ * varies between runs, so for M <= 64 results can differ in the last bf16 bit from
+ * run to run; the 128/256-row tile kernels (M > 64) are deterministic.
  */
 swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2,
                              void* preact, void* y,
