@@ -515,3 +515,17 @@ def test_cuda_graph_replay_matches_direct_calls(b, M):
             # few tokens: several CTAs reduce-add fp32 partials into the same rows in an
             # order that varies from run to run, so bf16 results may differ in the last bit
             parity(got, want.double().cpu().numpy(), name)
+
+
+@pytest.mark.parametrize("s", [Shape(301, 264, 392, 136), Shape(65, 128, 256, 128), Shape(1000, 520, 264, 72)],
+                         ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
+def test_backward_token_counts_not_multiple_of_8(b, bwd_mode, s):
+    # ragged token counts: the weight gradients' K (= M) ends inside a 64-token k-block
+    _, x, W1, W2, dy = workloads.make_block(s, seed=77)
+    preact = workloads.make_preact(s, seed=77, gate_sweep=True)
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, preact, dy)
+    dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(preact), dev(dy))
+    ok_status(b)
+    parity(dx, dx_ref, "dx")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
