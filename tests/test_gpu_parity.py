@@ -529,3 +529,31 @@ def test_backward_token_counts_not_multiple_of_8(b, bwd_mode, s):
     parity(dx, dx_ref, "dx")
     parity(dW1, dW1_ref, "dW1")
     parity(dW2, dW2_ref, "dW2")
+
+
+def _random_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.choice([int(rng.integers(1, 65)), int(rng.integers(65, 700))]))
+        D, H, Dout = (8 * int(rng.integers(1, 80)) for _ in range(3))
+        out.append(Shape(M, D, H, Dout))
+    return out
+
+
+@pytest.mark.parametrize("s", _random_shapes(24, 2026), ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
+def test_random_shapes_forward_backward(b, s):
+    # seeded random sizes (M in 1..699, D / H / Dout multiples of 8 up to 632): every tile
+    # size, ragged tail and path choice the host makes for them
+    _, x, W1, W2, dy = workloads.make_block(s, seed=s.M + 7 * s.H)
+    pre_in = workloads.make_preact(s, seed=s.D + s.Dout, gate_sweep=True)
+    preact, y = b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2))
+    dx, dW1, dW2 = b.swiglu_mlp_bwd(dev(x), dev(W1), dev(W2), dev(pre_in), dev(dy))
+    ok_status(b)
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2)
+    parity(preact, p_ref, "preact")
+    parity(y, y_ref, "y")
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre_in, dy)
+    parity(dx, dx_ref, "dx")
+    parity(dW1, dW1_ref, "dW1")
+    parity(dW2, dW2_ref, "dW2")
