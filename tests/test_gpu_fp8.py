@@ -109,3 +109,21 @@ def test_fp8_few_tokens(b, M, small_m_path):
     parity(preact, p_ref, "preact")
     check_codes(h8, hpre, h8_ref, sc["s_h"], "h8")
     parity(y, y_ref, "y")
+
+
+def _random_fp8_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    return [Shape(int(rng.choice([int(rng.integers(1, 65)), int(rng.integers(65, 600))])),
+                  16 * int(rng.integers(1, 40)), 16 * int(rng.integers(1, 40)), 8 * int(rng.integers(1, 80)))
+            for _ in range(n)]
+
+
+@pytest.mark.parametrize("s", _random_fp8_shapes(10, 31), ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
+def test_fp8_random_shapes(b, s):
+    x8, W1_8, W2_8, sc = workloads.make_fp8_block(s, seed=95 + s.M, s_h=1.0 / 128)
+    p_ref, hpre, h8_ref, y_ref = oracle.fwd_fp8(x8, W1_8, W2_8, **sc)
+    preact, h8, y = b.swiglu_mlp_fwd_fp8(x8.cuda(), W1_8.cuda(), W2_8.cuda(), **sc)
+    assert b.swiglu_mlp_device_status() == 0
+    parity(preact, p_ref, "preact")
+    check_codes(h8, hpre, h8_ref, sc["s_h"], "h8")
+    parity(y, y_ref, "y")

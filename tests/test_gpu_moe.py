@@ -174,3 +174,38 @@ def test_moe_host_step_runner_matches_direct_calls(b):
     for o in outs:
         for k, ref in (("y", y), ("dx", dx), ("dW1", dW1), ("dW2", dW2)):
             assert torch.equal(o[k], ref.cpu()), k
+
+
+def _random_moe(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        E = int(rng.integers(1, 13))
+        counts = [int(c) if rng.random() > 0.2 else 0 for c in rng.integers(0, 400, size=E)]
+        D, H, Dout = (8 * int(rng.integers(1, 50)) for _ in range(3))
+        out.append((counts, D, H, Dout))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_moe(8, 77), ids=lambda c: f"E{len(c[0])}_T{sum(c[0])}_D{c[1]}_H{c[2]}")
+def test_moe_random_layers(b, case):
+    counts, D, H, Dout = case
+    x, W1, W2, dy, preact = _experts(counts, D, H, Dout, seed=84 + len(counts))
+    p_ref, _, y_ref = oracle.moe_fwd(x, W1, W2, counts)
+    _, gp_ref, _, dx_ref, dW1_ref, dW2_ref = oracle.moe_bwd_full(x, W1, W2, preact, dy, counts)
+    T = sum(counts)
+    ws = torch.empty(max(16, b.swiglu_moe_bwd_workspace_size(counts, D, H, Dout)), dtype=torch.uint8, device="cuda")
+    pre_gpu, y = b.swiglu_moe_fwd(dev(x), dev(W1), dev(W2), counts)
+    dx, dW1, dW2 = b.swiglu_moe_bwd(dev(x), dev(W1), dev(W2), dev(preact), dev(dy), counts, workspace=ws)
+    assert b.swiglu_mlp_device_status() == 0
+    if T:
+        parity(pre_gpu, p_ref, "preact")
+        parity(y, y_ref, "y")
+        parity(b.bwd_workspace_views(ws, T, H)[1], gp_ref, "grad_preact")
+        parity(dx, dx_ref, "dx")
+    for e in range(len(counts)):
+        if counts[e]:
+            parity(dW1[e], dW1_ref[e], f"dW1[{e}]")
+            parity(dW2[e], dW2_ref[e], f"dW2[{e}]")
+        else:
+            assert dW1[e].abs().max().item() == 0 and dW2[e].abs().max().item() == 0
