@@ -376,6 +376,12 @@ def run_ours(args):
                     "traffic": measured_traffic(dom, wl if not args.residual else "residual"),
                     "peak_source": f"{pk_src} bf16_tflops_sustained (kernel timed inside a long step)"}
     fused = kstats.get("bwd_grad_h", {})
+    # forward / backward kernel time per step: every step launches the same sequence, the
+    # forward's kernels (element-wise ones included) before the first backward kernel
+    per_step = max(1, len(recs) // K)
+    nf = next((i for i, (k, _) in enumerate(recs[:per_step]) if k.startswith("bwd")), per_step)
+    fwd_ms = sum(t for i, (_, t) in enumerate(recs) if i % per_step < nf) / K
+    bwd_ms = max(1e-9, sum(t for i, (_, t) in enumerate(recs) if i % per_step >= nf) / K)
 
     # ---- end to end: pinned host inputs in, results out, every step; copies of
     # neighbouring steps overlap this step's compute (HostStepRunner)
@@ -441,9 +447,13 @@ def run_ours(args):
         "step_hbm_gbs_compulsory": round(step_bytes / (ms * 1e-3) / 1e9, 1),
         "fused_grad_preact_us": fused.get("avg_us"),
         "fused_grad_preact_tflops": fused.get("tflops"),
-        "fwd_ms": round(sum(kstats[k]["avg_us"] for k in ("fwd_preact", "fwd_down")) / 1e3, 4),
-        "bwd_ms": round(sum(kstats[k]["avg_us"] for k in ("bwd_grad_h", "bwd_dW2", "bwd_dx", "bwd_dW1", "bwd_gemms")
-                            if k in kstats) / 1e3, 4),
+        "fwd_ms": round(fwd_ms, 4),
+        "bwd_ms": round(bwd_ms, 4),
+        "fwd_tflops": round(flops["fwd"] / (fwd_ms * 1e-3) / 1e12, 1),
+        "bwd_tflops": round(flops["bwd"] / (bwd_ms * 1e-3) / 1e12, 1),
+        "fwd_frac_of_sustained_peak": round(flops["fwd"] / (fwd_ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 3),
+        "bwd_frac_of_sustained_peak": round(flops["bwd"] / (bwd_ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"], 3),
+        "fused_grad_preact_frac_of_sustained_peak": fused.get("frac_of_sustained_peak"),
         "kernels": kstats,
         "roofline": roofline,
         "cpu_baseline": cpu,
