@@ -8,12 +8,11 @@
 //   C^T [N, M] += W [N, K-slice] * X [M, K-slice]^T
 //
 // with the weight W as the 128-row tcgen05 A operand (K-major, or MN-major when W
-// is stored transposed) and the tokens X as an N = 16..64 B operand.  The work --
-// (N / 128) weight tiles x K / 64 k-blocks -- is dealt out evenly ("stream-K"): CTA b
-// of G streams the k-blocks [b * total / G, (b + 1) * total / G) of the tile-major
-// sequence, so every SM reads the same share of the weights.  Each piece of a tile a
-// CTA covers adds its 128 x M fp32 partial into a zero-initialised fp32 buffer with a
-// TMA reduce-add.
+// is stored transposed) and the tokens X as an N = 16..64 B operand.  The K range is
+// split so that (N / 128) x splits work units cover the SMs; work unit (tile, split)
+// stores its 128 x M fp32 partial into plane `split` of an fp32 buffer [splits][N][ld]
+// with a TMA store.  The element-wise kernels add the planes in a fixed order, so the
+// results are the same bits on every run (no order-dependent reduction).
 // Element-wise kernels then round and transpose the fp32 sums into the bf16 outputs
 // and apply the SwiGLU forward or backward -- for M tokens grad_h is M x H fp32
 // (0.7 MB at decode sizes), so it is written once to global memory and read once
@@ -21,7 +20,7 @@
 //
 // Warp roles as in gemm_kernel.cuh: warp 0 TMA producer, warp 1 TMEM owner and MMA
 // issuer (two accumulators of <= 64 fp32 columns), warps 4..7 drain TMEM, stage the
-// fp32 tile in shared memory and issue the reduce-adds.  Every wait is bounded.
+// fp32 tile in shared memory and issue the stores.  Every wait is bounded.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -46,11 +45,11 @@ constexpr uint32_t SK_TMEM_COLS = 128;                  // 2 x 64 fp32 columns
 struct SkinnyArgs {
     CUtensorMap w;      // weight (MMA A): K-major box 64 x 128, or MN-major box 64 x 64 (two per stage)
     CUtensorMap x;      // tokens (MMA B) [M, K]: K-major box 64 x n_mma
-    CUtensorMap out;    // fp32 [N, n_mma] accumulation buffer: box 16 x 32, 64-byte swizzle
+    CUtensorMap out;    // fp32 partial planes (m, n, split) of [splits][N][n_mma]: box 16 x 32 x 1, 64-byte swizzle
     int N, K;
     int n_mma;          // tokens rounded up to a multiple of 16 (MMA N)
     int w_mn;           // weight stored [K, N] (N contiguous)
-    int n_tiles, k_blocks;
+    int n_tiles, splits, kb_per_split, k_blocks;
     unsigned long long timeout_ns;
     int* err;
     int debug_flags;
@@ -70,10 +69,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
     const unsigned long long tmo = args.timeout_ns;
     int* const err = args.err;
     const int n_mma = args.n_mma;
-    // this CTA's share of the tile-major (tile, k-block) sequence
-    const long long total = (long long)args.n_tiles * args.k_blocks;
-    const long long share_lo = total * blockIdx.x / gridDim.x;
-    const long long share_hi = total * (blockIdx.x + 1) / gridDim.x;
+    const int units = args.n_tiles * args.splits;
 
     const uint32_t bar0 = base + SK_OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -109,13 +105,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    // piece at position pos of the share: weight rows [128 * tile, +128), k-blocks
-    // [kb0, kb1) -- up to the end of the tile or of the share; pos advances by kb1 - kb0
-    auto piece = [&](long long pos, int& n0, int& kb0, int& kb1) {
-        const int tile = (int)(pos / args.k_blocks);
+    // work unit u: weight rows [128 * (u % n_tiles), +128), k-blocks of split u / n_tiles
+    auto unit_range = [&](int u, int& n0, int& kb0, int& kb1) {
+        const int tile = u % args.n_tiles;
+        const int split = u / args.n_tiles;
         n0 = tile * BM;
-        kb0 = (int)(pos - (long long)tile * args.k_blocks);
-        kb1 = (int)min((long long)args.k_blocks, kb0 + (share_hi - pos));
+        kb0 = split * args.kb_per_split;
+        kb1 = min(args.k_blocks, kb0 + args.kb_per_split);
     };
 
     if (warp == 0) {
@@ -127,9 +123,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
             const uint32_t tx = SK_A_BYTES + (uint32_t)n_mma * BK * 2;
             const bool w_mn = args.w_mn != 0;
             bool ok = true;
-            int n0, kb0, kb1;
-            for (long long pos = share_lo; pos < share_hi && ok; pos += kb1 - kb0) {
-                piece(pos, n0, kb0, kb1);
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int n0, kb0, kb1;
+                unit_range(u, n0, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
                         ok = false;
@@ -169,9 +165,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            int n0, kb0, kb1;
-            for (long long pos = share_lo; pos < share_hi && ok; pos += kb1 - kb0, ++local) {
-                piece(pos, n0, kb0, kb1);
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+                int n0, kb0, kb1;
+                unit_range(u, n0, kb0, kb1);
                 const int ab = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
                 if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, tmo, err, abort_flag, ERR_MMA)) {
@@ -216,9 +212,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
         const uint32_t out_tile = base + SK_OFF_OUT + wq * SK_OUT_WARP;
         int local = 0;
         bool ok = true;
-        int n0, kb0, kb1;
-        for (long long pos = share_lo; pos < share_hi && ok; pos += kb1 - kb0, ++local) {
-            piece(pos, n0, kb0, kb1);
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+            int n0, kb0, kb1;
+            unit_range(u, n0, kb0, kb1);
+            const int split = u / args.n_tiles;
             const int ab = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             const bool got = __all_sync(0xffffffffu,
@@ -230,7 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
             ptx::tc_fence_after();
             const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * SK_MAX_M);
             const int chunks = n_mma / 16;
-            // the previous unit's reduce-adds must have read the staging tile
+            // the previous unit's stores must have read the staging tile
             if (lane == 0) ptx::bulk_wait_group_read<0>();
             __syncwarp();
             for (int c = 0; c < chunks; ++c) {
@@ -248,7 +245,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && n0 + 32 * wq < args.N) {
-                for (int c = 0; c < chunks; ++c) ptx::tma_reduce_add_2d(&args.out, out_tile + c * 2048, 16 * c, n0 + 32 * wq);
+                for (int c = 0; c < chunks; ++c)
+                    ptx::tma_store_3d(&args.out, out_tile + c * 2048, 16 * c, n0 + 32 * wq, split);
             }
             if (lane == 0) ptx::bulk_commit_group();
         }
@@ -267,29 +265,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) skinny_gemm_kernel(const __gri
 // element-wise finishing kernels (fp32 [N, ld] transposed sums -> bf16 outputs)
 // ---------------------------------------------------------------------------
 
+// The fp32 partial planes of the split-K products: element (row n, token m) of the
+// sum is the planes' values added in plane order (a fixed order: the same bits on
+// every run).
+struct Planes {
+    const float* p;
+    int ld;                // tokens per row (M rounded up to 16)
+    int count;             // splits
+    long long stride;      // elements per plane (rows * ld)
+    __device__ __forceinline__ float at(long long row, int m) const {
+        const float* q = p + row * ld + m;
+        float s = q[0];
+#pragma unroll 8
+        for (int k = 1; k < count; ++k) s += q[k * stride];   // loads independent, adds in plane order
+        return s;
+    }
+};
+
 // out [M, N] bf16 = round(scale * acc^T (+ res)), res [M, N] bf16 optional (the
 // residual block); scale is 1 except for FP8 sums
-__global__ void skinny_cast_kernel(const float* __restrict__ acc, int ld, const __nv_bfloat16* __restrict__ res,
+__global__ void skinny_cast_kernel(Planes acc, const __nv_bfloat16* __restrict__ res,
                                    __nv_bfloat16* __restrict__ out, int M, int N, float scale = 1.0f) {
     const long long total = (long long)M * N;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
         const int m = (int)(i / N), n = (int)(i % N);
         const float r = res ? __bfloat162float(res[i]) : 0.0f;
-        out[i] = __float2bfloat16_rn(scale * acc[(long long)n * ld + m] + r);
+        out[i] = __float2bfloat16_rn(scale * acc.at(n, m) + r);
     }
 }
 
 // FP8 SwiGLU forward from the unscaled fp32 sums preact^T [2H, ld]: preact [M, 2H]
 // (optional, bf16 of scale_acc * sum) and h8 [M, H] = E4M3(h * inv_s_h), h from the
 // bf16 preact as in the bf16 kernels; codes round to nearest even and saturate.
-__global__ void skinny_swiglu_fwd_fp8_kernel(const float* __restrict__ acc, int ld, float scale_acc, float inv_s_h,
+__global__ void skinny_swiglu_fwd_fp8_kernel(Planes acc, float scale_acc, float inv_s_h,
                                              __nv_bfloat16* __restrict__ preact, uint8_t* __restrict__ h8, int M,
                                              int H) {
     const long long total = (long long)M * H;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
         const int m = (int)(i / H), j = (int)(i % H);
-        const __nv_bfloat16 lb = __float2bfloat16_rn(scale_acc * acc[(long long)j * ld + m]);
-        const __nv_bfloat16 gb = __float2bfloat16_rn(scale_acc * acc[(long long)(H + j) * ld + m]);
+        const __nv_bfloat16 lb = __float2bfloat16_rn(scale_acc * acc.at(j, m));
+        const __nv_bfloat16 gb = __float2bfloat16_rn(scale_acc * acc.at(H + j, m));
         if (preact) {
             preact[(long long)m * 2 * H + j] = lb;
             preact[(long long)m * 2 * H + H + j] = gb;
@@ -302,13 +317,13 @@ __global__ void skinny_swiglu_fwd_fp8_kernel(const float* __restrict__ acc, int 
 
 // SwiGLU forward from the fp32 preact^T [2H, ld]: preact [M, 2H] and h [M, H],
 // h = bf16(left * bf16(silu(gate))) with left, gate the bf16-rounded preact.
-__global__ void skinny_swiglu_fwd_kernel(const float* __restrict__ acc, int ld, __nv_bfloat16* __restrict__ preact,
+__global__ void skinny_swiglu_fwd_kernel(Planes acc, __nv_bfloat16* __restrict__ preact,
                                          __nv_bfloat16* __restrict__ h, int M, int H) {
     const long long total = (long long)M * H;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
         const int m = (int)(i / H), j = (int)(i % H);
-        const __nv_bfloat16 lb = __float2bfloat16_rn(acc[(long long)j * ld + m]);
-        const __nv_bfloat16 gb = __float2bfloat16_rn(acc[(long long)(H + j) * ld + m]);
+        const __nv_bfloat16 lb = __float2bfloat16_rn(acc.at(j, m));
+        const __nv_bfloat16 gb = __float2bfloat16_rn(acc.at(H + j, m));
         preact[(long long)m * 2 * H + j] = lb;
         preact[(long long)m * 2 * H + H + j] = gb;
         const float g = __bfloat162float(gb);
@@ -318,14 +333,13 @@ __global__ void skinny_swiglu_fwd_kernel(const float* __restrict__ acc, int ld, 
 
 // SwiGLU backward from the fp32 grad_h^T [H, ld] and the saved preact:
 // grad_preact [M, 2H] = [grad_h * silu(gate) | grad_h * left * silu'(gate)], h [M, H].
-__global__ void skinny_swiglu_bwd_kernel(const float* __restrict__ acc, int ld,
-                                         const __nv_bfloat16* __restrict__ preact,
+__global__ void skinny_swiglu_bwd_kernel(Planes acc, const __nv_bfloat16* __restrict__ preact,
                                          __nv_bfloat16* __restrict__ grad_preact, __nv_bfloat16* __restrict__ h, int M,
                                          int H) {
     const long long total = (long long)M * H;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
         const int m = (int)(i / H), j = (int)(i % H);
-        const float gh = acc[(long long)j * ld + m];
+        const float gh = acc.at(j, m);
         const float l = __bfloat162float(preact[(long long)m * 2 * H + j]);
         const float g = __bfloat162float(preact[(long long)m * 2 * H + H + j]);
         const float sig = sigmoid_mufu(g);

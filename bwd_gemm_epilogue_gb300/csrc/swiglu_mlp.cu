@@ -336,14 +336,43 @@ swiglu_status launch_traced(int kind, cudaStream_t stream, F&& do_launch) {
     return SWIGLU_OK;
 }
 
-// acc [N, ld] fp32 = W * X^T with W [N, K] (w_mn = 0) or [K, N] (w_mn = 1) and X [M, K];
-// the k-blocks of all weight tiles dealt out evenly over the SMs (each CTA reduce-adds
-// the partial sums of the pieces it covers).  acc is zeroed here first.
+// Split-K plan of one small-M product with N weight rows and reduction length K: the
+// fewest splits whose makespan ceil(tiles * s / SMs) / s (in whole-K tiles) is within 2 %
+// of the best over s = 1..32 with >= 2 k-blocks per split.  Planned for the GB300's 152
+// SMs, so that the workspace queries (which see no device) and the launches agree.
+constexpr int kPlanSms = 152;
+struct SkinnyPlan {
+    int n_tiles, k_blocks, kb_per_split, splits;
+};
+SkinnyPlan skinny_plan(int64_t N, int64_t K, bool fp8) {
+    SkinnyPlan p;
+    const int bke = fp8 ? 2 * BK : BK;
+    p.n_tiles = (int)((N + BM - 1) / BM);
+    p.k_blocks = (int)((K + bke - 1) / bke);
+    auto span_of = [&](int sp) {
+        const long long units = (long long)p.n_tiles * sp;
+        return (double)((units + kPlanSms - 1) / kPlanSms) / sp;
+    };
+    double best = span_of(1);
+    for (int sp = 2; sp <= 32 && sp * 2 <= p.k_blocks; ++sp) best = span_of(sp) < best ? span_of(sp) : best;
+    int splits = 1;
+    while (span_of(splits) > best * 1.02) ++splits;
+    p.kb_per_split = (p.k_blocks + splits - 1) / splits;
+    p.splits = (p.k_blocks + p.kb_per_split - 1) / p.kb_per_split;   // every split non-empty
+    return p;
+}
+
+// Bytes of the fp32 partial planes [splits][N][M16] of one small-M product.
+size_t skinny_acc_bytes(int64_t N, int64_t K, int64_t M, bool fp8) {
+    return (size_t)skinny_plan(N, K, fp8).splits * (size_t)N * (size_t)skinny_ld(M) * 4;
+}
+
+// Partial planes of acc^T [N, M16] = W * X^T with W [N, K] (w_mn = 0) or [K, N] (w_mn = 1)
+// and X [M, K]: work unit (tile, split) stores its 128 x M16 partial into plane `split`;
+// *planes describes them for the element-wise kernels, which add them in plane order.
 swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, const void* X, float* acc, int64_t N,
-                         int64_t K, int64_t M, cudaStream_t s, bool fp8 = false) {
+                         int64_t K, int64_t M, cudaStream_t s, bool fp8, Planes* planes) {
     const int64_t ld = skinny_ld(M);
-    cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)N * ld * 4, s);
-    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync(skinny accumulator)", e);
     static thread_local SkinnyArgs a;
     std::memset(&a, 0, sizeof a);
     if (fp8) {
@@ -358,31 +387,34 @@ swiglu_status run_skinny(DeviceState* st, int kind, const void* W, bool w_mn, co
         if (!encode_operand(&a.x, X, M, K, false, (uint32_t)ld))
             return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny x)");
     }
+    const SkinnyPlan plan = skinny_plan(N, K, fp8);
     {
-        cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)N};
-        cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-        cuuint32_t box[2] = {16, 32};
-        cuuint32_t estr[2] = {1, 1};
-        if (g_encode(&a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr,
+        cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)N, (cuuint64_t)plan.splits};
+        cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)N * ld * 4};
+        cuuint32_t box[3] = {16, 32, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode(&a.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, acc, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny accumulator)");
+            return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (skinny partial planes)");
     }
     a.N = (int)N;
     a.K = (int)K;
     a.n_mma = (int)ld;
     a.w_mn = w_mn ? 1 : 0;
-    a.n_tiles = (int)((N + BM - 1) / BM);
-    a.k_blocks = (int)((K + (fp8 ? 2 * BK : BK) - 1) / (fp8 ? 2 * BK : BK));
+    a.n_tiles = plan.n_tiles;
+    a.k_blocks = plan.k_blocks;
+    a.kb_per_split = plan.kb_per_split;
+    a.splits = plan.splits;
     a.timeout_ns = g_timeout_ns.load();
     a.err = st->err_word;
     a.debug_flags = g_debug_flags.load();
+    *planes = Planes{acc, (int)ld, plan.splits, (long long)N * ld};
     auto kern = fp8 ? skinny_gemm_kernel<OP_E4M3> : skinny_gemm_kernel<OP_BF16>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SK_SMEM_BYTES);
     if (e != cudaSuccess) return fail(SWIGLU_ERR_LAUNCH, "cudaFuncSetAttribute(skinny smem)", e);
-    // stream-K: every CTA streams an equal share of the n_tiles x k_blocks k-blocks
-    const long long total = (long long)a.n_tiles * a.k_blocks;
-    const int grid = (int)(total < st->num_sms ? total : st->num_sms);
+    const int units = plan.n_tiles * plan.splits;
+    const int grid = units < st->num_sms ? units : st->num_sms;
     return launch_traced(kind, s, [&]() {
         kern<<<grid, NUM_THREADS, SK_SMEM_BYTES, s>>>(a);
         return cudaGetLastError();
@@ -398,17 +430,16 @@ int elementwise_grid(DeviceState* st, long long total) {
 struct SkinnyFwdWs { void* h; float* pt; float* yt; };
 struct SkinnyBwdWs { void* h; void* gp; float* gt; float* dxt; };
 
-size_t skinny_fwd_ws(int64_t M, int64_t H, int64_t Dout, SkinnyFwdWs* w, void* base);
-size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, SkinnyBwdWs* w, void* base);
+size_t skinny_fwd_ws(int64_t M, int64_t D, int64_t H, int64_t Dout, SkinnyFwdWs* w, void* base);
+size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, int64_t Dout, SkinnyBwdWs* w, void* base);
 
 bool dims_ok(int64_t v) { return v > 0 && v % 8 == 0 && v < (int64_t(1) << 31); }
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Workspace layouts of the small-M path: the regular buffers first (h; h and
-// grad_preact), then the fp32 transposed accumulators.
-size_t skinny_fwd_ws(int64_t M, int64_t H, int64_t Dout, SkinnyFwdWs* w, void* base) {
-    const int64_t ld = skinny_ld(M);
+// grad_preact), then the fp32 partial planes of the transposed products.
+size_t skinny_fwd_ws(int64_t M, int64_t D, int64_t H, int64_t Dout, SkinnyFwdWs* w, void* base) {
     size_t off = 0;
     auto take = [&](size_t bytes) {
         uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
@@ -416,14 +447,13 @@ size_t skinny_fwd_ws(int64_t M, int64_t H, int64_t Dout, SkinnyFwdWs* w, void* b
         return p;
     };
     uint8_t* h = take((size_t)M * H * 2);
-    uint8_t* pt = take((size_t)2 * H * ld * 4);
-    uint8_t* yt = take((size_t)Dout * ld * 4);
+    uint8_t* pt = take(skinny_acc_bytes(2 * H, D, M, false));     // preact^T planes, K = D
+    uint8_t* yt = take(skinny_acc_bytes(Dout, H, M, false));      // y^T planes, K = H
     if (w) *w = SkinnyFwdWs{h, reinterpret_cast<float*>(pt), reinterpret_cast<float*>(yt)};
     return off;
 }
 
-size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, SkinnyBwdWs* w, void* base) {
-    const int64_t ld = skinny_ld(M);
+size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, int64_t Dout, SkinnyBwdWs* w, void* base) {
     size_t off = 0;
     auto take = [&](size_t bytes) {
         uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
@@ -432,8 +462,8 @@ size_t skinny_bwd_ws(int64_t M, int64_t D, int64_t H, SkinnyBwdWs* w, void* base
     };
     uint8_t* h = take((size_t)M * H * 2);
     uint8_t* gp = take((size_t)M * 2 * H * 2);
-    uint8_t* gt = take((size_t)H * ld * 4);
-    uint8_t* dxt = take((size_t)D * ld * 4);
+    uint8_t* gt = take(skinny_acc_bytes(H, Dout, M, false));      // grad_h^T planes, K = Dout
+    uint8_t* dxt = take(skinny_acc_bytes(D, 2 * H, M, false));    // dx^T planes, K = 2H
     if (w) *w = SkinnyBwdWs{h, gp, reinterpret_cast<float*>(gt), reinterpret_cast<float*>(dxt)};
     return off;
 }
@@ -443,22 +473,22 @@ swiglu_status run_fwd_skinny(DeviceState* st, const void* x, const void* W1, con
                              int64_t M, int64_t D, int64_t H, int64_t Dout, void* ws, cudaStream_t s,
                              bool residual) {
     SkinnyFwdWs w;
-    skinny_fwd_ws(M, H, Dout, &w, ws);
-    const int ld = (int)skinny_ld(M);
-    swiglu_status rc = run_skinny(st, SWIGLU_KERNEL_FWD_PREACT, W1, false, x, w.pt, 2 * H, D, M, s);   // preact^T
+    skinny_fwd_ws(M, D, H, Dout, &w, ws);
+    Planes pt, yt;
+    swiglu_status rc = run_skinny(st, SWIGLU_KERNEL_FWD_PREACT, W1, false, x, w.pt, 2 * H, D, M, s, false, &pt);
     if (rc != SWIGLU_OK) return rc;
     const int g = elementwise_grid(st, (long long)M * H);
     rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-        skinny_swiglu_fwd_kernel<<<g, 256, 0, s>>>(w.pt, ld, static_cast<__nv_bfloat16*>(preact),
+        skinny_swiglu_fwd_kernel<<<g, 256, 0, s>>>(pt, static_cast<__nv_bfloat16*>(preact),
                                                     static_cast<__nv_bfloat16*>(w.h), (int)M, (int)H);
         return cudaGetLastError();
     });
     if (rc != SWIGLU_OK) return rc;
-    rc = run_skinny(st, SWIGLU_KERNEL_FWD_DOWN, W2, false, w.h, w.yt, Dout, H, M, s);   // y^T
+    rc = run_skinny(st, SWIGLU_KERNEL_FWD_DOWN, W2, false, w.h, w.yt, Dout, H, M, s, false, &yt);   // y^T
     if (rc != SWIGLU_OK) return rc;
     const int g2 = elementwise_grid(st, (long long)M * Dout);
     return launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-        skinny_cast_kernel<<<g2, 256, 0, s>>>(w.yt, ld, residual ? static_cast<const __nv_bfloat16*>(x) : nullptr,
+        skinny_cast_kernel<<<g2, 256, 0, s>>>(yt, residual ? static_cast<const __nv_bfloat16*>(x) : nullptr,
                                               static_cast<__nv_bfloat16*>(y), (int)M, (int)Dout);
         return cudaGetLastError();
     });
@@ -574,14 +604,14 @@ extern "C" {
 size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
     (void)D;
     if (M <= 0 || H <= 0) return 0;
-    if (M <= SK_MAX_M && Dout > 0) return skinny_fwd_ws(M, H, Dout, nullptr, nullptr);
+    if (M <= SK_MAX_M && Dout > 0 && D > 0) return skinny_fwd_ws(M, D, H, Dout, nullptr, nullptr);
     return round256((size_t)M * (size_t)H * 2);
 }
 
 size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
     (void)Dout;
     if (M <= 0 || H <= 0) return 0;
-    if (M <= SK_MAX_M && D > 0) return skinny_bwd_ws(M, D, H, nullptr, nullptr);
+    if (M <= SK_MAX_M && D > 0 && Dout > 0) return skinny_bwd_ws(M, D, H, Dout, nullptr, nullptr);
     return round256((size_t)M * (size_t)H * 2) + round256((size_t)M * (size_t)H * 4);
 }
 
@@ -649,23 +679,23 @@ static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, con
     if (use_skinny(M)) {
         // M <= 64 tokens: weight-streaming products transposed and split over K
         SkinnyBwdWs w;
-        skinny_bwd_ws(M, D, H, &w, workspace);
-        const int ld = (int)skinny_ld(M);
-        rc = run_skinny(st, SWIGLU_KERNEL_BWD_GRAD_H, W2, true, dy, w.gt, H, Dout, M, s);   // grad_h^T = W2^T dy^T
+        skinny_bwd_ws(M, D, H, Dout, &w, workspace);
+        Planes gt, dxt;
+        rc = run_skinny(st, SWIGLU_KERNEL_BWD_GRAD_H, W2, true, dy, w.gt, H, Dout, M, s, false, &gt);   // grad_h^T
         if (rc != SWIGLU_OK) return rc;
         const int ge = elementwise_grid(st, (long long)M * H);
         rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-            skinny_swiglu_bwd_kernel<<<ge, 256, 0, s>>>(w.gt, ld, static_cast<const __nv_bfloat16*>(preact),
+            skinny_swiglu_bwd_kernel<<<ge, 256, 0, s>>>(gt, static_cast<const __nv_bfloat16*>(preact),
                                                          static_cast<__nv_bfloat16*>(w.gp),
                                                          static_cast<__nv_bfloat16*>(w.h), (int)M, (int)H);
             return cudaGetLastError();
         });
         if (rc != SWIGLU_OK) return rc;
-        rc = run_skinny(st, SWIGLU_KERNEL_BWD_DX, W1, true, w.gp, w.dxt, D, 2 * H, M, s);   // dx^T = W1^T gp^T
+        rc = run_skinny(st, SWIGLU_KERNEL_BWD_DX, W1, true, w.gp, w.dxt, D, 2 * H, M, s, false, &dxt);   // dx^T
         if (rc != SWIGLU_OK) return rc;
         const int gc = elementwise_grid(st, (long long)M * D);
         rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-            skinny_cast_kernel<<<gc, 256, 0, s>>>(w.dxt, ld, residual ? static_cast<const __nv_bfloat16*>(dy) : nullptr,
+            skinny_cast_kernel<<<gc, 256, 0, s>>>(dxt, residual ? static_cast<const __nv_bfloat16*>(dy) : nullptr,
                                                   static_cast<__nv_bfloat16*>(dx), (int)M, (int)D);
             return cudaGetLastError();
         });
@@ -1277,15 +1307,14 @@ namespace {
 
 // Workspace of the FP8 forward: for M <= 64 the fp32 sums preact^T [2H, M16] and
 // y^T [Dout, M16] (M16 = M rounded up to 16); nothing otherwise.
-size_t fp8_fwd_ws(int64_t M, int64_t H, int64_t Dout, float** pt, float** yt, void* base) {
+size_t fp8_fwd_ws(int64_t M, int64_t D, int64_t H, int64_t Dout, float** pt, float** yt, void* base) {
     if (!use_skinny(M)) return 0;
-    const size_t ld = (size_t)skinny_ld(M);
-    const size_t a = round256((size_t)2 * H * ld * 4);
+    const size_t a = round256(skinny_acc_bytes(2 * H, D, M, true));
     if (base) {
         *pt = static_cast<float*>(base);
         *yt = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + a);
     }
-    return a + round256((size_t)Dout * ld * 4);
+    return a + round256(skinny_acc_bytes(Dout, H, M, true));
 }
 
 // M <= 64 tokens: weight-streaming FP8 products (transposed, split over K) and
@@ -1294,23 +1323,23 @@ swiglu_status run_fwd_fp8_skinny(DeviceState* st, const void* x8, const void* W1
                                  float s_w1, float s_w2, float s_h, void* preact, void* h8, void* y, int64_t M,
                                  int64_t D, int64_t H, int64_t Dout, void* ws, cudaStream_t s) {
     float *pt = nullptr, *yt = nullptr;
-    fp8_fwd_ws(M, H, Dout, &pt, &yt, ws);
-    const int ld = (int)skinny_ld(M);
-    swiglu_status rc = run_skinny(st, SWIGLU_KERNEL_FWD_PREACT, W1_8, false, x8, pt, 2 * H, D, M, s, true);
+    fp8_fwd_ws(M, D, H, Dout, &pt, &yt, ws);
+    Planes ptp, ytp;
+    swiglu_status rc = run_skinny(st, SWIGLU_KERNEL_FWD_PREACT, W1_8, false, x8, pt, 2 * H, D, M, s, true, &ptp);
     if (rc != SWIGLU_OK) return rc;
     const int g = elementwise_grid(st, (long long)M * H);
     rc = launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-        skinny_swiglu_fwd_fp8_kernel<<<g, 256, 0, s>>>(pt, ld, s_x * s_w1, 1.0f / s_h,
+        skinny_swiglu_fwd_fp8_kernel<<<g, 256, 0, s>>>(ptp, s_x * s_w1, 1.0f / s_h,
                                                         static_cast<__nv_bfloat16*>(preact),
                                                         static_cast<uint8_t*>(h8), (int)M, (int)H);
         return cudaGetLastError();
     });
     if (rc != SWIGLU_OK) return rc;
-    rc = run_skinny(st, SWIGLU_KERNEL_FWD_DOWN, W2_8, false, h8, yt, Dout, H, M, s, true);
+    rc = run_skinny(st, SWIGLU_KERNEL_FWD_DOWN, W2_8, false, h8, yt, Dout, H, M, s, true, &ytp);
     if (rc != SWIGLU_OK) return rc;
     const int g2 = elementwise_grid(st, (long long)M * Dout);
     return launch_traced(SWIGLU_KERNEL_ELEMENTWISE, s, [&]() {
-        skinny_cast_kernel<<<g2, 256, 0, s>>>(yt, ld, nullptr, static_cast<__nv_bfloat16*>(y), (int)M, (int)Dout,
+        skinny_cast_kernel<<<g2, 256, 0, s>>>(ytp, nullptr, static_cast<__nv_bfloat16*>(y), (int)M, (int)Dout,
                                               s_h * s_w2);
         return cudaGetLastError();
     });
@@ -1366,7 +1395,7 @@ swiglu_status run_fwd_fp8(DeviceState* st, const void* x8, const void* W1_8, con
 extern "C" size_t swiglu_mlp_fwd_fp8_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
     (void)D;
     if (M <= 0 || H <= 0 || Dout <= 0) return 0;
-    return fp8_fwd_ws(M, H, Dout, nullptr, nullptr, nullptr);
+    return fp8_fwd_ws(M, D, H, Dout, nullptr, nullptr, nullptr);
 }
 
 extern "C" swiglu_status swiglu_mlp_fwd_fp8(const void* x8, const void* W1_8, const void* W2_8, float s_x,

@@ -57,13 +57,14 @@ typedef enum {
 } swiglu_status;
 
 /* Bytes of workspace swiglu_mlp_fwd needs: the transient h [M,H] bf16; for M <= 64
- * also two fp32 accumulators of the small-M path (preact^T [2H, M16] and
- * y^T [Dout, M16], M16 = M rounded up to 16), each on a 256-byte boundary. */
+ * also the small-M path's fp32 partial sums of preact^T [2H, M16] and y^T [Dout, M16]
+ * (M16 = M rounded up to 16), one plane per K split (the split counts are planned for
+ * 152 SMs), each buffer on a 256-byte boundary. */
 size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
 
 /* Bytes of workspace swiglu_mlp_bwd needs: h [M,H] and grad_preact [M,2H], bf16,
  * each starting on a 256-byte boundary; for M <= 64 also the small-M path's fp32
- * accumulators grad_h^T [H, M16] and dx^T [D, M16]. */
+ * partial sums of grad_h^T [H, M16] and dx^T [D, M16], one plane per K split. */
 size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
 
 /*
@@ -76,9 +77,9 @@ size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Do
  * h = bf16(left * bf16(silu(gate))), then y = h @ W2^T.  For M <= 64 tokens
  * (decode) the two products run transposed with the weights as the 128-row MMA
  * operand, split over K into fp32 workspace sums, and small element-wise kernels
- * apply the SwiGLU and round to bf16.  The split sums are added in an order that
- * varies between runs, so for M <= 64 results can differ in the last bf16 bit from
- * run to run; the 128/256-row tile kernels (M > 64) are deterministic.
+ * apply the SwiGLU and round to bf16.  Each K split writes its own fp32 partial and
+ * the element-wise kernels add them in a fixed order, so every path returns the same
+ * bits on every run.
  */
 swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2,
                              void* preact, void* y,

@@ -32,8 +32,10 @@ def test_workspace_sizes():
     # ragged: each buffer starts on a 256-byte boundary
     assert b.swiglu_mlp_bwd_workspace_size(3, 8, 8, 8) == 256 + 256 + 512 + 512   # + small-M fp32 sums
     assert b.swiglu_mlp_bwd_workspace_size(65, 8, 8, 8) == 1280 + 2304            # M > 64: h, grad_preact
-    # small-M forward: h, preact^T [2H, 16], y^T [Dout, 16] (fp32)
-    assert b.swiglu_mlp_fwd_workspace_size(16, 4096, 11008, 4096) == 16 * 11008 * 2 + 2 * 11008 * 16 * 4 + 4096 * 16 * 4
+    # small-M forward: h, then one fp32 partial plane per K split of preact^T [2H, 16] and of
+    # y^T [Dout, 16]; for 16 tokens at 4096 x 11008 the split-K plan (152 SMs) uses 7 and 14
+    assert b.swiglu_mlp_fwd_workspace_size(16, 4096, 11008, 4096) == \
+        16 * 11008 * 2 + 7 * 2 * 11008 * 16 * 4 + 14 * 4096 * 16 * 4
 
 
 def test_strerror_and_version():
@@ -139,7 +141,8 @@ def test_fp8_forward_argument_errors(lib):
     assert f(x=None) == 1
     assert f(h8=A16 + 8) == 3
     # few tokens need fp32 workspace sums
-    assert lib.swiglu_mlp_fwd_fp8_workspace_size(16, 4096, 11008, 4096) == 2 * 11008 * 16 * 4 + 4096 * 16 * 4
+    # fp32 partial planes: 7 K splits of preact^T, 13 of y^T (128-value FP8 k-blocks)
+    assert lib.swiglu_mlp_fwd_fp8_workspace_size(16, 4096, 11008, 4096) == 7 * 2 * 11008 * 16 * 4 + 13 * 4096 * 16 * 4
     assert lib.swiglu_mlp_fwd_fp8_workspace_size(65, 4096, 11008, 4096) == 0
     assert lib.swiglu_mlp_fwd_fp8(A16, A16, A16, 1.0, 1.0, 1.0, 1.0, None, A16, A16, 16, 256, 512, 256,
                                   None, 0, None) == 4
