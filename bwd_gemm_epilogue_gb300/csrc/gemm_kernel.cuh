@@ -1,20 +1,25 @@
 // gemm_kernel.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a with
-// the SwiGLU MLP block's three epilogues.
+// the SwiGLU MLP block's epilogues.
 //
-//   C[M, N] = A[M, K] * B[N, K]^T        bf16 in, fp32 accumulate in TMEM
+//   C[M, N] = A[M, K] * B[N, K]^T        bf16 (or FP8 E4M3) in, fp32 accumulate in TMEM
 //
 // A and B are each either K-major (K contiguous in memory) or MN-major (M or N
 // contiguous); the TMA boxes and the UMMA shared-memory descriptors differ, the
-// rest of the kernel does not.  One CTA per SM, 256 threads:
+// rest of the kernel does not.  Template parameters: EPI (epilogue, below), CG (1 or
+// 2 CTAs per tile), SCHED (where the launch's problems and tile order come from: one
+// problem, up to three in the parameter block, or a table in global memory -- the
+// experts of an MoE layer) and OP (bf16 or E4M3 operands).  One CTA per SM:
 //
 //   warp 0      TMA producer: A/B k-blocks into a STAGES-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma into one of two TMEM
 //               accumulators (2 x 256 fp32 columns = all 512 TMEM columns)
-//   warp 2      epilogue-input producer (SWIGLU_BWD only): TMA-prefetches the
-//               saved preact left/gate sub-tiles the epilogue consumes
+//   warp 2      epilogue-input producer (SWIGLU_BWD and STORE_ADD): TMA-prefetches
+//               the saved preact left/gate sub-tiles, or the residual tiles, that
+//               the epilogue consumes
 //   warp 3      idle
-//   warps 4..7  epilogue: TMEM -> registers (lane quadrant = warp % 4), the
-//               epilogue math, bf16 tiles staged in shared memory, TMA stores
+//   warps 4..   epilogue (4 warps; 8 for the store-only epilogues, two per quadrant):
+//               TMEM -> registers (lane quadrant = warp % 4), the epilogue math,
+//               tiles staged in shared memory, TMA stores
 //
 // CG = 1: each CTA computes a 128 x 256 output tile with cta_group::1 MMAs.
 // CG = 2: a cluster of two CTAs computes a 256 x 256 tile with cta_group::2 MMAs.
@@ -39,7 +44,10 @@
 //                   prefetched left/gate: dleft = grad_h * silu(gate),
 //                   dgate = grad_h * left * silu'(gate), silu' = sigma + silu*(1 - sigma),
 //                   h = bf16(left * bf16(silu(gate))); stores grad_preact = [dleft|dgate]
-//                   and h.
+//                   and h, draining 16-column chunks.
+// With FP8 operands (OP_E4M3, the quantised GEMM epilogue of the lesson above, section
+// 26) the epilogue first multiplies the accumulator by the operands' scale product, and
+// the SwiGLU forward stores h quantised to E4M3, sat8(round(h / s_h)).
 // The SwiGLU forms follow the "SwiGLU MLP Drop-H technical report" (original math,
 // and the fused backward kernel's pseudo-code) and the fused dout-GEMM + SwiGLU
 // backward of the "SwiGLU MLP forward/backward optimization" note (section 4): the
