@@ -204,6 +204,17 @@ def peaks():
 
 # ----------------------------------------------------------------------------- our arm
 
+def block_memory_mib(M: int, D: int, H: int, Dout: int, bwd_workspace_bytes: int) -> dict:
+    """Device memory of one block beyond its inputs (x, W1, W2, dy), as the pages' memory
+    table counts it: after the forward the saved preact and the output y; at the
+    backward's peak also the backward workspace (h, grad_preact) and dx, dW1, dW2."""
+    mib = 2 ** 20
+    after_fwd = (M * 2 * H + M * Dout) * 2
+    peak = after_fwd + bwd_workspace_bytes + (M * D + 2 * H * D + Dout * H) * 2
+    return {"after_fwd": round(after_fwd / mib, 1), "bwd_peak": round(peak / mib, 1),
+            "pages_drop_h_b200": {"after_fwd": 686.1, "peak": 1905.1}}
+
+
 def graph_replay_timing(step, dev, K: int, step_flops: float):
     """The same step captured once into a CUDA graph and replayed K times: the launch
     gaps between the step's short kernels go away (the decode step is launch-bound)."""
@@ -464,6 +475,7 @@ def run_ours(args):
         "clocks": clk,
         "cublas_eager_comparison": eager,
         "cuda_graph": graph,
+        "memory_mib": block_memory_mib(M, D, H, Do, ws_b.numel()),
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
