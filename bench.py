@@ -204,6 +204,26 @@ def peaks():
 
 # ----------------------------------------------------------------------------- our arm
 
+def write_ceiling_gbs(nbytes: int, dev) -> float:
+    """HBM bandwidth of a write-only stream of `nbytes` (torch fill_ of a bf16 buffer),
+    best of 5 repetitions of 10 fills, CUDA events."""
+    import torch
+
+    t = torch.empty(max(1, nbytes // 2), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        t.fill_(1.0)
+    best = float("inf")
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            t.fill_(1.0)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        best = min(best, e0.elapsed_time(e1) / 10)
+    return t.numel() * 2 / (best * 1e-3) / 1e9
+
+
 def block_memory_mib(M: int, D: int, H: int, Dout: int, bwd_workspace_bytes: int) -> dict:
     """Device memory of one block beyond its inputs (x, W1, W2, dy), as the pages' memory
     table counts it: after the forward the saved preact and the output y; at the
@@ -379,6 +399,12 @@ def run_ours(args):
         roofline = {"kernel": dom, "bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                     "frac": round(dom_gbs / pk["hbm_gbs"], 3), "traffic": measured_traffic(dom, wl if not args.residual else "residual"),
                     "peak_source": f"{pk_src} hbm_gbs"}
+        if dom == "bwd_gemms":
+            # the weight gradients are almost all writes: their own ceiling is a write-only
+            # stream, measured here on the same part (torch fill_ of the same number of bytes)
+            wc = write_ceiling_gbs(kb[dom], dev)
+            roofline["write_only_ceiling_gbs"] = round(wc, 1)
+            roofline["frac_of_write_only_ceiling"] = round(dom_gbs / wc, 3)
     else:
         dom_achieved = kstats[dom]["tflops"]
         roofline = {"kernel": dom, "bound": "tensor", "achieved": dom_achieved,
