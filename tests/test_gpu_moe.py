@@ -209,3 +209,25 @@ def test_moe_random_layers(b, case):
             parity(dW2[e], dW2_ref[e], f"dW2[{e}]")
         else:
             assert dW1[e].abs().max().item() == 0 and dW2[e].abs().max().item() == 0
+
+
+def test_moe_many_calls_in_flight(b):
+    # 20 forward calls queued back to back (more than the 8 pinned table slots, each call
+    # copying two tables) on two streams, with different counts and inputs per call; every
+    # result must be the one its own call asked for
+    D, H, Dout = 64, 128, 64
+    calls = []
+    for i in range(20):
+        counts = [(7 * i + 3 * e) % 50 for e in range(3)]
+        x, W1, W2, _, _ = _experts(counts, D, H, Dout, seed=200 + i)
+        calls.append((counts, x, W1, W2))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for i, (counts, x, W1, W2) in enumerate(calls):
+        with torch.cuda.stream(streams[i % 2]):
+            outs.append(b.swiglu_moe_fwd(dev(x), dev(W1), dev(W2), counts))
+    torch.cuda.synchronize()
+    assert b.swiglu_mlp_device_status() == 0
+    for (counts, x, W1, W2), (_, y) in zip(calls, outs):
+        if sum(counts):
+            parity(y, oracle.moe_fwd(x, W1, W2, counts)[2], f"y (counts {counts})")
