@@ -552,3 +552,43 @@ def test_random_shapes_forward_backward(b, s):
     parity(dx, dx_ref, "dx")
     parity(dW1, dW1_ref, "dW1")
     parity(dW2, dW2_ref, "dW2")
+
+
+@pytest.mark.parametrize("path", ["few_tokens", "moe_table", "moe_table_fused_bwd", "fp8"])
+def test_bounded_wait_times_out_on_every_kernel_family(b, path):
+    # the producer-skip hook on the weight-streaming, problem-table and FP8 kernels: every
+    # consumer wait runs out, the launch ends with SWIGLU_ERR_TIMEOUT recorded, and the same
+    # call afterwards computes the right result on the same context
+    s = Shape(16 if path == "few_tokens" else 300, 128, 256, 128)
+    counts = [100, 0, 200]
+
+    def run():
+        if path == "few_tokens":
+            _, x, W1, W2, _ = workloads.make_block(s, seed=90)
+            return b.swiglu_mlp_fwd(dev(x), dev(W1), dev(W2))[1], oracle.fwd(x, W1, W2)[2]
+        if path.startswith("moe"):
+            g = torch.Generator().manual_seed(91)
+            x = torch.randn(300, 128, generator=g).to(torch.bfloat16)
+            W1 = (torch.randn(3, 512, 128, generator=g) / 12).to(torch.bfloat16)
+            W2 = (torch.randn(3, 128, 256, generator=g) / 16).to(torch.bfloat16)
+            if path == "moe_table":
+                return b.swiglu_moe_fwd(dev(x), dev(W1), dev(W2), counts)[1], oracle.moe_fwd(x, W1, W2, counts)[2]
+            dy = torch.randn(300, 128, generator=g).to(torch.bfloat16)
+            pre = torch.randn(300, 512, generator=g).to(torch.bfloat16)
+            dx = b.swiglu_moe_bwd(dev(x), dev(W1), dev(W2), dev(pre), dev(dy), counts)[0]
+            return dx, oracle.moe_bwd_full(x, W1, W2, pre, dy, counts)[3]
+        x8, W1_8, W2_8, sc = workloads.make_fp8_block(s, 92)
+        return b.swiglu_mlp_fwd_fp8(dev(x8), dev(W1_8), dev(W2_8), **sc)[2], oracle.fwd_fp8(x8, W1_8, W2_8, **sc)[3]
+
+    b.swiglu_mlp_set_wait_timeout_ns(50_000_000)
+    b.swiglu_mlp_set_debug_flags(1)
+    try:
+        run()
+        assert b.swiglu_mlp_device_status() == 6      # SWIGLU_ERR_TIMEOUT
+    finally:
+        b.swiglu_mlp_set_debug_flags(0)
+        b.swiglu_mlp_set_wait_timeout_ns(4_000_000_000)
+    assert b.swiglu_mlp_device_status() == 0
+    got, ref = run()
+    ok_status(b)
+    parity(got, ref, f"{path} after timeout")
