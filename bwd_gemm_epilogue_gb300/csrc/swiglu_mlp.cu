@@ -832,7 +832,7 @@ int swiglu_mlp_trace_end(void) {
     return n;
 }
 
-int swiglu_mlp_abi_version(void) { return 100; }
+int swiglu_mlp_abi_version(void) { return 200; }
 
 }  // extern "C"
 

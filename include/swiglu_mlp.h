@@ -265,7 +265,8 @@ typedef enum {
 void swiglu_mlp_trace_begin(void** events, int* kinds, int capacity);
 int swiglu_mlp_trace_end(void);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 200 = the block, its residual
+ * variant, the FP8 forward and (swiglu_moe.h) the MoE layer. */
 int swiglu_mlp_abi_version(void);
 
 #ifdef __cplusplus
