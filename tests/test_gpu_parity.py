@@ -592,3 +592,36 @@ def test_bounded_wait_times_out_on_every_kernel_family(b, path):
     got, ref = run()
     ok_status(b)
     parity(got, ref, f"{path} after timeout")
+
+
+def test_every_path_is_bit_reproducible(b):
+    # the same inputs twice give the same bits on every path: the tile kernels accumulate
+    # each output tile in one CTA (pair), the few-token kernels add their per-split planes
+    # in a fixed order, the MoE launches are tile-disjoint
+    def twice(fn):
+        a = fn()
+        c = fn()
+        ok_status(b)
+        for u, v in zip(a, c):
+            assert torch.equal(u, v)
+
+    for M in (16, 300):
+        s = Shape(M, 256, 512, 256)
+        _, x, W1, W2, dy = workloads.make_block(s, seed=95)
+        x, W1, W2, dy = dev(x), dev(W1), dev(W2), dev(dy)
+        pre = dev(workloads.make_preact(s, seed=95))
+        twice(lambda: b.swiglu_mlp_fwd(x, W1, W2))
+        twice(lambda: b.swiglu_mlp_bwd(x, W1, W2, pre, dy))
+        twice(lambda: b.swiglu_mlp_bwd(x, W1, W2, pre, dy, residual=True))
+        x8, W1_8, W2_8, sc = workloads.make_fp8_block(s, 96)
+        x8, W1_8, W2_8 = dev(x8), dev(W1_8), dev(W2_8)
+        twice(lambda: b.swiglu_mlp_fwd_fp8(x8, W1_8, W2_8, **sc))
+    counts = [40, 0, 90, 7]
+    g = torch.Generator().manual_seed(97)
+    x = dev(torch.randn(137, 128, generator=g).to(torch.bfloat16))
+    W1 = dev((torch.randn(4, 512, 128, generator=g) / 12).to(torch.bfloat16))
+    W2 = dev((torch.randn(4, 128, 256, generator=g) / 16).to(torch.bfloat16))
+    dy = dev(torch.randn(137, 128, generator=g).to(torch.bfloat16))
+    pre = dev(torch.randn(137, 512, generator=g).to(torch.bfloat16))
+    twice(lambda: b.swiglu_moe_fwd(x, W1, W2, counts))
+    twice(lambda: b.swiglu_moe_bwd(x, W1, W2, pre, dy, counts))
