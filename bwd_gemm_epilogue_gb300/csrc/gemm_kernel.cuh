@@ -135,8 +135,18 @@ static_assert(sizeof(ScheduledArgs) <= 32764, "kernel parameter block limit");
 //   SRC_TABLE   any number of problems (the experts of an MoE layer, each with its own
 //               row count) in a table in global memory, written by the host before the
 //               launch, with the host tile list beside it.  Cluster c runs the entries
-//               sched[sched_off[c] .. sched_off[c + 1]), each problem << 20 | tile.
-constexpr int SRC_SINGLE = 0, SRC_PARAMS = 1, SRC_TABLE = 2;
+//               sched[sched_off[c] .. sched_off[c + 1]), each problem << 20 | tile;
+//   SRC_TABLE_COMMON  a table whose problems all share k_blocks, a_mn and b_mn (the
+//               experts of one MoE GEMM): the producer takes those three from the
+//               parameter block.
+// The producer's mainloop issues one TMA copy per operand and k-block.  When its loop
+// count and operand layout come from fixed offsets of the parameter block, those
+// copies issue at about twice the rate measured when the same values come from a
+// run-time-selected problem (a table entry, shared memory or a parameter selected
+// by index): 15-17 % of a producer-bound GEMM.  So the list source gives the producer
+// one copy of its tile body per problem index, and uniform tables say so.
+constexpr int SRC_SINGLE = 0, SRC_PARAMS = 1, SRC_TABLE = 2, SRC_TABLE_COMMON = 3;
+__host__ __device__ constexpr bool is_table(int src) { return src >= SRC_TABLE; }
 constexpr int TABLE_TILE_BITS = 20;
 struct alignas(128) TableEntry {
     CUtensorMap a, b, o0;
@@ -154,6 +164,7 @@ struct TableArgs {
     unsigned long long timeout_ns;
     int* err;
     int debug_flags;
+    int common_k_blocks, common_a_mn, common_b_mn;   // SRC_TABLE_COMMON: shared by every problem
 };
 
 template <int EPI, int CG>
@@ -281,7 +292,7 @@ __device__ __forceinline__ int tiles_end(const Args& a, int c) {
 // statements clobber memory, and parameter or table fields would be reloaded.
 template <int SRC, class Args>
 __device__ __forceinline__ Problem problem_at(const Args& a, int it, int& pi, int& lt) {
-    if constexpr (SRC == SRC_TABLE) {
+    if constexpr (is_table(SRC)) {
         const int v = __ldg(a.sched + it);
         pi = v >> TABLE_TILE_BITS;
         lt = v & ((1 << TABLE_TILE_BITS) - 1);
@@ -302,7 +313,7 @@ __device__ __forceinline__ Problem problem_at(const Args& a, int it, int& pi, in
 enum MapId { MAP_A, MAP_B, MAP_O0, MAP_O1, MAP_I0 };
 template <int SRC, int WHICH, class Args>
 __device__ __forceinline__ const CUtensorMap* map_of(const Args& a, int pi) {
-    if constexpr (SRC == SRC_TABLE) {
+    if constexpr (is_table(SRC)) {
         const TableEntry* e = a.table + pi;
         if constexpr (WHICH == MAP_A) return &e->a;
         else if constexpr (WHICH == MAP_B) return &e->b;
@@ -402,7 +413,7 @@ __device__ __forceinline__ uint32_t stage_offset(int r, int c) {
 
 template <int EPI, int CG, int SCHED>
 using ArgsOf = typename std::conditional<
-    SCHED == SRC_TABLE, TableArgs,
+    is_table(SCHED), TableArgs,
     typename std::conditional<SCHED == SRC_PARAMS, ScheduledArgs, KernelArgs>::type>::type;
 
 template <int EPI, int CG, int SCHED, int OP = OP_BF16>
@@ -456,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
-        if constexpr (SCHED != SRC_TABLE) {
+        if constexpr (!is_table(SCHED)) {
 #pragma unroll
             for (int q = 0; q < MAX_PROBLEMS; ++q) {
                 if (q < args.num_problems) {
@@ -501,15 +512,17 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 const Problem pr = problem_at<SCHED>(args, it, pi, lt);
                 const CUtensorMap* mA = map_of<SCHED, MAP_A>(args, pi);
                 const CUtensorMap* mB = map_of<SCHED, MAP_B>(args, pi);
-                if (SCHED == SRC_TABLE && pi != seen_pi) {
+                if (is_table(SCHED) && pi != seen_pi) {
                     ptx::tmap_acquire(mA);
                     ptx::tmap_acquire(mB);
                     seen_pi = pi;
                 }
-                const int k_blocks = pr.k_blocks;
-                const bool a_mn = pr.a_mn != 0, b_mn = pr.b_mn != 0;
+                // One tile's k-blocks.  Called with parameter-block fields wherever the
+                // source allows it (see SRC_TABLE_COMMON).
+                auto tile = [&](const Problem& p, int k_blocks, bool a_mn, bool b_mn, const CUtensorMap* ma,
+                                const CUtensorMap* mb) {
                 int tm, tn;
-                tile_coords(pr, lt, tm, tn);
+                tile_coords(p, lt, tm, tn);
                 const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
@@ -529,31 +542,45 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         else ptx::tma_load_2d(dst, m, fb, c0, c1);
                     };
                     if (a_mn) {
-                        load2(sA, mA, m0, k0);
-                        load2(sA + 8192, mA, m0 + 64, k0);
+                        load2(sA, ma, m0, k0);
+                        load2(sA + 8192, ma, m0 + 64, k0);
                     } else {
-                        load2(sA, mA, k0, m0);
+                        load2(sA, ma, k0, m0);
                     }
                     if (EPI == EPI_SWIGLU_FWD) {
                         // W1 as (k, j, half): CG == 1 loads both slabs, CG == 2 the slab of its rank
                         const int j0 = tn * (BN / 2);
                         if (CG == 2) {
-                            ptx::tma_load_3d_pair(sB, mB, fb, k0, j0, (int)rank);
+                            ptx::tma_load_3d_pair(sB, mb, fb, k0, j0, (int)rank);
                         } else {
-                            ptx::tma_load_3d(sB, mB, fb, k0, j0, 0);
-                            ptx::tma_load_3d(sB + C::B_BYTES / 2, mB, fb, k0, j0, 1);
+                            ptx::tma_load_3d(sB, mb, fb, k0, j0, 0);
+                            ptx::tma_load_3d(sB + C::B_BYTES / 2, mb, fb, k0, j0, 1);
                         }
                     } else if (b_mn) {
                         const int n0 = tn * BN + C::B_ROWS * (int)rank;
 #pragma unroll
-                        for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mB, n0 + 64 * i, k0);
+                        for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mb, n0 + 64 * i, k0);
                     } else {
-                        load2(sB, mB, k0, tn * BN + C::B_ROWS * (int)rank);
+                        load2(sB, mb, k0, tn * BN + C::B_ROWS * (int)rank);
                     }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                }
+                };
+                if constexpr (SCHED == SRC_PARAMS) {
+                    // one copy per problem index: that problem's fields at fixed offsets
+                    auto fixed = [&](const Problem& p, const CUtensorMap* ma, const CUtensorMap* mb) {
+                        tile(p, p.k_blocks, p.a_mn != 0, p.b_mn != 0, ma, mb);
+                    };
+                    if (pi == 0) fixed(args.prob[0], &args.a[0], &args.b[0]);
+                    else if (pi == 1) fixed(args.prob[1], &args.a[1], &args.b[1]);
+                    else fixed(args.prob[2], &args.a[2], &args.b[2]);
+                } else if constexpr (SCHED == SRC_TABLE_COMMON) {
+                    tile(pr, args.common_k_blocks, args.common_a_mn != 0, args.common_b_mn != 0, mA, mB);
+                } else {
+                    tile(pr, pr.k_blocks, pr.a_mn != 0, pr.b_mn != 0, mA, mB);
                 }
             }
             if (!ok) {
@@ -651,7 +678,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 const Problem pr0 = problem_at<SCHED>(args, it, pi, lt);
                 tile_coords(pr0, lt, tm, tn);
                 const CUtensorMap* mI = map_of<SCHED, MAP_I0>(args, pi);
-                if (SCHED == SRC_TABLE && pi != seen_pi) {
+                if (is_table(SCHED) && pi != seen_pi) {
                     ptx::tmap_acquire(mI);
                     seen_pi = pi;
                 }
@@ -693,7 +720,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 const Problem pr = problem_at<SCHED>(args, it, pi, lt);
                 if (!pr.res) continue;
                 const CUtensorMap* mI = map_of<SCHED, MAP_I0>(args, pi);
-                if (SCHED == SRC_TABLE && pi != seen_pi) {
+                if (is_table(SCHED) && pi != seen_pi) {
                     ptx::tmap_acquire(mI);
                     seen_pi = pi;
                 }
@@ -743,7 +770,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             const int n_limit = pr.N;
             const CUtensorMap* mO0 = map_of<SCHED, MAP_O0>(args, pi);
             const CUtensorMap* mO1 = map_of<SCHED, MAP_O1>(args, pi);
-            if (SCHED == SRC_TABLE && pi != seen_pi && lane == 0) {
+            if (is_table(SCHED) && pi != seen_pi && lane == 0) {
                 ptx::tmap_acquire(mO0);
                 if (!C::STORE_ONLY) ptx::tmap_acquire(mO1);
             }

@@ -289,7 +289,7 @@ swiglu_status launch_grid(DeviceState* st, int kind, const ArgsOf<EPI, CG, SCHED
 // fields, the host schedule and the grid.
 template <int EPI, int CG, int SCHED, int OP = OP_BF16>
 swiglu_status launch(DeviceState* st, int kind, ArgsOf<EPI, CG, SCHED>& args, cudaStream_t stream) {
-    static_assert(SCHED != SRC_TABLE, "table launches go through launch_table");
+    static_assert(!is_table(SCHED), "table launches go through launch_table");
     int tiles = 0;
     for (int q = 0; q < args.num_problems; ++q) {
         args.prob[q].tile_begin = tiles;
@@ -989,7 +989,13 @@ swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& e
     if (table_bytes((size_t)n, (size_t)tiles) > dev_bytes) return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "problem table");
     const uintptr_t raw = reinterpret_cast<uintptr_t>(dev_table);
     dev_table = reinterpret_cast<void*>((raw + 255) & ~uintptr_t(255));
-    const int slots = cluster_slots<EPI, CG, SRC_TABLE>(st);
+    // experts of one GEMM share k-blocks and operand layout: the kernel then takes them
+    // from its parameters (a faster producer mainloop)
+    bool common = true;
+    for (const TableEntry& e : ents)
+        common = common && e.prob.k_blocks == ents[0].prob.k_blocks && e.prob.a_mn == ents[0].prob.a_mn &&
+                 e.prob.b_mn == ents[0].prob.b_mn;
+    const int slots = common ? cluster_slots<EPI, CG, SRC_TABLE_COMMON>(st) : cluster_slots<EPI, CG, SRC_TABLE>(st);
     if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
     const int units = (int)std::min<long long>(tiles, std::min(slots, kMaxUnits));
 
@@ -1039,6 +1045,10 @@ swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& e
     a.timeout_ns = g_timeout_ns.load();
     a.err = st->err_word;
     a.debug_flags = g_debug_flags.load();
+    a.common_k_blocks = ents[0].prob.k_blocks;
+    a.common_a_mn = ents[0].prob.a_mn;
+    a.common_b_mn = ents[0].prob.b_mn;
+    if (common) return launch_grid<EPI, CG, SRC_TABLE_COMMON>(st, kind, a, units, s);
     return launch_grid<EPI, CG, SRC_TABLE>(st, kind, a, units, s);
 }
 
