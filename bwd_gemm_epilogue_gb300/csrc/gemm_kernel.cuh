@@ -139,12 +139,13 @@ static_assert(sizeof(ScheduledArgs) <= 32764, "kernel parameter block limit");
 //   SRC_TABLE_COMMON  a table whose problems all share k_blocks, a_mn and b_mn (the
 //               experts of one MoE GEMM): the producer takes those three from the
 //               parameter block.
-// The producer's mainloop issues one TMA copy per operand and k-block.  When its loop
-// count and operand layout come from fixed offsets of the parameter block, those
-// copies issue at about twice the rate measured when the same values come from a
-// run-time-selected problem (a table entry, shared memory or a parameter selected
-// by index): 15-17 % of a producer-bound GEMM.  So the list source gives the producer
-// one copy of its tile body per problem index, and uniform tables say so.
+// The producer's mainloop issues one TMA copy per operand and k-block.  When its
+// operand layout (a_mn, b_mn) comes from fixed offsets of the parameter block or is a
+// compile-time constant, those copies issue at about twice the rate measured when it
+// comes from a run-time-selected problem (a table entry, shared memory or a parameter
+// selected by index): 15-17 % of a producer-bound GEMM.  So the list source gives the
+// producer one copy of its tile body per problem index, uniform tables carry the
+// layout in the parameters, and other tables get one copy per operand layout.
 constexpr int SRC_SINGLE = 0, SRC_PARAMS = 1, SRC_TABLE = 2, SRC_TABLE_COMMON = 3;
 __host__ __device__ constexpr bool is_table(int src) { return src >= SRC_TABLE; }
 constexpr int TABLE_TILE_BITS = 20;
@@ -579,6 +580,13 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     else fixed(args.prob[2], &args.a[2], &args.b[2]);
                 } else if constexpr (SCHED == SRC_TABLE_COMMON) {
                     tile(pr, args.common_k_blocks, args.common_a_mn != 0, args.common_b_mn != 0, mA, mB);
+                } else if constexpr (SCHED == SRC_TABLE) {
+                    // one copy per operand layout: the layout as a compile-time constant
+                    const bool am = pr.a_mn != 0, bm = pr.b_mn != 0;
+                    if (am && bm) tile(pr, pr.k_blocks, true, true, mA, mB);
+                    else if (am) tile(pr, pr.k_blocks, true, false, mA, mB);
+                    else if (bm) tile(pr, pr.k_blocks, false, true, mA, mB);
+                    else tile(pr, pr.k_blocks, false, false, mA, mB);
                 } else {
                     tile(pr, pr.k_blocks, pr.a_mn != 0, pr.b_mn != 0, mA, mB);
                 }
