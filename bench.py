@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -171,11 +172,14 @@ def cpu_baseline(s, x, W1, W2, dy, preact, seconds: float):
 # ----------------------------------------------------------------------------- profile summary
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources with runs of white space collapsed: a change of
+    formatting keeps the counters taken before it, any other edit voids them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bwd_gemm_epilogue_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+            text = open(os.path.join(csrc, name), "rb").read()
+            h.update(name.encode() + b"\0" + re.sub(rb"\s+", b" ", text).strip() + b"\0")
     return h.hexdigest()[:16]
 
 

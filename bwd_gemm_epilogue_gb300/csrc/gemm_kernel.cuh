@@ -522,53 +522,53 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 // source allows it (see SRC_TABLE_COMMON).
                 auto tile = [&](const Problem& p, int k_blocks, bool a_mn, bool b_mn, const CUtensorMap* ma,
                                 const CUtensorMap* mb) {
-                int tm, tn;
-                tile_coords(p, lt, tm, tn);
-                const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
-                for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb_local = full_bar(stage);
-                    // CG == 2: both CTAs' copies complete on the leader's stage barrier.
-                    const uint32_t fb = CG == 2 ? full_bar_leader + 8u * stage : fb_local;
-                    if (leader) ptx::mbar_arrive_expect_tx(fb_local, C::TX_BYTES);
-                    last_parity[stage] = (int)phase;
-                    const int k0 = kb * BKE;
-                    const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
-                    const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
-                    auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
-                        if (CG == 2) ptx::tma_load_2d_pair(dst, m, fb, c0, c1);
-                        else ptx::tma_load_2d(dst, m, fb, c0, c1);
-                    };
-                    if (a_mn) {
-                        load2(sA, ma, m0, k0);
-                        load2(sA + 8192, ma, m0 + 64, k0);
-                    } else {
-                        load2(sA, ma, k0, m0);
-                    }
-                    if (EPI == EPI_SWIGLU_FWD) {
-                        // W1 as (k, j, half): CG == 1 loads both slabs, CG == 2 the slab of its rank
-                        const int j0 = tn * (BN / 2);
-                        if (CG == 2) {
-                            ptx::tma_load_3d_pair(sB, mb, fb, k0, j0, (int)rank);
-                        } else {
-                            ptx::tma_load_3d(sB, mb, fb, k0, j0, 0);
-                            ptx::tma_load_3d(sB + C::B_BYTES / 2, mb, fb, k0, j0, 1);
+                    int tm, tn;
+                    tile_coords(p, lt, tm, tn);
+                    const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
+                    for (int kb = 0; kb < k_blocks; ++kb) {
+                        if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
+                            ok = false;
+                            break;
                         }
-                    } else if (b_mn) {
-                        const int n0 = tn * BN + C::B_ROWS * (int)rank;
+                        const uint32_t fb_local = full_bar(stage);
+                        // CG == 2: both CTAs' copies complete on the leader's stage barrier.
+                        const uint32_t fb = CG == 2 ? full_bar_leader + 8u * stage : fb_local;
+                        if (leader) ptx::mbar_arrive_expect_tx(fb_local, C::TX_BYTES);
+                        last_parity[stage] = (int)phase;
+                        const int k0 = kb * BKE;
+                        const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
+                        const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
+                        auto load2 = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+                            if (CG == 2) ptx::tma_load_2d_pair(dst, m, fb, c0, c1);
+                            else ptx::tma_load_2d(dst, m, fb, c0, c1);
+                        };
+                        if (a_mn) {
+                            load2(sA, ma, m0, k0);
+                            load2(sA + 8192, ma, m0 + 64, k0);
+                        } else {
+                            load2(sA, ma, k0, m0);
+                        }
+                        if (EPI == EPI_SWIGLU_FWD) {
+                            // W1 as (k, j, half): CG == 1 loads both slabs, CG == 2 the slab of its rank
+                            const int j0 = tn * (BN / 2);
+                            if (CG == 2) {
+                                ptx::tma_load_3d_pair(sB, mb, fb, k0, j0, (int)rank);
+                            } else {
+                                ptx::tma_load_3d(sB, mb, fb, k0, j0, 0);
+                                ptx::tma_load_3d(sB + C::B_BYTES / 2, mb, fb, k0, j0, 1);
+                            }
+                        } else if (b_mn) {
+                            const int n0 = tn * BN + C::B_ROWS * (int)rank;
 #pragma unroll
-                        for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mb, n0 + 64 * i, k0);
-                    } else {
-                        load2(sB, mb, k0, tn * BN + C::B_ROWS * (int)rank);
+                            for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mb, n0 + 64 * i, k0);
+                        } else {
+                            load2(sB, mb, k0, tn * BN + C::B_ROWS * (int)rank);
+                        }
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
                 };
                 if constexpr (SCHED == SRC_PARAMS) {
                     // one copy per problem index: that problem's fields at fixed offsets
