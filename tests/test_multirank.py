@@ -2,7 +2,9 @@
 
 Each rank runs an independent replica of the block; ranks meet only to agree on
 the slowest rank's time, and only rank 0 prints.  These tests exercise that
-logic with two gloo processes on 127.0.0.1 -- no GPU, no NCCL.
+logic with two gloo processes on 127.0.0.1 -- no GPU, no NCCL.  One more checks,
+with the oracle, the data-parallel reading of the block: token rows split across
+ranks need one exchange, the sum of the weight gradients.
 """
 import os
 import socket
@@ -70,3 +72,65 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
         steps, warmup = 3, 1
     bench.run_reference(Args())        # rank 1: returns at once, prints nothing
     assert capsys.readouterr().out == ""
+
+
+def _dp_worker(rank, world, port, out):
+    """Rank `rank` takes its share of the token rows through the oracle's block."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch
+    import oracle
+    from bwd_gemm_epilogue_gb300 import workloads
+    from bwd_gemm_epilogue_gb300.workloads import Shape
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        s, x, W1, W2, dy = workloads.make_block(Shape(96, 64, 80, 48), seed=7)
+        rows = slice(rank * s.M // world, (rank + 1) * s.M // world)
+        xs, dys = x[rows].contiguous(), dy[rows].contiguous()
+        preact, _, y = oracle.fwd(xs, W1, W2)
+        # the saved preact is bf16-rounded: back to bf16 exactly, like the other inputs
+        _, _, _, dx, dW1, dW2 = oracle.bwd_full(xs, W1, W2, torch.from_numpy(preact).to(torch.bfloat16), dys)
+        dW1, dW2 = torch.from_numpy(dW1), torch.from_numpy(dW2)
+        dist.all_reduce(dW1)                     # the one exchange the row split needs
+        dist.all_reduce(dW2)
+        ys = [torch.empty_like(torch.from_numpy(y)) for _ in range(world)]
+        dxs = [torch.empty_like(torch.from_numpy(dx)) for _ in range(world)]
+        dist.all_gather(ys, torch.from_numpy(y))
+        dist.all_gather(dxs, torch.from_numpy(dx))
+        out[rank] = (torch.cat(ys).numpy(), torch.cat(dxs).numpy(), dW1.numpy(), dW2.numpy())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_row_shards_with_summed_weight_gradients_give_the_full_batch():
+    # Data parallelism over token rows: y and dx are row-wise, so each rank's rows are
+    # final; dW1 and dW2 are sums over rows, so the ranks' partial sums add up to the
+    # full batch's (up to the fp64 order of the additions).
+    import sys
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+    import oracle
+    from bwd_gemm_epilogue_gb300 import workloads
+    from bwd_gemm_epilogue_gb300.workloads import Shape
+    oracle.build()                               # once, before the ranks load it
+    world = 2
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_dp_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+        res = dict(out)
+    _, x, W1, W2, dy = workloads.make_block(Shape(96, 64, 80, 48), seed=7)
+    preact, _, y = oracle.fwd(x, W1, W2)
+    preact = torch.from_numpy(preact).to(torch.bfloat16)
+    _, _, _, dx, dW1, dW2 = oracle.bwd_full(x, W1, W2, preact, dy)
+    for rank in range(world):
+        ys, dxs, dW1s, dW2s = res[rank]
+        np.testing.assert_array_equal(ys, y)
+        np.testing.assert_array_equal(dxs, dx)
+        np.testing.assert_allclose(dW1s, dW1, rtol=1e-12, atol=1e-12 * np.abs(dW1).max())
+        np.testing.assert_allclose(dW2s, dW2, rtol=1e-12, atol=1e-12 * np.abs(dW2).max())
+    # a rank that skipped the exchange would hold only its own rows' share
+    _, _, _, _, dW1_half, _ = oracle.bwd_full(x[:48].contiguous(), W1, W2, preact[:48].contiguous(),
+                                               dy[:48].contiguous())
+    assert np.abs(dW1_half - dW1).max() > 1e-3 * np.abs(dW1).max()
