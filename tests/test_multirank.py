@@ -3,8 +3,11 @@
 Each rank runs an independent replica of the block; ranks meet only to agree on
 the slowest rank's time, and only rank 0 prints.  These tests exercise that
 logic with two gloo processes on 127.0.0.1 -- no GPU, no NCCL.  One more checks,
-with the oracle, the data-parallel reading of the block: token rows split across
-ranks need one exchange, the sum of the weight gradients.
+with the oracle, the data-parallel reading of the block (token rows split across
+ranks need one exchange, the sum of the weight gradients), and one the
+tensor-parallel reading (hidden columns split across ranks: y and dx are sums of
+partial products).  The managers are started with spawn: the oracle's OpenMP
+threads make a later fork unsafe.
 """
 import os
 import socket
@@ -41,7 +44,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_agree_on_the_slowest_time():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
@@ -116,7 +119,7 @@ def test_row_shards_with_summed_weight_gradients_give_the_full_batch():
     from bwd_gemm_epilogue_gb300.workloads import Shape
     oracle.build()                               # once, before the ranks load it
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_dp_worker, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
@@ -134,3 +137,64 @@ def test_row_shards_with_summed_weight_gradients_give_the_full_batch():
     _, _, _, _, dW1_half, _ = oracle.bwd_full(x[:48].contiguous(), W1, W2, preact[:48].contiguous(),
                                                dy[:48].contiguous())
     assert np.abs(dW1_half - dW1).max() > 1e-3 * np.abs(dW1).max()
+
+
+def _tp_worker(rank, world, port, out):
+    """Rank `rank` holds hidden columns J_r: W1 rows J_r (left) and H + J_r (gate), W2 columns J_r."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch
+    import oracle
+    from bwd_gemm_epilogue_gb300 import workloads
+    from bwd_gemm_epilogue_gb300.workloads import Shape
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        s, x, W1, W2, dy = workloads.make_block(Shape(64, 48, 96, 40), seed=11)
+        J = slice(rank * s.H // world, (rank + 1) * s.H // world)
+        W1r = torch.cat([W1[J], W1[s.H:][J]]).contiguous()
+        W2r = W2[:, J].contiguous()
+        preact, _, y = oracle.fwd(x, W1r, W2r)
+        _, _, _, dx, dW1r, dW2r = oracle.bwd_full(x, W1r, W2r, torch.from_numpy(preact).to(torch.bfloat16), dy)
+        y, dx = torch.from_numpy(y), torch.from_numpy(dx)
+        dist.all_reduce(y)                       # after the down projection
+        dist.all_reduce(dx)                      # after dx = grad_preact @ W1
+        out[rank] = (y.numpy(), dx.numpy(), dW1r, dW2r)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_hidden_column_shards_with_summed_outputs_give_the_full_block():
+    # Tensor parallelism over the hidden dimension: each rank's left/gate columns are a
+    # complete SwiGLU of their own, so y and dx are sums of per-rank partial products and
+    # each rank's weight gradients are its slices of the full ones.
+    import sys
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+    import oracle
+    from bwd_gemm_epilogue_gb300 import workloads
+    from bwd_gemm_epilogue_gb300.workloads import Shape
+    oracle.build()
+    world = 2
+    with mp.get_context("spawn").Manager() as m:
+        out = m.dict()
+        mp.spawn(_tp_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+        res = dict(out)
+    s, x, W1, W2, dy = workloads.make_block(Shape(64, 48, 96, 40), seed=11)
+    preact, _, y = oracle.fwd(x, W1, W2)
+    _, _, _, dx, dW1, dW2 = oracle.bwd_full(x, W1, W2, torch.from_numpy(preact).to(torch.bfloat16), dy)
+    half = s.H // world
+    for rank in range(world):
+        ys, dxs, dW1r, dW2r = res[rank]
+        np.testing.assert_allclose(ys, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+        np.testing.assert_allclose(dxs, dx, rtol=1e-12, atol=1e-12 * np.abs(dx).max())
+        J = slice(rank * half, (rank + 1) * half)
+        np.testing.assert_allclose(dW1r[:half], dW1[J], rtol=1e-12, atol=1e-12 * np.abs(dW1).max())
+        np.testing.assert_allclose(dW1r[half:], dW1[s.H:][J], rtol=1e-12, atol=1e-12 * np.abs(dW1).max())
+        np.testing.assert_allclose(dW2r, dW2[:, J], rtol=1e-12, atol=1e-12 * np.abs(dW2).max())
+    # pairing a rank's left columns with another rank's gate columns is not the block
+    W1_wrong = torch.cat([W1[:half], W1[s.H + half:]]).contiguous()
+    _, _, y_wrong = oracle.fwd(x, W1_wrong, W2[:, :half].contiguous())
+    _, _, y_right = oracle.fwd(x, torch.cat([W1[:half], W1[s.H:s.H + half]]).contiguous(), W2[:, :half].contiguous())
+    assert np.abs(y_wrong - y_right).max() > 1e-2 * np.abs(y_right).max()
