@@ -120,6 +120,37 @@ def _empty(shape, like: torch.Tensor) -> torch.Tensor:
     return torch.empty(shape, dtype=torch.bfloat16, device=like.device)
 
 
+# The kernels' tensor maps are built from the sizes, not from the tensors: a buffer of the
+# wrong shape would be read or written past its end.  So every tensor a call receives is
+# checked against the shape, dtype and device the sizes imply, before anything is launched.
+
+def _expect(t: torch.Tensor, name: str, shape, dtype, device) -> torch.Tensor:
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the call's other tensors are on {device}")
+    return t
+
+
+def _out(t, name: str, shape, like: torch.Tensor, dtype=torch.bfloat16) -> torch.Tensor:
+    """A caller's output buffer, checked, or a new one."""
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return _expect(t, name, shape, dtype, like.device)
+
+
+def _same_device(like: torch.Tensor, **tensors) -> None:
+    for name, t in tensors.items():
+        if t is not None and t.device != like.device:
+            raise ValueError(f"{name}: on {t.device}, the call's other tensors are on {like.device}")
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
 # ---------------------------------------------------------------------------- sizes / status
 
 def swiglu_mlp_fwd_workspace_size(M: int, D: int, H: int, Dout: int) -> int:
@@ -192,12 +223,14 @@ class LaunchTrace:
 
 # ---------------------------------------------------------------------------- compute
 
-def _dims(x, W1, W2):
+def _dims(x, W1, W2, dtype=torch.bfloat16):
     M, D = x.shape
     H2, D1 = W1.shape
     Dout, H = W2.shape
     if D1 != D or H2 != 2 * H:
         raise ValueError(f"shape mismatch: x {tuple(x.shape)}, W1 {tuple(W1.shape)}, W2 {tuple(W2.shape)}")
+    for name, t in (("x", x), ("W1", W1), ("W2", W2)):
+        _expect(t, name, t.shape, dtype, x.device)
     return M, D, H, Dout
 
 
@@ -205,14 +238,15 @@ def swiglu_mlp_fwd(x, W1, W2, preact=None, y=None, workspace=None, residual: boo
     """Forward; returns (preact [M,2H], y [M,Dout]).  residual: y = x + MLP(x)
     (swiglu_mlp_fwd_residual; D == Dout)."""
     M, D, H, Dout = _dims(x, W1, W2)
-    preact = _empty((M, 2 * H), x) if preact is None else preact
-    y = _empty((M, Dout), x) if y is None else y
+    preact = _out(preact, "preact", (M, 2 * H), x)
+    y = _out(y, "y", (M, Dout), x)
+    _same_device(x, workspace=workspace)
     need = swiglu_mlp_fwd_workspace_size(M, D, H, Dout)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     fn = lib().swiglu_mlp_fwd_residual if residual else lib().swiglu_mlp_fwd
     st = fn(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), M, D, H, Dout,
-            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(x.device))
+            _ptr(workspace), _nbytes(workspace), _stream(x.device))
     _check(st, "swiglu_mlp_fwd_residual" if residual else "swiglu_mlp_fwd")
     return preact, y
 
@@ -225,8 +259,8 @@ def swiglu_mlp_fwd_noalloc(x, W1, W2, preact=None, y=None):
     instead of a caller workspace (for callers that cannot allocate; M*H <= 2^25).
     Calls share that array: calls that overlap on the GPU race.  Returns (preact, y)."""
     M, D, H, Dout = _dims(x, W1, W2)
-    preact = _empty((M, 2 * H), x) if preact is None else preact
-    y = _empty((M, Dout), x) if y is None else y
+    preact = _out(preact, "preact", (M, 2 * H), x)
+    y = _out(y, "y", (M, Dout), x)
     st = lib().swiglu_mlp_fwd_noalloc(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), M, D, H, Dout,
                                       _stream(x.device))
     _check(st, "swiglu_mlp_fwd_noalloc")
@@ -237,17 +271,18 @@ def swiglu_mlp_bwd(x, W1, W2, preact, dy, dx=None, dW1=None, dW2=None, workspace
     """Backward; returns (dx [M,D], dW1 [2H,D], dW2 [Dout,H]).  residual: dx += dy
     (swiglu_mlp_bwd_residual; D == Dout)."""
     M, D, H, Dout = _dims(x, W1, W2)
-    if tuple(preact.shape) != (M, 2 * H) or tuple(dy.shape) != (M, Dout):
-        raise ValueError("preact / dy shape mismatch")
-    dx = _empty((M, D), x) if dx is None else dx
-    dW1 = _empty((2 * H, D), x) if dW1 is None else dW1
-    dW2 = _empty((Dout, H), x) if dW2 is None else dW2
+    _expect(preact, "preact", (M, 2 * H), torch.bfloat16, x.device)
+    _expect(dy, "dy", (M, Dout), torch.bfloat16, x.device)
+    dx = _out(dx, "dx", (M, D), x)
+    dW1 = _out(dW1, "dW1", (2 * H, D), x)
+    dW2 = _out(dW2, "dW2", (Dout, H), x)
+    _same_device(x, workspace=workspace)
     need = swiglu_mlp_bwd_workspace_size(M, D, H, Dout)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     fn = lib().swiglu_mlp_bwd_residual if residual else lib().swiglu_mlp_bwd
     st = fn(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dW1), _ptr(dW2),
-            M, D, H, Dout, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(x.device))
+            M, D, H, Dout, _ptr(workspace), _nbytes(workspace), _stream(x.device))
     _check(st, "swiglu_mlp_bwd_residual" if residual else "swiglu_mlp_bwd")
     return dx, dW1, dW2
 
@@ -268,22 +303,18 @@ def swiglu_mlp_fwd_fp8(x8, W1_8, W2_8, s_x: float, s_w1: float, s_w2: float, s_h
                        preact=None, h8=None, y=None, store_preact: bool = True, workspace=None):
     """FP8 forward (E4M3 operands, per-tensor scales); returns (preact [M,2H] bf16 or
     None, h8 [M,H] E4M3, y [M,Dout] bf16)."""
-    M, D = x8.shape
-    H2, D1 = W1_8.shape
-    Dout, H = W2_8.shape
-    if D1 != D or H2 != 2 * H:
-        raise ValueError("shape mismatch")
-    if store_preact and preact is None:
-        preact = _empty((M, 2 * H), x8)
-    h8 = torch.empty(M, H, dtype=torch.float8_e4m3fn, device=x8.device) if h8 is None else h8
-    y = _empty((M, Dout), x8) if y is None else y
+    M, D, H, Dout = _dims(x8, W1_8, W2_8, dtype=torch.float8_e4m3fn)
+    if store_preact:
+        preact = _out(preact, "preact", (M, 2 * H), x8)
+    h8 = _out(h8, "h8", (M, H), x8, dtype=torch.float8_e4m3fn)
+    y = _out(y, "y", (M, Dout), x8)
+    _same_device(x8, workspace=workspace)
     if workspace is None:
         n = swiglu_mlp_fwd_fp8_workspace_size(M, D, H, Dout)
         workspace = torch.empty(n, dtype=torch.uint8, device=x8.device) if n else None
     st = lib().swiglu_mlp_fwd_fp8(_ptr(x8), _ptr(W1_8), _ptr(W2_8), s_x, s_w1, s_w2, s_h,
                                   _ptr(preact) if store_preact else None, _ptr(h8), _ptr(y), M, D, H, Dout,
-                                  _ptr(workspace), 0 if workspace is None else workspace.numel(),
-                                  _stream(x8.device))
+                                  _ptr(workspace), _nbytes(workspace), _stream(x8.device))
     _check(st, "swiglu_mlp_fwd_fp8")
     return (preact if store_preact else None), h8, y
 
@@ -294,8 +325,10 @@ def swiglu_mlp_fused_grad_preact(dy, W2, preact, grad_preact=None, h=None):
     Dout2, H = W2.shape
     if Dout2 != Dout or tuple(preact.shape) != (M, 2 * H):
         raise ValueError("shape mismatch")
-    grad_preact = _empty((M, 2 * H), dy) if grad_preact is None else grad_preact
-    h = _empty((M, H), dy) if h is None else h
+    for name, t in (("dy", dy), ("W2", W2), ("preact", preact)):
+        _expect(t, name, t.shape, torch.bfloat16, dy.device)
+    grad_preact = _out(grad_preact, "grad_preact", (M, 2 * H), dy)
+    h = _out(h, "h", (M, H), dy)
     st = lib().swiglu_mlp_fused_grad_preact(_ptr(dy), _ptr(W2), _ptr(preact), _ptr(grad_preact), _ptr(h),
                                             M, H, Dout, _stream(dy.device))
     _check(st, "swiglu_mlp_fused_grad_preact")
@@ -304,7 +337,9 @@ def swiglu_mlp_fused_grad_preact(dy, W2, preact, grad_preact=None, h=None):
 
 def swiglu_mlp_gemm_bf16(A, B, M: int, N: int, K: int, a_mn_major: bool, b_mn_major: bool, C=None):
     """C [M,N] = A * B^T; A is [M,K] (or [K,M] if a_mn_major), B is [N,K] (or [K,N] if b_mn_major)."""
-    C = _empty((M, N), A) if C is None else C
+    _expect(A, "A", (K, M) if a_mn_major else (M, K), torch.bfloat16, A.device)
+    _expect(B, "B", (K, N) if b_mn_major else (N, K), torch.bfloat16, A.device)
+    C = _out(C, "C", (M, N), A)
     st = lib().swiglu_mlp_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(a_mn_major), int(b_mn_major),
                                     _stream(A.device))
     _check(st, "swiglu_mlp_gemm_bf16")
@@ -350,6 +385,8 @@ def _moe_dims(x, W1, W2):
     E2, Dout, H = W2.shape
     if D1 != D or H2 != 2 * H or E2 != E:
         raise ValueError(f"shape mismatch: x {tuple(x.shape)}, W1 {tuple(W1.shape)}, W2 {tuple(W2.shape)}")
+    for name, t in (("x", x), ("W1", W1), ("W2", W2)):
+        _expect(t, name, t.shape, torch.bfloat16, x.device)
     return T, E, D, H, Dout
 
 
@@ -370,13 +407,14 @@ def swiglu_moe_fwd(x, W1, W2, counts, preact=None, y=None, workspace=None):
     arr, En, total = _counts(counts)
     if En != E or total != T:
         raise ValueError(f"counts: {En} experts summing to {total}, expected {E} and {T}")
-    preact = _empty((T, 2 * H), x) if preact is None else preact
-    y = _empty((T, Dout), x) if y is None else y
+    preact = _out(preact, "preact", (T, 2 * H), x)
+    y = _out(y, "y", (T, Dout), x)
+    _same_device(x, workspace=workspace)
     if workspace is None:
         workspace = torch.empty(max(16, swiglu_moe_fwd_workspace_size(counts, D, H, Dout)), dtype=torch.uint8,
                                 device=x.device)
     st = lib().swiglu_moe_fwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(y), ctypes.cast(arr, _vp), E, D, H,
-                              Dout, _ptr(workspace), workspace.numel(), _stream(x.device))
+                              Dout, _ptr(workspace), _nbytes(workspace), _stream(x.device))
     _check(st, "swiglu_moe_fwd")
     return preact, y
 
@@ -387,14 +425,17 @@ def swiglu_moe_bwd(x, W1, W2, preact, dy, counts, dx=None, dW1=None, dW2=None, w
     arr, En, total = _counts(counts)
     if En != E or total != T:
         raise ValueError(f"counts: {En} experts summing to {total}, expected {E} and {T}")
-    dx = _empty((T, D), x) if dx is None else dx
-    dW1 = _empty((E, 2 * H, D), x) if dW1 is None else dW1
-    dW2 = _empty((E, Dout, H), x) if dW2 is None else dW2
+    _expect(preact, "preact", (T, 2 * H), torch.bfloat16, x.device)
+    _expect(dy, "dy", (T, Dout), torch.bfloat16, x.device)
+    dx = _out(dx, "dx", (T, D), x)
+    dW1 = _out(dW1, "dW1", (E, 2 * H, D), x)
+    dW2 = _out(dW2, "dW2", (E, Dout, H), x)
+    _same_device(x, workspace=workspace)
     if workspace is None:
         workspace = torch.empty(max(16, swiglu_moe_bwd_workspace_size(counts, D, H, Dout)), dtype=torch.uint8,
                                 device=x.device)
     st = lib().swiglu_moe_bwd(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dW1),
                               _ptr(dW2), ctypes.cast(arr, _vp), E, D, H, Dout, _ptr(workspace),
-                              workspace.numel(), _stream(x.device))
+                              _nbytes(workspace), _stream(x.device))
     _check(st, "swiglu_moe_bwd")
     return dx, dW1, dW2
