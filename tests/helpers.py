@@ -12,7 +12,19 @@ REL_FRO = 5e-3
 MAX_ABS_FRAC = 2e-2
 
 
-def parity(gpu, ref, name=""):
+# Per-tile bar for the full-size checks, which also compare each tile's few sampled
+# rows or columns on their own.  Both sides store grad_preact and h in bf16, and where
+# the exact value lies within the fp32 path's error of a bf16 rounding midpoint the two
+# round to neighbouring values (one ulp: 2^-8 to 2^-7 relative).  When one such element
+# dominates a short reduction -- dW1 and dW2 sum over only 16 tokens at decode sizes --
+# a whole output row moves by up to 2^-7 (0.8 %), and a tile of four sampled rows then
+# reads up to that much (seen: 5.5e-3 against the tensor bar of 5e-3).  2e-2 leaves
+# room for it and still fails a tile that lost a k-block, took another tile's data or
+# was not written.
+TILE_REL_FRO = 2e-2
+
+
+def parity(gpu, ref, name="", rel_fro=REL_FRO, max_abs_frac=MAX_ABS_FRAC):
     """Assert the parity bar between a GPU tensor (any dtype) and an fp64 oracle array."""
     g = gpu.detach().float().cpu().double().numpy() if isinstance(gpu, torch.Tensor) else np.asarray(gpu, np.float64)
     r = np.asarray(ref, dtype=np.float64)
@@ -23,8 +35,8 @@ def parity(gpu, ref, name=""):
     rel = err / nr if nr > 0 else err
     mx = np.max(np.abs(r)) if r.size else 0.0
     worst = np.max(np.abs(g - r)) if r.size else 0.0
-    assert rel <= REL_FRO, f"{name}: relative Frobenius error {rel:.3e} > {REL_FRO}"
-    assert worst <= MAX_ABS_FRAC * mx + 1e-30, f"{name}: max abs error {worst:.3e} > {MAX_ABS_FRAC} * {mx:.3e}"
+    assert rel <= rel_fro, f"{name}: relative Frobenius error {rel:.3e} > {rel_fro}"
+    assert worst <= max_abs_frac * mx + 1e-30, f"{name}: max abs error {worst:.3e} > {max_abs_frac} * {mx:.3e}"
     return rel, worst
 
 
