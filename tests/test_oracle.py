@@ -501,3 +501,11 @@ def test_identity_down_projection_passes_dy_through():
     sg = 1.0 / (1.0 + np.exp(-gate))
     want_l = np.vectorize(oracle.round_bf16)(dy.double().numpy() * gate * sg)
     np.testing.assert_allclose(gp[:, :24], want_l, rtol=0, atol=0)
+    # dgate with its single bf16 rounding: silu' written in the drop-h report's form
+    # sigma + silu * (1 - sigma) (the oracle evaluates sigma * (1 + g * (1 - sigma))),
+    # times left and grad_h = dy, rounded once
+    silu_p = sg + gate * sg * (1.0 - sg)
+    want_g = np.vectorize(oracle.round_bf16)(dy.double().numpy() * left * silu_p)
+    np.testing.assert_allclose(gp[:, 24:], want_g, rtol=0, atol=0)
+    # the rounding point matters: the unrounded products differ from the stored values
+    assert np.any(dy.double().numpy() * left * silu_p != gp[:, 24:])
