@@ -4,8 +4,10 @@ swiglu_mlp_fwd_noalloc serves callers that cannot allocate device memory (a
 plugin whose host framework owns all allocations, a real-time loop that must
 not call cudaMalloc, a process with a fixed memory budget): it keeps the
 forward's transient h in a 64 MiB array built into the library instead of a
-caller workspace.  Its results must match swiglu_mlp_fwd's, and a second call
-must not be disturbed by what the first one left in that shared array.
+caller workspace.  Its results must be swiglu_mlp_fwd's bits where both run the
+same kernels (M > 64), must match the oracle where they do not (M <= 64), and a
+second call must not be disturbed by what the first one left in that shared
+array.
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test; it also passes when run alone in a new process.
@@ -46,16 +48,36 @@ def _noalloc_via_abi(b, x, W1, W2):
 @pytest.mark.parametrize("s", [Shape(300, 320, 392, 264), Shape(1024, 512, 1536, 768)],
                          ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
 def test_noalloc_forward_matches_workspace_forward_twice(b, s):
+    # For M > 64 both entry points run the same tile kernels, which are deterministic:
+    # the results must be the same bits, on each of two calls in a row.
     for call, seed in enumerate((21, 22)):      # two calls in a row, different inputs
         _, x, W1, W2, _ = workloads.make_block(s, seed=seed)
         x, W1, W2 = x.cuda(), W1.cuda(), W2.cuda()
         pre_ref, y_ref = b.swiglu_mlp_fwd(x, W1, W2)
         pre, y = _noalloc_via_abi(b, x, W1, W2)
         assert b.swiglu_mlp_device_status() == 0
-        ref_p = pre_ref.float().cpu().double().numpy()
-        ref_y = y_ref.float().cpu().double().numpy()
-        parity(pre, ref_p, f"preact (call {call})")
-        parity(y, ref_y, f"y (call {call})")
+        assert torch.equal(pre, pre_ref), f"preact (call {call})"
+        assert torch.equal(y, y_ref), f"y (call {call})"
+
+
+@pytest.mark.parametrize("s", [Shape(16, 128, 384, 512), Shape(64, 256, 520, 136)],
+                         ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}_Do{s.Dout}")
+def test_noalloc_few_tokens_against_oracle_twice(b, s):
+    # For M <= 64 the ordinary forward takes the few-token kernels while the
+    # allocation-free one keeps the tile kernels: the two are compared through the
+    # oracle (and with each other within the same bar), on two calls in a row.
+    import oracle
+    for call, seed in enumerate((23, 24)):
+        _, x, W1, W2, _ = workloads.make_block(s, seed=seed, gate_sweep=True)
+        p_ref, _, y_ref = oracle.fwd(x, W1, W2)
+        xd, W1d, W2d = x.cuda(), W1.cuda(), W2.cuda()
+        pre, y = _noalloc_via_abi(b, xd, W1d, W2d)
+        pre_ws, y_ws = b.swiglu_mlp_fwd(xd, W1d, W2d)
+        assert b.swiglu_mlp_device_status() == 0
+        parity(pre, p_ref, f"preact (call {call})")
+        parity(y, y_ref, f"y (call {call})")
+        parity(pre, pre_ws.float().cpu().double().numpy(), f"preact vs swiglu_mlp_fwd (call {call})")
+        parity(y, y_ws.float().cpu().double().numpy(), f"y vs swiglu_mlp_fwd (call {call})")
 
 
 def test_noalloc_rejects_sizes_beyond_the_builtin_scratch(b):
