@@ -618,15 +618,15 @@ size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Do
 static swiglu_status fwd_impl(const void* x, const void* W1, const void* W2, void* preact, void* y, int64_t M,
                               int64_t D, int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes,
                               void* stream, bool residual) {
-    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "forward: a size is negative or zero");
     if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
-        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+        return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "forward: unsupported shape (widths must be positive multiples of 8 below 2^31)");
     if (M == 0) return SWIGLU_OK;
-    if (!x || !W1 || !W2 || !preact || !y || !workspace) return SWIGLU_ERR_INVALID_ARG;
+    if (!x || !W1 || !W2 || !preact || !y || !workspace) return fail(SWIGLU_ERR_INVALID_ARG, "forward: a required pointer is null");
     if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(preact) || !aligned16(y) ||
         !aligned16(workspace))
-        return SWIGLU_ERR_MISALIGNED;
-    if (workspace_bytes < swiglu_mlp_fwd_workspace_size(M, D, H, Dout)) return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+        return fail(SWIGLU_ERR_MISALIGNED, "forward: a pointer is not 16-byte aligned");
+    if (workspace_bytes < swiglu_mlp_fwd_workspace_size(M, D, H, Dout)) return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "forward: workspace smaller than the size query returns");
     DeviceState* st;
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
@@ -655,11 +655,11 @@ swiglu_status swiglu_mlp_fwd_residual(const void* x, const void* W1, const void*
 static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
                               void* dx, void* dW1, void* dW2, int64_t M, int64_t D, int64_t H, int64_t Dout,
                               void* workspace, size_t workspace_bytes, void* stream, bool residual) {
-    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "backward: a size is negative or zero");
     if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
-        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
-    if (!W1 || !W2 || !dW1 || !dW2) return SWIGLU_ERR_INVALID_ARG;
-    if (!aligned16(W1) || !aligned16(W2) || !aligned16(dW1) || !aligned16(dW2)) return SWIGLU_ERR_MISALIGNED;
+        return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "backward: unsupported shape (widths must be positive multiples of 8 below 2^31)");
+    if (!W1 || !W2 || !dW1 || !dW2) return fail(SWIGLU_ERR_INVALID_ARG, "backward: a required pointer is null");
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(dW1) || !aligned16(dW2)) return fail(SWIGLU_ERR_MISALIGNED, "backward: a pointer is not 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 0) {
         cudaError_t e = cudaMemsetAsync(dW1, 0, (size_t)2 * H * D * 2, s);
@@ -667,10 +667,10 @@ static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, con
         if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync", e);
         return SWIGLU_OK;
     }
-    if (!x || !preact || !dy || !dx || !workspace) return SWIGLU_ERR_INVALID_ARG;
+    if (!x || !preact || !dy || !dx || !workspace) return fail(SWIGLU_ERR_INVALID_ARG, "backward: a required pointer is null");
     if (!aligned16(x) || !aligned16(preact) || !aligned16(dy) || !aligned16(dx) || !aligned16(workspace))
-        return SWIGLU_ERR_MISALIGNED;
-    if (workspace_bytes < swiglu_mlp_bwd_workspace_size(M, D, H, Dout)) return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+        return fail(SWIGLU_ERR_MISALIGNED, "backward: a pointer is not 16-byte aligned");
+    if (workspace_bytes < swiglu_mlp_bwd_workspace_size(M, D, H, Dout)) return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "backward: workspace smaller than the size query returns");
     DeviceState* st;
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
@@ -744,13 +744,13 @@ swiglu_status swiglu_mlp_bwd_residual(const void* x, const void* W1, const void*
 
 swiglu_status swiglu_mlp_fused_grad_preact(const void* dy, const void* W2, const void* preact, void* grad_preact,
                                            void* h, int64_t M, int64_t H, int64_t Dout, void* stream) {
-    if (M < 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_fused_grad_preact: a size is negative or zero");
     if (!dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
-        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+        return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "swiglu_mlp_fused_grad_preact: unsupported shape (widths must be positive multiples of 8 below 2^31)");
     if (M == 0) return SWIGLU_OK;
-    if (!dy || !W2 || !preact || !grad_preact || !h) return SWIGLU_ERR_INVALID_ARG;
+    if (!dy || !W2 || !preact || !grad_preact || !h) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_fused_grad_preact: a required pointer is null");
     if (!aligned16(dy) || !aligned16(W2) || !aligned16(preact) || !aligned16(grad_preact) || !aligned16(h))
-        return SWIGLU_ERR_MISALIGNED;
+        return fail(SWIGLU_ERR_MISALIGNED, "swiglu_mlp_fused_grad_preact: a pointer is not 16-byte aligned");
     DeviceState* st;
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
@@ -759,14 +759,14 @@ swiglu_status swiglu_mlp_fused_grad_preact(const void* dy, const void* W2, const
 
 swiglu_status swiglu_mlp_gemm_bf16(const void* A, const void* B, void* Cp, int64_t M, int64_t N, int64_t K,
                                    int a_mn_major, int b_mn_major, void* stream) {
-    if (M <= 0 || N <= 0 || K <= 0) return SWIGLU_ERR_INVALID_ARG;
-    if (!A || !B || !Cp) return SWIGLU_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_gemm_bf16: a size is negative or zero");
+    if (!A || !B || !Cp) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_gemm_bf16: a required pointer is null");
     const int64_t a_inner = a_mn_major ? M : K;
     const int64_t b_inner = b_mn_major ? N : K;
     if (a_inner % 8 || b_inner % 8 || N % 8 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
         K >= (int64_t(1) << 31))
-        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(Cp)) return SWIGLU_ERR_MISALIGNED;
+        return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "swiglu_mlp_gemm_bf16: unsupported shape (widths must be positive multiples of 8 below 2^31)");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(Cp)) return fail(SWIGLU_ERR_MISALIGNED, "swiglu_mlp_gemm_bf16: a pointer is not 16-byte aligned");
     DeviceState* st;
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
@@ -878,13 +878,13 @@ swiglu_status scratch_address(void** out) {
 extern "C" swiglu_status swiglu_mlp_fwd_noalloc(const void* x, const void* W1, const void* W2, void* preact,
                                                 void* y, int64_t M, int64_t D, int64_t H, int64_t Dout,
                                                 void* stream) {
-    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_fwd_noalloc: a size is negative or zero");
     if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
-        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+        return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "swiglu_mlp_fwd_noalloc: unsupported shape (widths must be positive multiples of 8 below 2^31)");
     if (M == 0) return SWIGLU_OK;
-    if (!x || !W1 || !W2 || !preact || !y) return SWIGLU_ERR_INVALID_ARG;
+    if (!x || !W1 || !W2 || !preact || !y) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_fwd_noalloc: a required pointer is null");
     if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(preact) || !aligned16(y))
-        return SWIGLU_ERR_MISALIGNED;
+        return fail(SWIGLU_ERR_MISALIGNED, "swiglu_mlp_fwd_noalloc: a pointer is not 16-byte aligned");
     const size_t need = (size_t)M * (size_t)H * 2;
     if (need > (size_t)SWIGLU_MLP_NOALLOC_SCRATCH_BYTES) {
         std::snprintf(g_detail, sizeof g_detail,
@@ -1130,7 +1130,7 @@ T* at_row(void* base, int64_t row, int64_t width) {
 
 swiglu_status moe_check(const std::vector<int64_t>& off, const MoeDims& d) {
     if (!dims_ok(d.D) || !dims_ok(d.H) || !dims_ok(d.Dout) || 2 * d.H >= (int64_t(1) << 31))
-        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+        return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "moe_check: unsupported shape (widths must be positive multiples of 8 below 2^31)");
     (void)off;
     return SWIGLU_OK;
 }
@@ -1159,17 +1159,17 @@ swiglu_status swiglu_moe_fwd(const void* x, const void* W1, const void* W2, void
                              const int64_t* counts, int64_t E, int64_t D, int64_t H, int64_t Dout,
                              void* workspace, size_t workspace_bytes, void* stream) {
     std::vector<int64_t> off;
-    if (!moe_offsets(counts, E, off) || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (!moe_offsets(counts, E, off) || D <= 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_moe_fwd: invalid expert counts or a size that is not positive");
     const MoeDims d{E, D, H, Dout, off[E]};
     swiglu_status rc = moe_check(off, d);
     if (rc != SWIGLU_OK) return rc;
     if (d.T == 0) return SWIGLU_OK;
-    if (!x || !W1 || !W2 || !preact || !y || !workspace) return SWIGLU_ERR_INVALID_ARG;
+    if (!x || !W1 || !W2 || !preact || !y || !workspace) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_moe_fwd: a required pointer is null");
     if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(preact) || !aligned16(y) ||
         !aligned16(workspace))
-        return SWIGLU_ERR_MISALIGNED;
+        return fail(SWIGLU_ERR_MISALIGNED, "swiglu_moe_fwd: a pointer is not 16-byte aligned");
     if (workspace_bytes < swiglu_moe_fwd_workspace_size(counts, E, D, H, Dout))
-        return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+        return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "swiglu_moe_fwd: workspace smaller than the size query returns");
     DeviceState* st;
     rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
@@ -1218,18 +1218,18 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
                              void* dx, void* dW1, void* dW2, const int64_t* counts, int64_t E, int64_t D,
                              int64_t H, int64_t Dout, void* workspace, size_t workspace_bytes, void* stream) {
     std::vector<int64_t> off;
-    if (!moe_offsets(counts, E, off) || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (!moe_offsets(counts, E, off) || D <= 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_moe_bwd: invalid expert counts or a size that is not positive");
     const MoeDims d{E, D, H, Dout, off[E]};
     swiglu_status rc = moe_check(off, d);
     if (rc != SWIGLU_OK) return rc;
-    if (!W1 || !W2 || !dW1 || !dW2) return SWIGLU_ERR_INVALID_ARG;
-    if (!aligned16(W1) || !aligned16(W2) || !aligned16(dW1) || !aligned16(dW2)) return SWIGLU_ERR_MISALIGNED;
+    if (!W1 || !W2 || !dW1 || !dW2) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_moe_bwd: a required pointer is null");
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(dW1) || !aligned16(dW2)) return fail(SWIGLU_ERR_MISALIGNED, "swiglu_moe_bwd: a pointer is not 16-byte aligned");
     if (d.T > 0) {
-        if (!x || !preact || !dy || !dx || !workspace) return SWIGLU_ERR_INVALID_ARG;
+        if (!x || !preact || !dy || !dx || !workspace) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_moe_bwd: a required pointer is null");
         if (!aligned16(x) || !aligned16(preact) || !aligned16(dy) || !aligned16(dx) || !aligned16(workspace))
-            return SWIGLU_ERR_MISALIGNED;
+            return fail(SWIGLU_ERR_MISALIGNED, "swiglu_moe_bwd: a pointer is not 16-byte aligned");
         if (workspace_bytes < swiglu_moe_bwd_workspace_size(counts, E, D, H, Dout))
-            return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+            return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "swiglu_moe_bwd: workspace smaller than the size query returns");
     }
     DeviceState* st;
     rc = get_device_state(&st);
@@ -1412,19 +1412,19 @@ extern "C" swiglu_status swiglu_mlp_fwd_fp8(const void* x8, const void* W1_8, co
                                             float s_w1, float s_w2, float s_h, void* preact, void* h8, void* y,
                                             int64_t M, int64_t D, int64_t H, int64_t Dout, void* workspace,
                                             size_t workspace_bytes, void* stream) {
-    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return SWIGLU_ERR_INVALID_ARG;
+    if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_fwd_fp8: a size is negative or zero");
     if (D % 16 || H % 16 || !dims_ok(Dout) || D >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31) ||
         M >= (int64_t(1) << 31))
         return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "fp8 forward: D and H multiples of 16, Dout of 8");
     if (!(s_x > 0.0f) || !(s_w1 > 0.0f) || !(s_w2 > 0.0f) || !(s_h > 0.0f) || !std::isfinite(1.0f / s_h))
         return fail(SWIGLU_ERR_INVALID_ARG, "fp8 forward: scales must be positive and finite");
     if (M == 0) return SWIGLU_OK;
-    if (!x8 || !W1_8 || !W2_8 || !h8 || !y) return SWIGLU_ERR_INVALID_ARG;
+    if (!x8 || !W1_8 || !W2_8 || !h8 || !y) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_fwd_fp8: a required pointer is null");
     if (!aligned16(x8) || !aligned16(W1_8) || !aligned16(W2_8) || !aligned16(h8) || !aligned16(y) ||
         (preact && !aligned16(preact)) || (workspace && !aligned16(workspace)))
-        return SWIGLU_ERR_MISALIGNED;
+        return fail(SWIGLU_ERR_MISALIGNED, "swiglu_mlp_fwd_fp8: a pointer is not 16-byte aligned");
     const size_t need = swiglu_mlp_fwd_fp8_workspace_size(M, D, H, Dout);
-    if (need > 0 && (!workspace || workspace_bytes < need)) return SWIGLU_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "swiglu_mlp_fwd_fp8: workspace smaller than the size query returns");
     DeviceState* st;
     swiglu_status rc = get_device_state(&st);
     if (rc != SWIGLU_OK) return rc;
