@@ -113,6 +113,14 @@ def _ptr(t: torch.Tensor | None):
 
 
 def _stream(device) -> ctypes.c_void_p:
+    """The current stream of `device`, which must be the current CUDA device: the
+    library launches on the current device (and keeps its per-device state there),
+    so tensors on another GPU would be addressed from the wrong one."""
+    if device is not None:
+        device = torch.device(device)
+        if device.type == "cuda" and device.index is not None and device.index != torch.cuda.current_device():
+            raise ValueError(f"tensors are on {device} but the current CUDA device is cuda:"
+                             f"{torch.cuda.current_device()}; call inside torch.cuda.device({device.index})")
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 

@@ -114,3 +114,11 @@ def test_wrong_buffers_are_refused_by_name(b):
     for call, err, match in _wrong_calls(b):
         with pytest.raises(err, match=match):
             call()
+
+
+def test_tensors_on_another_device_than_the_current_one_are_refused(b, monkeypatch):
+    # The library launches on the current CUDA device; tensors on another GPU would be
+    # addressed from the wrong one.  The binding refuses before any launch.
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    with pytest.raises(ValueError, match="current CUDA device"):
+        b._stream(torch.device("cuda", 0))
