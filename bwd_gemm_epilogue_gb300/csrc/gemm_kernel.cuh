@@ -101,6 +101,8 @@ struct Problem {
     int band;         // n-tiles per raster band (L2 reuse)
     int k_blocks;
     int a_mn, b_mn;   // operand major-ness (1 = M- or N-contiguous)
+    int a3d, b3d;     // an MN-major operand whose M (N) is a multiple of 64 has a 3-D map
+                      // (64, K, MN / 64): one copy per k-block instead of one per 64 rows
     int res;          // EPI_STORE_ADD: add the residual tensor (tensor map i0) to this problem's output
     int tile_begin;   // index of this problem's first tile in the launch
     int no_o0;        // EPI_SWIGLU_FWD: do not store preact (o0), only h
@@ -166,6 +168,7 @@ struct TableArgs {
     int* err;
     int debug_flags;
     int common_k_blocks, common_a_mn, common_b_mn;   // SRC_TABLE_COMMON: shared by every problem
+    int common_a3d, common_b3d;
 };
 
 template <int EPI, int CG>
@@ -502,9 +505,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             const uint32_t full_bar_leader = CG == 2 ? ptx::mapa_shared(full_bar(0), 0) : 0u;
             int stage = 0;
             uint32_t phase = 0;
-            int last_parity[C::STAGES];
-#pragma unroll
-            for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
+            uint32_t issued = 0, last_par = 0;   // per stage: a copy was issued, and its phase parity
             bool ok = true;
             int seen_pi = -1;
             for (int it = t_first; it < t_end && ok; it += t_step) {
@@ -520,8 +521,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 }
                 // One tile's k-blocks.  Called with parameter-block fields wherever the
                 // source allows it (see SRC_TABLE_COMMON).
-                auto tile = [&](const Problem& p, int k_blocks, bool a_mn, bool b_mn, const CUtensorMap* ma,
-                                const CUtensorMap* mb) {
+                auto tile = [&](const Problem& p, int k_blocks, bool a_mn, bool b_mn, bool a3d, bool b3d,
+                                const CUtensorMap* ma, const CUtensorMap* mb) {
                     int tm, tn;
                     tile_coords(p, lt, tm, tn);
                     const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
@@ -534,7 +535,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         // CG == 2: both CTAs' copies complete on the leader's stage barrier.
                         const uint32_t fb = CG == 2 ? full_bar_leader + 8u * stage : fb_local;
                         if (leader) ptx::mbar_arrive_expect_tx(fb_local, C::TX_BYTES);
-                        last_parity[stage] = (int)phase;
+                        issued |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         const int k0 = kb * BKE;
                         const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
                         const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
@@ -542,9 +544,17 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                             if (CG == 2) ptx::tma_load_2d_pair(dst, m, fb, c0, c1);
                             else ptx::tma_load_2d(dst, m, fb, c0, c1);
                         };
+                        auto load3 = [&](uint32_t dst, const CUtensorMap* m, int c1, int c2) {
+                            if (CG == 2) ptx::tma_load_3d_pair(dst, m, fb, 0, c1, c2);
+                            else ptx::tma_load_3d(dst, m, fb, 0, c1, c2);
+                        };
                         if (a_mn) {
-                            load2(sA, ma, m0, k0);
-                            load2(sA + 8192, ma, m0 + 64, k0);
+                            if (a3d) {
+                                load3(sA, ma, k0, m0 >> 6);   // both 64-row blocks in one copy
+                            } else {
+                                load2(sA, ma, m0, k0);
+                                load2(sA + 8192, ma, m0 + 64, k0);
+                            }
                         } else {
                             load2(sA, ma, k0, m0);
                         }
@@ -559,8 +569,12 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                             }
                         } else if (b_mn) {
                             const int n0 = tn * BN + C::B_ROWS * (int)rank;
+                            if (b3d) {
+                                load3(sB, mb, k0, n0 >> 6);   // all 64-row blocks in one copy
+                            } else {
 #pragma unroll
-                            for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mb, n0 + 64 * i, k0);
+                                for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mb, n0 + 64 * i, k0);
+                            }
                         } else {
                             load2(sB, mb, k0, tn * BN + C::B_ROWS * (int)rank);
                         }
@@ -573,29 +587,30 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 if constexpr (SCHED == SRC_PARAMS) {
                     // one copy per problem index: that problem's fields at fixed offsets
                     auto fixed = [&](const Problem& p, const CUtensorMap* ma, const CUtensorMap* mb) {
-                        tile(p, p.k_blocks, p.a_mn != 0, p.b_mn != 0, ma, mb);
+                        tile(p, p.k_blocks, p.a_mn != 0, p.b_mn != 0, p.a3d != 0, p.b3d != 0, ma, mb);
                     };
                     if (pi == 0) fixed(args.prob[0], &args.a[0], &args.b[0]);
                     else if (pi == 1) fixed(args.prob[1], &args.a[1], &args.b[1]);
                     else fixed(args.prob[2], &args.a[2], &args.b[2]);
                 } else if constexpr (SCHED == SRC_TABLE_COMMON) {
-                    tile(pr, args.common_k_blocks, args.common_a_mn != 0, args.common_b_mn != 0, mA, mB);
+                    tile(pr, args.common_k_blocks, args.common_a_mn != 0, args.common_b_mn != 0, args.common_a3d != 0,
+                         args.common_b3d != 0, mA, mB);
                 } else if constexpr (SCHED == SRC_TABLE) {
                     // one copy per operand layout: the layout as a compile-time constant
-                    const bool am = pr.a_mn != 0, bm = pr.b_mn != 0;
-                    if (am && bm) tile(pr, pr.k_blocks, true, true, mA, mB);
-                    else if (am) tile(pr, pr.k_blocks, true, false, mA, mB);
-                    else if (bm) tile(pr, pr.k_blocks, false, true, mA, mB);
-                    else tile(pr, pr.k_blocks, false, false, mA, mB);
+                    const bool am = pr.a_mn != 0, bm = pr.b_mn != 0, a3 = pr.a3d != 0, b3 = pr.b3d != 0;
+                    if (am && bm) tile(pr, pr.k_blocks, true, true, a3, b3, mA, mB);
+                    else if (am) tile(pr, pr.k_blocks, true, false, a3, false, mA, mB);
+                    else if (bm) tile(pr, pr.k_blocks, false, true, false, b3, mA, mB);
+                    else tile(pr, pr.k_blocks, false, false, false, false, mA, mB);
                 } else {
-                    tile(pr, pr.k_blocks, pr.a_mn != 0, pr.b_mn != 0, mA, mB);
+                    tile(pr, pr.k_blocks, pr.a_mn != 0, pr.b_mn != 0, pr.a3d != 0, pr.b3d != 0, mA, mB);
                 }
             }
             if (!ok) {
                 // Let the loads already issued land before the CTA's shared memory goes away.
                 if (leader) {
                     for (int s = 0; s < C::STAGES; ++s)
-                        if (last_parity[s] >= 0) drain_wait(full_bar(s), (uint32_t)last_parity[s], tmo);
+                        if ((issued >> s) & 1u) drain_wait(full_bar(s), (last_par >> s) & 1u, tmo);
                 } else {
                     spin_ns(100000);
                 }

@@ -124,9 +124,23 @@ bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Operand maps for the mainloop.  K-major: box 64 (k) x rows; MN-major: box 64 (mn) x 64 (k).
-bool encode_operand(CUtensorMap* m, const void* ptr, int64_t mn, int64_t k, bool mn_major, uint32_t rows) {
-    if (mn_major) return encode_2d(m, ptr, (uint64_t)mn, (uint64_t)k, (uint64_t)mn * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+// Operand maps for the mainloop.  K-major: box 64 (k) x rows.  MN-major: box 64 (mn) x
+// 64 (k), one copy per 64 rows -- or, when MN is a multiple of 64 and `three_d` is given,
+// the 3-D view (64 mn, k, mn / 64) with box 64 x 64 x rows / 64, whose copy lands the
+// same rows / 64 blocks of 8 KB in shared memory with a single instruction (*three_d is
+// set then).  Fewer copies per k-block relieve the producer thread.
+bool encode_operand(CUtensorMap* m, const void* ptr, int64_t mn, int64_t k, bool mn_major, uint32_t rows,
+                    bool* three_d = nullptr) {
+    if (three_d) *three_d = false;
+    if (mn_major) {
+        if (three_d && mn % 64 == 0 && rows >= 64 && rows % 64 == 0 &&
+            encode_3d(m, ptr, 64, (uint64_t)k, (uint64_t)(mn / 64), (uint64_t)mn * 2, 128, 64, 64, rows / 64,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) {
+            *three_d = true;
+            return true;
+        }
+        return encode_2d(m, ptr, (uint64_t)mn, (uint64_t)k, (uint64_t)mn * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     return encode_2d(m, ptr, (uint64_t)k, (uint64_t)mn, (uint64_t)k * 2, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -172,6 +186,8 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     p.k_blocks = (int)((K + BK - 1) / BK);
     p.a_mn = a_mn ? 1 : 0;
     p.b_mn = b_mn ? 1 : 0;
+    p.a3d = 0;
+    p.b3d = 0;
     p.res = 0;
     p.tile_begin = 0;
     p.no_o0 = 0;
@@ -523,7 +539,8 @@ swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, con
     std::memset(&a, 0, sizeof a);
     if (!encode_operand(&a.a[0], dy, M, Dout, false, BM)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (a)");
     // B(n = j, k = o) = W2[o, j]: MN-major
-    if (!encode_operand(&a.b[0], W2, H, Dout, true, 0)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
+    bool b3d = false;
+    if (!encode_operand(&a.b[0], W2, H, Dout, true, BN / cg, &b3d)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
     constexpr uint32_t ck = Cfg<EPI_SWIGLU_BWD, 2>::CK;
     static_assert(ck == Cfg<EPI_SWIGLU_BWD, 1>::CK, "one chunk width for both tile sizes");
     if (!encode_paired(&a.o0[0], grad_preact, M, H, 32, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
@@ -531,6 +548,7 @@ swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, con
     if (!encode_paired(&a.i0, preact, M, H, BM, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
     a.num_problems = 1;
     a.prob[0] = make_problem(M, H, Dout, (H + BN - 1) / BN, false, true, cg);
+    a.prob[0].b3d = b3d ? 1 : 0;
     if (cg == 2) return launch<EPI_SWIGLU_BWD, 2, SRC_SINGLE>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
     return launch<EPI_SWIGLU_BWD, 1, SRC_SINGLE>(st, SWIGLU_KERNEL_BWD_GRAD_H, a, s);
 }
@@ -547,10 +565,13 @@ struct GemmSpec {
 // Fill problem q of `a`: C [M,N] = A * B^T (+ R) with either operand K-major or MN-major.
 // A residual goes through the launch's single residual map i0.
 bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg) {
-    if (!encode_operand(&a.a[q], g.A, g.M, g.K, g.a_mn, BM)) return false;
-    if (!encode_operand(&a.b[q], g.B, g.N, g.K, g.b_mn, BN / cg)) return false;
+    bool a3d = false, b3d = false;
+    if (!encode_operand(&a.a[q], g.A, g.M, g.K, g.a_mn, BM, &a3d)) return false;
+    if (!encode_operand(&a.b[q], g.B, g.N, g.K, g.b_mn, BN / cg, &b3d)) return false;
     if (!encode_out_2d(&a.o0[q], g.C, g.M, g.N)) return false;
     a.prob[q] = make_problem(g.M, g.N, g.K, (g.N + BN - 1) / BN, g.a_mn, g.b_mn, cg);
+    a.prob[q].a3d = a3d ? 1 : 0;
+    a.prob[q].b3d = b3d ? 1 : 0;
     if (g.R) {
         if (!encode_2d(&a.i0, g.R, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.N * 2, CHUNK, BM, CU_TENSOR_MAP_SWIZZLE_64B))
             return false;
@@ -994,7 +1015,8 @@ swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& e
     bool common = true;
     for (const TableEntry& e : ents)
         common = common && e.prob.k_blocks == ents[0].prob.k_blocks && e.prob.a_mn == ents[0].prob.a_mn &&
-                 e.prob.b_mn == ents[0].prob.b_mn;
+                 e.prob.b_mn == ents[0].prob.b_mn && e.prob.a3d == ents[0].prob.a3d &&
+                 e.prob.b3d == ents[0].prob.b3d;
     const int slots = common ? cluster_slots<EPI, CG, SRC_TABLE_COMMON>(st) : cluster_slots<EPI, CG, SRC_TABLE>(st);
     if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
     const int units = (int)std::min<long long>(tiles, std::min(slots, kMaxUnits));
@@ -1048,6 +1070,8 @@ swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& e
     a.common_k_blocks = ents[0].prob.k_blocks;
     a.common_a_mn = ents[0].prob.a_mn;
     a.common_b_mn = ents[0].prob.b_mn;
+    a.common_a3d = ents[0].prob.a3d;
+    a.common_b3d = ents[0].prob.b3d;
     if (common) return launch_grid<EPI, CG, SRC_TABLE_COMMON>(st, kind, a, units, s);
     return launch_grid<EPI, CG, SRC_TABLE>(st, kind, a, units, s);
 }
@@ -1112,10 +1136,13 @@ size_t moe_bwd_tables(const std::vector<int64_t>& off, const MoeDims& d, size_t*
 // Plain-GEMM entry: C [M,N] = A * B^T, either operand K-major or MN-major.
 bool fill_gemm(TableEntry& t, const GemmSpec& g, int cg) {
     std::memset(&t, 0, sizeof t);
-    if (!encode_operand(&t.a, g.A, g.M, g.K, g.a_mn, BM)) return false;
-    if (!encode_operand(&t.b, g.B, g.N, g.K, g.b_mn, BN / cg)) return false;
+    bool a3d = false, b3d = false;
+    if (!encode_operand(&t.a, g.A, g.M, g.K, g.a_mn, BM, &a3d)) return false;
+    if (!encode_operand(&t.b, g.B, g.N, g.K, g.b_mn, BN / cg, &b3d)) return false;
     if (!encode_out_2d(&t.o0, g.C, g.M, g.N)) return false;
     t.prob = make_problem(g.M, g.N, g.K, (g.N + BN - 1) / BN, g.a_mn, g.b_mn, cg);
+    t.prob.a3d = a3d ? 1 : 0;
+    t.prob.b3d = b3d ? 1 : 0;
     return true;
 }
 
@@ -1259,14 +1286,16 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
         ents.emplace_back();
         TableEntry& t = ents.back();
         std::memset(&t, 0, sizeof t);
+        bool b3d = false;
         bool ok = encode_operand(&t.a, at_row<uint8_t>(dy, off[e], Dout), m, Dout, false, BM);
-        ok = ok && encode_operand(&t.b, at_row<uint8_t>(W2, e * Dout, H), H, Dout, true, 0);
+        ok = ok && encode_operand(&t.b, at_row<uint8_t>(W2, e * Dout, H), H, Dout, true, BN / cg, &b3d);
         constexpr uint32_t ck = Cfg<EPI_SWIGLU_BWD, 2>::CK;
         ok = ok && encode_paired(&t.o0, at_row<uint8_t>(gp, off[e], 2 * H), m, H, 32, ck);
         ok = ok && encode_out_2d(&t.o1, at_row<uint8_t>(h, off[e], H), m, H, ck);
         ok = ok && encode_paired(&t.i0, at_row<uint8_t>(preact, off[e], 2 * H), m, H, BM, ck);
         if (!ok) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe grad_h)");
         t.prob = make_problem(m, H, Dout, (H + BN - 1) / BN, false, true, cg);
+        t.prob.b3d = b3d ? 1 : 0;
     }
     rc = cg == 2 ? launch_table<EPI_SWIGLU_BWD, 2>(st, SWIGLU_KERNEL_BWD_GRAD_H, ents, table_a, tab_a, s)
                  : launch_table<EPI_SWIGLU_BWD, 1>(st, SWIGLU_KERNEL_BWD_GRAD_H, ents, table_a, tab_a, s);
