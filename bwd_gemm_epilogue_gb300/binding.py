@@ -54,6 +54,12 @@ SIGNATURES = {
     "swiglu_mlp_trace_begin": (None, [_vp, _vp, _i32]),
     "swiglu_mlp_trace_end": (_i32, []),
     "swiglu_mlp_abi_version": (_i32, []),
+    "swiglu_mlp_tp_shard_pack": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp]),
+    "swiglu_mlp_tp_shard_unpack_grads": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp]),
+    "swiglu_mlp_tp_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _vp, _sz, _vp]),
+    "swiglu_mlp_tp_chunk_rows": (_i64, [_i64, _i32]),
+    "swiglu_mlp_tp_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _sz,
+                                 _vp]),
     "swiglu_moe_fwd_workspace_size": (_sz, [_vp, _i64, _i64, _i64, _i64]),
     "swiglu_moe_bwd_workspace_size": (_sz, [_vp, _i64, _i64, _i64, _i64]),
     "swiglu_moe_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
@@ -292,6 +298,100 @@ def swiglu_mlp_bwd(x, W1, W2, preact, dy, dx=None, dW1=None, dW2=None, workspace
     st = fn(_ptr(x), _ptr(W1), _ptr(W2), _ptr(preact), _ptr(dy), _ptr(dx), _ptr(dW1), _ptr(dW2),
             M, D, H, Dout, _ptr(workspace), _nbytes(workspace), _stream(x.device))
     _check(st, "swiglu_mlp_bwd_residual" if residual else "swiglu_mlp_bwd")
+    return dx, dW1, dW2
+
+
+# ---------------------------------------------------------------------------- tensor-parallel shards
+
+def swiglu_mlp_tp_shard_pack(W1, W2, j0: int, Hs: int, W1_shard=None, W2_shard=None):
+    """Rank shard of the full weights: W1_shard [2*Hs, D] (rows j0.. and H + j0..),
+    W2_shard [Dout, Hs] (columns j0..)."""
+    H2, D = W1.shape
+    Dout, H = W2.shape
+    if H2 != 2 * H:
+        raise ValueError(f"shape mismatch: W1 {tuple(W1.shape)}, W2 {tuple(W2.shape)}")
+    _expect(W1, "W1", (2 * H, D), torch.bfloat16, W1.device)
+    _expect(W2, "W2", (Dout, H), torch.bfloat16, W1.device)
+    W1_shard = _out(W1_shard, "W1_shard", (2 * Hs, D), W1)
+    W2_shard = _out(W2_shard, "W2_shard", (Dout, Hs), W1)
+    st = lib().swiglu_mlp_tp_shard_pack(_ptr(W1), _ptr(W2), _ptr(W1_shard), _ptr(W2_shard), D, H, Dout, j0, Hs,
+                                        _stream(W1.device))
+    _check(st, "swiglu_mlp_tp_shard_pack")
+    return W1_shard, W2_shard
+
+
+def swiglu_mlp_tp_shard_unpack_grads(dW1_shard, dW2_shard, dW1, dW2, j0: int):
+    """Write a shard's weight gradients into rows j0.., H + j0.. of dW1 and columns j0.. of dW2."""
+    H2, D = dW1.shape
+    Dout, H = dW2.shape
+    Hs = dW2_shard.shape[1]
+    _expect(dW1, "dW1", (2 * H, D), torch.bfloat16, dW1.device)
+    _expect(dW2, "dW2", (Dout, H), torch.bfloat16, dW1.device)
+    _expect(dW1_shard, "dW1_shard", (2 * Hs, D), torch.bfloat16, dW1.device)
+    _expect(dW2_shard, "dW2_shard", (Dout, Hs), torch.bfloat16, dW1.device)
+    st = lib().swiglu_mlp_tp_shard_unpack_grads(_ptr(dW1_shard), _ptr(dW2_shard), _ptr(dW1), _ptr(dW2), D, H, Dout,
+                                                j0, Hs, _stream(dW1.device))
+    _check(st, "swiglu_mlp_tp_shard_unpack_grads")
+    return dW1, dW2
+
+
+def swiglu_mlp_tp_chunk_rows(M: int, n_chunks: int) -> int:
+    return int(lib().swiglu_mlp_tp_chunk_rows(M, n_chunks))
+
+
+def _events(events):
+    if not events:
+        return None, None
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    return arr, len(events)
+
+
+def swiglu_mlp_tp_fwd(x, W1_shard, W2_shard, preact=None, y=None, workspace=None, n_chunks: int = 1,
+                      chunk_events=None):
+    """Shard forward: (preact_shard [M, 2*Hs], partial y [M, Dout]).  chunk_events: n_chunks
+    torch.cuda.Event objects, recorded when the rows of chunk c of y are final."""
+    M, D, Hs, Dout = _dims(x, W1_shard, W2_shard)
+    preact = _out(preact, "preact", (M, 2 * Hs), x)
+    y = _out(y, "y", (M, Dout), x)
+    _same_device(x, workspace=workspace)
+    if workspace is None:
+        workspace = torch.empty(max(16, swiglu_mlp_fwd_workspace_size(M, D, Hs, Dout)), dtype=torch.uint8,
+                                device=x.device)
+    if chunk_events is not None and len(chunk_events) != n_chunks:
+        raise ValueError(f"chunk_events: {len(chunk_events)} events for {n_chunks} chunks")
+    for e in chunk_events or ():
+        if e.cuda_event == 0:   # a torch event is created on its first record
+            e.record(torch.cuda.current_stream(x.device))
+    arr, _ = _events(chunk_events)
+    st = lib().swiglu_mlp_tp_fwd(_ptr(x), _ptr(W1_shard), _ptr(W2_shard), _ptr(preact), _ptr(y), M, D, Hs, Dout,
+                                 n_chunks, arr, _ptr(workspace), _nbytes(workspace), _stream(x.device))
+    _check(st, "swiglu_mlp_tp_fwd")
+    return preact, y
+
+
+def swiglu_mlp_tp_bwd(x, W1_shard, W2_shard, preact, dy, dx=None, dW1=None, dW2=None, workspace=None,
+                      dx_event=None):
+    """Shard backward: (partial dx [M, D], dW1_shard [2*Hs, D], dW2_shard [Dout, Hs]).
+    dx_event: a torch.cuda.Event recorded when dx is final, before the weight gradients."""
+    M, D, Hs, Dout = _dims(x, W1_shard, W2_shard)
+    _expect(preact, "preact", (M, 2 * Hs), torch.bfloat16, x.device)
+    _expect(dy, "dy", (M, Dout), torch.bfloat16, x.device)
+    dx = _out(dx, "dx", (M, D), x)
+    dW1 = _out(dW1, "dW1", (2 * Hs, D), x)
+    dW2 = _out(dW2, "dW2", (Dout, Hs), x)
+    _same_device(x, workspace=workspace)
+    if workspace is None:
+        workspace = torch.empty(max(16, swiglu_mlp_bwd_workspace_size(M, D, Hs, Dout)), dtype=torch.uint8,
+                                device=x.device)
+    ev = None
+    if dx_event is not None:
+        if dx_event.cuda_event == 0:
+            dx_event.record(torch.cuda.current_stream(x.device))
+        ev = ctypes.c_void_p(dx_event.cuda_event)
+    st = lib().swiglu_mlp_tp_bwd(_ptr(x), _ptr(W1_shard), _ptr(W2_shard), _ptr(preact), _ptr(dy), _ptr(dx),
+                                 _ptr(dW1), _ptr(dW2), M, D, Hs, Dout, ev, _ptr(workspace), _nbytes(workspace),
+                                 _stream(x.device))
+    _check(st, "swiglu_mlp_tp_bwd")
     return dx, dW1, dW2
 
 

@@ -673,9 +673,20 @@ swiglu_status swiglu_mlp_fwd_residual(const void* x, const void* W1, const void*
     return fwd_impl(x, W1, W2, preact, y, M, D, H, Dout, workspace, workspace_bytes, stream, true);
 }
 
+// Records `event` (a cudaEvent_t, may be NULL) on `s`.
+static swiglu_status record_event(void* event, cudaStream_t s) {
+    if (!event) return SWIGLU_OK;
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(event), s);
+    return e == cudaSuccess ? SWIGLU_OK : fail(SWIGLU_ERR_CUDA, "cudaEventRecord", e);
+}
+
+// dx_event (tensor-parallel backward): when set, dx is computed by a launch of its own and
+// the event is recorded after it, before the weight gradients' launch, so that a caller
+// can reduce dx across ranks while dW1 and dW2 are computed.
 static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
                               void* dx, void* dW1, void* dW2, int64_t M, int64_t D, int64_t H, int64_t Dout,
-                              void* workspace, size_t workspace_bytes, void* stream, bool residual) {
+                              void* workspace, size_t workspace_bytes, void* stream, bool residual,
+                              void* dx_event = nullptr) {
     if (M < 0 || D <= 0 || H <= 0 || Dout <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "backward: a size is negative or zero");
     if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || M >= (int64_t(1) << 31) || 2 * H >= (int64_t(1) << 31))
         return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "backward: unsupported shape (widths must be positive multiples of 8 below 2^31)");
@@ -686,7 +697,7 @@ static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, con
         cudaError_t e = cudaMemsetAsync(dW1, 0, (size_t)2 * H * D * 2, s);
         if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, (size_t)Dout * H * 2, s);
         if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync", e);
-        return SWIGLU_OK;
+        return record_event(dx_event, s);
     }
     if (!x || !preact || !dy || !dx || !workspace) return fail(SWIGLU_ERR_INVALID_ARG, "backward: a required pointer is null");
     if (!aligned16(x) || !aligned16(preact) || !aligned16(dy) || !aligned16(dx) || !aligned16(workspace))
@@ -721,6 +732,8 @@ static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, con
             return cudaGetLastError();
         });
         if (rc != SWIGLU_OK) return rc;
+        rc = record_event(dx_event, s);
+        if (rc != SWIGLU_OK) return rc;
         // the weight gradients (K = M) are output-bound: the regular kernels, as one launch when both use CTA pairs
         const GemmSpec wg[2] = {{dy, w.h, dW2, Dout, H, M, true, true}, {w.gp, x, dW1, 2 * H, D, M, true, true}};
         if (pick_cg(Dout) == 2 && pick_cg(2 * H) == 2 && !(g_debug_flags.load() & DEBUG_UNGROUPED))
@@ -737,6 +750,22 @@ static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, con
         {grad_preact, x, dW1, 2 * H, D, M, true, true},       // dW1 = grad_preact^T @ x (merged)
     };
     if (residual) g[1].R = dy;
+    if (dx_event) {
+        // dx first, on its own; then dW2 and dW1 (one launch when both use CTA pairs)
+        rc = run_gemm(st, SWIGLU_KERNEL_BWD_DX, g[1].A, g[1].B, g[1].C, g[1].M, g[1].N, g[1].K, false, true, s, g[1].R);
+        if (rc != SWIGLU_OK) return rc;
+        rc = record_event(dx_event, s);
+        if (rc != SWIGLU_OK) return rc;
+        const GemmSpec wg[2] = {g[0], g[2]};
+        int64_t wtiles = 0;
+        for (const GemmSpec& q : wg) wtiles += ((q.M + 2 * BM - 1) / (2 * BM)) * ((q.N + BN - 1) / BN);
+        if (!(g_debug_flags.load() & (DEBUG_UNGROUPED | DEBUG_FORCE_SINGLE_CTA)) && Dout > BM && 2 * H > BM &&
+            wtiles <= MAX_SCHED)
+            return run_gemm_group(st, SWIGLU_KERNEL_BWD_GEMMS, wg, 2, s);
+        rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, g[0].A, g[0].B, g[0].C, g[0].M, g[0].N, g[0].K, true, true, s);
+        if (rc != SWIGLU_OK) return rc;
+        return run_gemm(st, SWIGLU_KERNEL_BWD_DW1, g[2].A, g[2].B, g[2].C, g[2].M, g[2].N, g[2].K, true, true, s);
+    }
     int64_t pair_tiles = 0;   // tiles of the grouped launch (256-row CTA-pair tiles)
     for (const GemmSpec& q : g) pair_tiles += ((q.M + 2 * BM - 1) / (2 * BM)) * ((q.N + BN - 1) / BN);
     const bool grouped = !(g_debug_flags.load() & (DEBUG_UNGROUPED | DEBUG_FORCE_SINGLE_CTA)) && Dout > BM &&
@@ -853,7 +882,140 @@ int swiglu_mlp_trace_end(void) {
     return n;
 }
 
-int swiglu_mlp_abi_version(void) { return 200; }
+int swiglu_mlp_abi_version(void) { return 201; }
+
+// ---------------------------------------------------------------- tensor-parallel shards
+//
+// "Lesson 24: MLP, GEMM and operator fusion in the Transformer", section 33: the first
+// projection is split by columns (rank r keeps the hidden units J = [j0, j0 + Hs), i.e.
+// W1 rows J and H + J, so that its SwiGLU is local) and the down projection by rows (W2
+// columns J); each rank's y and dx are partial sums that the ranks add up (section 39:
+// the reduction of one row chunk overlaps the GEMM of the next).
+
+static swiglu_status shard_check(const char* who, int64_t D, int64_t H, int64_t Dout, int64_t j0, int64_t Hs) {
+    if (!dims_ok(D) || !dims_ok(H) || !dims_ok(Dout) || !dims_ok(Hs) || j0 < 0 || j0 % 8 != 0 || j0 + Hs > H) {
+        std::snprintf(g_detail, sizeof g_detail,
+                      "%s: need D, H, Dout, Hs positive multiples of 8 and 0 <= j0 (a multiple of 8), j0 + Hs <= H", who);
+        return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    }
+    return SWIGLU_OK;
+}
+
+swiglu_status swiglu_mlp_tp_shard_pack(const void* W1, const void* W2, void* W1_shard, void* W2_shard, int64_t D,
+                                       int64_t H, int64_t Dout, int64_t j0, int64_t Hs, void* stream) {
+    swiglu_status rc = shard_check("swiglu_mlp_tp_shard_pack", D, H, Dout, j0, Hs);
+    if (rc != SWIGLU_OK) return rc;
+    if (!W1 || !W2 || !W1_shard || !W2_shard) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_tp_shard_pack: a required pointer is null");
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(W1_shard) || !aligned16(W2_shard))
+        return fail(SWIGLU_ERR_MISALIGNED, "swiglu_mlp_tp_shard_pack: a pointer is not 16-byte aligned");
+    DeviceState* st;
+    rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint8_t* w1 = static_cast<const uint8_t*>(W1);
+    uint8_t* w1s = static_cast<uint8_t*>(W1_shard);
+    const size_t block = (size_t)Hs * D * 2;   // Hs rows of W1
+    cudaError_t e = cudaMemcpyAsync(w1s, w1 + (size_t)j0 * D * 2, block, cudaMemcpyDeviceToDevice, s);   // left rows J
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(w1s + block, w1 + (size_t)(H + j0) * D * 2, block, cudaMemcpyDeviceToDevice, s);   // gate rows H + J
+    if (e == cudaSuccess)   // W2 columns J: Dout rows of Hs values, source pitch H
+        e = cudaMemcpy2DAsync(W2_shard, (size_t)Hs * 2, static_cast<const uint8_t*>(W2) + (size_t)j0 * 2, (size_t)H * 2,
+                              (size_t)Hs * 2, (size_t)Dout, cudaMemcpyDeviceToDevice, s);
+    return e == cudaSuccess ? SWIGLU_OK : fail(SWIGLU_ERR_CUDA, "swiglu_mlp_tp_shard_pack: copy", e);
+}
+
+swiglu_status swiglu_mlp_tp_shard_unpack_grads(const void* dW1_shard, const void* dW2_shard, void* dW1, void* dW2,
+                                               int64_t D, int64_t H, int64_t Dout, int64_t j0, int64_t Hs,
+                                               void* stream) {
+    swiglu_status rc = shard_check("swiglu_mlp_tp_shard_unpack_grads", D, H, Dout, j0, Hs);
+    if (rc != SWIGLU_OK) return rc;
+    if (!dW1 || !dW2 || !dW1_shard || !dW2_shard)
+        return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_tp_shard_unpack_grads: a required pointer is null");
+    if (!aligned16(dW1) || !aligned16(dW2) || !aligned16(dW1_shard) || !aligned16(dW2_shard))
+        return fail(SWIGLU_ERR_MISALIGNED, "swiglu_mlp_tp_shard_unpack_grads: a pointer is not 16-byte aligned");
+    DeviceState* st;
+    rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint8_t* g1s = static_cast<const uint8_t*>(dW1_shard);
+    uint8_t* g1 = static_cast<uint8_t*>(dW1);
+    const size_t block = (size_t)Hs * D * 2;
+    cudaError_t e = cudaMemcpyAsync(g1 + (size_t)j0 * D * 2, g1s, block, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(g1 + (size_t)(H + j0) * D * 2, g1s + block, block, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(static_cast<uint8_t*>(dW2) + (size_t)j0 * 2, (size_t)H * 2, dW2_shard, (size_t)Hs * 2,
+                              (size_t)Hs * 2, (size_t)Dout, cudaMemcpyDeviceToDevice, s);
+    return e == cudaSuccess ? SWIGLU_OK : fail(SWIGLU_ERR_CUDA, "swiglu_mlp_tp_shard_unpack_grads: copy", e);
+}
+
+swiglu_status swiglu_mlp_tp_fwd(const void* x, const void* W1_shard, const void* W2_shard, void* preact_shard,
+                                void* y_partial, int64_t M, int64_t D, int64_t Hs, int64_t Dout, int n_chunks,
+                                void* const* chunk_events, void* workspace, size_t workspace_bytes, void* stream) {
+    if (n_chunks < 1 || n_chunks > 1024) return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_tp_fwd: n_chunks must be in 1..1024");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto record_from = [&](int c0) -> swiglu_status {
+        for (int c = c0; chunk_events && c < n_chunks; ++c) {
+            const swiglu_status r = record_event(chunk_events[c], s);
+            if (r != SWIGLU_OK) return r;
+        }
+        return SWIGLU_OK;
+    };
+    if (M <= 0 || n_chunks == 1 || use_skinny(M)) {
+        // one piece: the block forward on the shard, every chunk ready at its end
+        const swiglu_status rc = fwd_impl(x, W1_shard, W2_shard, preact_shard, y_partial, M, D, Hs, Dout, workspace,
+                                          workspace_bytes, stream, false);
+        return rc != SWIGLU_OK ? rc : record_from(0);
+    }
+    // the same argument checks as the forward
+    swiglu_status rc = fwd_impl(x, W1_shard, W2_shard, preact_shard, y_partial, 0, D, Hs, Dout, workspace,
+                                workspace_bytes, stream, false);
+    if (rc != SWIGLU_OK) return rc;
+    if (!x || !W1_shard || !W2_shard || !preact_shard || !y_partial || !workspace)
+        return fail(SWIGLU_ERR_INVALID_ARG, "swiglu_mlp_tp_fwd: a required pointer is null");
+    if (!aligned16(x) || !aligned16(W1_shard) || !aligned16(W2_shard) || !aligned16(preact_shard) ||
+        !aligned16(y_partial) || !aligned16(workspace))
+        return fail(SWIGLU_ERR_MISALIGNED, "swiglu_mlp_tp_fwd: a pointer is not 16-byte aligned");
+    if (M >= (int64_t(1) << 31)) return fail(SWIGLU_ERR_UNSUPPORTED_SHAPE, "swiglu_mlp_tp_fwd: M too large");
+    if (workspace_bytes < swiglu_mlp_fwd_workspace_size(M, D, Hs, Dout))
+        return fail(SWIGLU_ERR_WORKSPACE_TOO_SMALL, "swiglu_mlp_tp_fwd: workspace smaller than the size query returns");
+    DeviceState* st;
+    rc = get_device_state(&st);
+    if (rc != SWIGLU_OK) return rc;
+    uint8_t* h = static_cast<uint8_t*>(workspace);
+    rc = run_fwd_preact(st, x, W1_shard, preact_shard, h, M, D, Hs, s);   // every row: preact and h of the shard
+    if (rc != SWIGLU_OK) return rc;
+    // the down projection in row chunks of whole 256-row tiles; chunk c's partial y is
+    // complete when chunk_events[c] fires
+    const int64_t per = ((M + n_chunks - 1) / n_chunks + 2 * BM - 1) / (2 * BM) * (2 * BM);
+    for (int c = 0; c < n_chunks; ++c) {
+        const int64_t r0 = (int64_t)c * per;
+        if (r0 < M) {
+            const int64_t rows = std::min<int64_t>(per, M - r0);
+            rc = run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h + (size_t)r0 * Hs * 2, W2_shard,
+                          static_cast<uint8_t*>(y_partial) + (size_t)r0 * Dout * 2, rows, Dout, Hs, false, false, s);
+            if (rc != SWIGLU_OK) return rc;
+        }
+        if (chunk_events) {
+            rc = record_event(chunk_events[c], s);
+            if (rc != SWIGLU_OK) return rc;
+        }
+    }
+    return SWIGLU_OK;
+}
+
+swiglu_status swiglu_mlp_tp_bwd(const void* x, const void* W1_shard, const void* W2_shard, const void* preact_shard,
+                                const void* dy, void* dx_partial, void* dW1_shard, void* dW2_shard, int64_t M,
+                                int64_t D, int64_t Hs, int64_t Dout, void* dx_event, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    return bwd_impl(x, W1_shard, W2_shard, preact_shard, dy, dx_partial, dW1_shard, dW2_shard, M, D, Hs, Dout,
+                    workspace, workspace_bytes, stream, false, dx_event);
+}
+
+int64_t swiglu_mlp_tp_chunk_rows(int64_t M, int n_chunks) {
+    if (M <= 0 || n_chunks < 1) return 0;
+    if (n_chunks == 1 || use_skinny(M)) return M;
+    return ((M + n_chunks - 1) / n_chunks + 2 * BM - 1) / (2 * BM) * (2 * BM);
+}
 
 }  // extern "C"
 

@@ -180,6 +180,60 @@ swiglu_status swiglu_mlp_gemm_bf16(const void* A, const void* B, void* C,
                                    int a_mn_major, int b_mn_major, void* stream);
 
 /*
+ * Tensor-parallel shards of the block ("Lesson 24: MLP, GEMM and operator fusion in the
+ * Transformer", lincklin.cn, section 33, the column-parallel MLP: the first projection
+ * split by output columns, the down projection by rows, and y = Y0 + Y1 + ... summed
+ * over the ranks; section 39: the reduction overlaps the GEMM).  Rank r owns the hidden
+ * units J = [j0, j0 + Hs): W1 rows J (left) and H + J (the matching gate rows), so its
+ * SwiGLU needs nothing from the other ranks, and W2 columns J.  A shard is stored packed:
+ *   W1_shard [2*Hs, D] = rows J of W1, then rows H + J;   W2_shard [Dout, Hs] = W2[:, J].
+ * Its forward and backward are the block's on the shard (H replaced by Hs): preact_shard
+ * [M, 2*Hs] = [left_J | gate_J]; y and dx are PARTIAL sums that the caller adds across the
+ * ranks (all-reduce or reduce-scatter); the weight gradients are the shard's own, complete.
+ * Workspaces: swiglu_mlp_fwd_workspace_size / swiglu_mlp_bwd_workspace_size with H = Hs.
+ *
+ * swiglu_mlp_tp_shard_pack copies rank r's shard out of the full weights (W1 [2H, D],
+ * W2 [Dout, H]); swiglu_mlp_tp_shard_unpack_grads writes a shard's dW1_shard / dW2_shard
+ * into the rows J, H + J of a full dW1 and the columns J of a full dW2 (the other entries
+ * are left as they are).  Both are stream-ordered device copies.  Need D, H, Dout, Hs
+ * multiples of 8, j0 a multiple of 8 and j0 + Hs <= H (SWIGLU_ERR_UNSUPPORTED_SHAPE
+ * otherwise).
+ */
+swiglu_status swiglu_mlp_tp_shard_pack(const void* W1, const void* W2, void* W1_shard, void* W2_shard,
+                                       int64_t D, int64_t H, int64_t Dout, int64_t j0, int64_t Hs, void* stream);
+swiglu_status swiglu_mlp_tp_shard_unpack_grads(const void* dW1_shard, const void* dW2_shard, void* dW1, void* dW2,
+                                               int64_t D, int64_t H, int64_t Dout, int64_t j0, int64_t Hs,
+                                               void* stream);
+
+/*
+ * Shard forward: preact_shard and the partial y_partial [M, Dout] = h_J @ W2[:, J]^T.
+ * The down projection runs in n_chunks row chunks (1..1024) of
+ * swiglu_mlp_tp_chunk_rows(M, n_chunks) rows (whole 256-row tiles; the last chunk may be
+ * shorter or empty); when chunk_events is not NULL it holds n_chunks cudaEvent_t handles
+ * (caller-owned) and event c is recorded on `stream` once rows of chunk c of y_partial
+ * are final, so a communication stream can start reducing chunk c while chunk c+1 is
+ * computed.  For M <= 64 (and n_chunks = 1) the forward runs in one piece and every event
+ * is recorded at its end.
+ */
+swiglu_status swiglu_mlp_tp_fwd(const void* x, const void* W1_shard, const void* W2_shard, void* preact_shard,
+                                void* y_partial, int64_t M, int64_t D, int64_t Hs, int64_t Dout, int n_chunks,
+                                void* const* chunk_events, void* workspace, size_t workspace_bytes, void* stream);
+int64_t swiglu_mlp_tp_chunk_rows(int64_t M, int n_chunks);
+
+/*
+ * Shard backward: dx_partial [M, D] = grad_preact_J @ W1_shard (a partial sum over the
+ * ranks), dW1_shard [2*Hs, D] and dW2_shard [Dout, Hs] (complete).  When dx_event (a
+ * caller-owned cudaEvent_t) is not NULL, dx is computed by a launch of its own and the
+ * event is recorded on `stream` when dx_partial is final, before the launch that computes
+ * dW1_shard and dW2_shard, so that dx can be reduced across the ranks meanwhile.  With
+ * dx_event NULL this is swiglu_mlp_bwd on the shard.
+ */
+swiglu_status swiglu_mlp_tp_bwd(const void* x, const void* W1_shard, const void* W2_shard, const void* preact_shard,
+                                const void* dy, void* dx_partial, void* dW1_shard, void* dW2_shard, int64_t M,
+                                int64_t D, int64_t Hs, int64_t Dout, void* dx_event, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then returns SWIGLU_TIMEOUT if any kernel of this
  * library on the current device gave up a bounded wait since the last call
  * (and clears that record), SWIGLU_ERR_CUDA if the stream reports a CUDA
@@ -266,7 +320,8 @@ void swiglu_mlp_trace_begin(void** events, int* kinds, int capacity);
 int swiglu_mlp_trace_end(void);
 
 /* ABI version of this header (major * 100 + minor): 200 = the block, its residual
- * variant, the FP8 forward and (swiglu_moe.h) the MoE layer. */
+ * variant, the FP8 forward and (swiglu_moe.h) the MoE layer; 201 adds the
+ * tensor-parallel shard entry points. */
 int swiglu_mlp_abi_version(void);
 
 #ifdef __cplusplus

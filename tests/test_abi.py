@@ -42,7 +42,7 @@ def test_strerror_and_version():
     from bwd_gemm_epilogue_gb300 import binding as b
     for code, name in b.STATUS_NAMES.items():
         assert b.swiglu_mlp_strerror(code).startswith(name)
-    assert b.swiglu_mlp_abi_version() == 200
+    assert b.swiglu_mlp_abi_version() == 201
 
 
 A16 = 0x10000          # fake, 16-byte aligned "device" addresses: validation never dereferences them

@@ -139,35 +139,59 @@ def test_row_shards_with_summed_weight_gradients_give_the_full_batch():
     assert np.abs(dW1_half - dW1).max() > 1e-3 * np.abs(dW1).max()
 
 
-def _tp_worker(rank, world, port, out):
-    """Rank `rank` holds hidden columns J_r: W1 rows J_r (left) and H + J_r (gate), W2 columns J_r."""
+class _OracleShardCompute:
+    """The shard products on the host (the oracle), for the tensor-parallel module's CPU path."""
+
+    def __init__(self, rows_per_chunk):
+        self.rows = rows_per_chunk
+
+    def chunk_rows(self, M, n_chunks):
+        return self.rows
+
+    def fwd(self, x, W1s, W2s, n_chunks, events):
+        import torch
+        import oracle
+        preact, _, y = oracle.fwd(x, W1s, W2s)
+        return torch.from_numpy(preact).to(torch.bfloat16), torch.from_numpy(y)
+
+    def bwd(self, x, W1s, W2s, preact, dy, event):
+        import torch
+        import oracle
+        _, _, _, dx, dW1s, dW2s = oracle.bwd_full(x, W1s, W2s, preact, dy)
+        return torch.from_numpy(dx), torch.from_numpy(dW1s), torch.from_numpy(dW2s)
+
+
+def _tp_worker(rank, world, port, out, reduce):
+    """Rank `rank` holds hidden columns J_r: W1 rows J_r (left) and H + J_r (gate), W2 columns J_r;
+    the library's tensor-parallel module chunks and reduces its partial y and dx."""
     import sys
     sys.path.insert(0, ROOT)
     import torch
-    import oracle
     from bwd_gemm_epilogue_gb300 import workloads
+    from bwd_gemm_epilogue_gb300.tensor_parallel import TensorParallelSwiGLU, shard_bounds
     from bwd_gemm_epilogue_gb300.workloads import Shape
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         s, x, W1, W2, dy = workloads.make_block(Shape(64, 48, 96, 40), seed=11)
-        J = slice(rank * s.H // world, (rank + 1) * s.H // world)
+        j0, Hs = shard_bounds(s.H, world, rank)
+        J = slice(j0, j0 + Hs)
         W1r = torch.cat([W1[J], W1[s.H:][J]]).contiguous()
         W2r = W2[:, J].contiguous()
-        preact, _, y = oracle.fwd(x, W1r, W2r)
-        _, _, _, dx, dW1r, dW2r = oracle.bwd_full(x, W1r, W2r, torch.from_numpy(preact).to(torch.bfloat16), dy)
-        y, dx = torch.from_numpy(y), torch.from_numpy(dx)
-        dist.all_reduce(y)                       # after the down projection
-        dist.all_reduce(dx)                      # after dx = grad_preact @ W1
-        out[rank] = (y.numpy(), dx.numpy(), dW1r, dW2r)
+        tp = TensorParallelSwiGLU(W1r, W2r, n_chunks=3, reduce=reduce, compute=_OracleShardCompute(24))
+        y, preact = tp.forward(x)                     # chunked reduction after the down projection
+        dx, dW1r, dW2r = tp.backward(x, preact, dy)   # chunked reduction of dx
+        out[rank] = (y.numpy(), dx.numpy(), dW1r.numpy(), dW2r.numpy(), [tp.owner(c) for c in range(3)])
     finally:
         dist.destroy_process_group()
 
 
-def test_hidden_column_shards_with_summed_outputs_give_the_full_block():
+@pytest.mark.parametrize("reduce", ["all_reduce", "reduce_scatter"])
+def test_hidden_column_shards_with_summed_outputs_give_the_full_block(reduce):
     # Tensor parallelism over the hidden dimension: each rank's left/gate columns are a
     # complete SwiGLU of their own, so y and dx are sums of per-rank partial products and
-    # each rank's weight gradients are its slices of the full ones.
+    # each rank's weight gradients are its slices of the full ones.  The reductions go
+    # through the library's tensor-parallel module in three row chunks of 24, 24 and 16 rows.
     import sys
     sys.path.insert(0, ROOT)
     import numpy as np
@@ -179,20 +203,39 @@ def test_hidden_column_shards_with_summed_outputs_give_the_full_block():
     world = 2
     with mp.get_context("spawn").Manager() as m:
         out = m.dict()
-        mp.spawn(_tp_worker, args=(world, _free_port(), out), nprocs=world, join=True)
+        mp.spawn(_tp_worker, args=(world, _free_port(), out, reduce), nprocs=world, join=True)
         res = dict(out)
     s, x, W1, W2, dy = workloads.make_block(Shape(64, 48, 96, 40), seed=11)
     preact, _, y = oracle.fwd(x, W1, W2)
     _, _, _, dx, dW1, dW2 = oracle.bwd_full(x, W1, W2, torch.from_numpy(preact).to(torch.bfloat16), dy)
     half = s.H // world
+    chunks = [slice(0, 24), slice(24, 48), slice(48, 64)]
     for rank in range(world):
-        ys, dxs, dW1r, dW2r = res[rank]
-        np.testing.assert_allclose(ys, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
-        np.testing.assert_allclose(dxs, dx, rtol=1e-12, atol=1e-12 * np.abs(dx).max())
+        ys, dxs, dW1r, dW2r, owners = res[rank]
+        assert owners == [0, 1, 0]
+        for c, rows in enumerate(chunks):
+            if reduce == "reduce_scatter" and owners[c] != rank:
+                continue                               # another rank receives this chunk's sum
+            np.testing.assert_allclose(ys[rows], y[rows], rtol=1e-12, atol=1e-12 * np.abs(y).max())
+            np.testing.assert_allclose(dxs[rows], dx[rows], rtol=1e-12, atol=1e-12 * np.abs(dx).max())
         J = slice(rank * half, (rank + 1) * half)
         np.testing.assert_allclose(dW1r[:half], dW1[J], rtol=1e-12, atol=1e-12 * np.abs(dW1).max())
         np.testing.assert_allclose(dW1r[half:], dW1[s.H:][J], rtol=1e-12, atol=1e-12 * np.abs(dW1).max())
         np.testing.assert_allclose(dW2r, dW2[:, J], rtol=1e-12, atol=1e-12 * np.abs(dW2).max())
+    if reduce == "reduce_scatter":                      # a chunk another rank owns holds a partial sum only
+        assert np.abs(res[1][0][chunks[0]] - y[chunks[0]]).max() > 1e-3 * np.abs(y).max()
+
+
+def test_pairing_left_and_gate_of_different_ranks_is_not_the_block():
+    import sys
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+    import oracle
+    from bwd_gemm_epilogue_gb300 import workloads
+    from bwd_gemm_epilogue_gb300.workloads import Shape
+    s, x, W1, W2, dy = workloads.make_block(Shape(64, 48, 96, 40), seed=11)
+    half = s.H // 2
     # pairing a rank's left columns with another rank's gate columns is not the block
     W1_wrong = torch.cat([W1[:half], W1[s.H + half:]]).contiguous()
     _, _, y_wrong = oracle.fwd(x, W1_wrong, W2[:, :half].contiguous())
