@@ -83,6 +83,11 @@ constexpr int NUM_THREADS = 256;
 constexpr int EPI_WARP0 = 4;
 constexpr int CHUNK = 32;         // epilogue columns per TMEM load
 constexpr uint32_t TMEM_COLS = 512;
+// The fused backward's epilogue takes the saved preact and writes its outputs in chunks
+// of PRE_COLS columns: 128-byte rows, the widest a TMA box with 128-byte swizzle moves
+// (each row of a box is one memory request, so wide rows mean few requests).
+constexpr int PRE_COLS = 64;
+constexpr int NPRE = BN / PRE_COLS;
 
 // Device error word bits (one per role that gave up waiting).
 constexpr int ERR_PRODUCER = 1, ERR_MMA = 2, ERR_EPILOGUE = 4, ERR_AUX = 8;
@@ -190,20 +195,22 @@ struct Cfg {
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;             // what the leader's stage barrier waits for
-    static constexpr int NOUT = STORE_ONLY ? 1 : 3;
+    static constexpr bool BWD = EPI == EPI_SWIGLU_BWD;
+    static constexpr int NOUT = (STORE_ONLY || BWD) ? 1 : 3;
     // Store-only epilogues (64 registers) run two warps per TMEM lane quadrant, each
     // draining every other chunk, so twice the TMA stores are in flight; the SwiGLU
     // epilogues need too many registers for that and keep one warp per quadrant.
     static constexpr int EPI_WARPS = STORE_ONLY ? 8 : 4;
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
-    static constexpr int OUT_TILE = 32 * CK * 2;                  // one warp's 32 x CK bf16 tile
-    static constexpr int OUT_BUFS =
-        (EPI == EPI_SWIGLU_BWD || (EPI == EPI_SWIGLU_FWD && CG == 1)) ? 1 : 2;
+    // one warp's 32-row bf16 staging tile of CK columns; the fused backward's warps each own
+    // one slot of two 32 x PRE_COLS tiles that first receive their preact chunk (left, gate)
+    // and then stage its outputs (dleft, dgate, then h in the first tile)
+    static constexpr int OUT_TILE = 32 * (BWD ? PRE_COLS : CK) * 2;
+    static constexpr int OUT_BUFS = (BWD || !(EPI == EPI_SWIGLU_FWD && CG == 1)) ? 2 : 1;
     static constexpr int OUT_WARP_BYTES = OUT_BUFS * NOUT * OUT_TILE;
-    // epilogue-input slots: preact left + gate (SWIGLU_BWD) or the residual (STORE_ADD)
-    static constexpr int EIN_SLOTS = (EPI == EPI_SWIGLU_BWD || EPI == EPI_STORE_ADD) ? 2 : 0;
-    static constexpr int EIN_HALF = BM * CK * 2;                  // 128 rows x CK cols bf16
-    static constexpr int EIN_SLOT_BYTES = (EPI == EPI_SWIGLU_BWD ? 2 : 1) * EIN_HALF;
+    // epilogue-input slots of the residual (STORE_ADD): 128 rows x CK cols bf16
+    static constexpr int EIN_SLOTS = EPI == EPI_STORE_ADD ? 2 : 0;
+    static constexpr int EIN_SLOT_BYTES = BM * CK * 2;
     static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CK : BN / CK;
 
     static constexpr int OFF_A = 0;
@@ -211,8 +218,9 @@ struct Cfg {
     static constexpr int OFF_EIN = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_OUT = OFF_EIN + EIN_SLOTS * EIN_SLOT_BYTES;
     static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_WARP_BYTES;
-    // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], ein_full[E], ein_empty[E], drain
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EIN_SLOTS + 1;
+    // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], ein_full[E], ein_empty[E], drain,
+    // and the fused backward's per-warp preact slots: slot_full[4]
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EIN_SLOTS + 1 + (BWD ? 4 : 0);
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;       // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;           // slack to align the base
@@ -451,7 +459,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
     auto ein_full_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 4 + s); };
     auto ein_empty_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 4 + C::EIN_SLOTS + s); };
-    const uint32_t drain_bar = bar0 + 8u * (C::NUM_BARS - 1);
+    const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4 + 2 * C::EIN_SLOTS);
+    auto slot_full_bar = [&](int w) { return drain_bar + 8u * (1 + w); };   // fused backward, epilogue warp w
     volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + C::OFF_MISC + 4);
 
@@ -469,6 +478,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             ptx::mbar_init(ein_empty_bar(s), 4);
         }
         ptx::mbar_init(drain_bar, 1);
+        if (C::BWD)
+            for (int w = 0; w < 4; ++w) ptx::mbar_init(slot_full_bar(w), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         if constexpr (!is_table(SCHED)) {
@@ -689,46 +700,6 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ epilogue-input producer
-        if (EPI == EPI_SWIGLU_BWD && lane == 0) {
-            int slot = 0;
-            uint32_t phase = 0;
-            int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
-            for (int s = 0; s < C::EIN_SLOTS; ++s) last_parity[s] = -1;
-            bool ok = true;
-            int seen_pi = -1;
-            for (int it = t_first; it < t_end && ok; it += t_step) {
-                int pi, lt, tm, tn;
-                const Problem pr0 = problem_at<SCHED>(args, it, pi, lt);
-                tile_coords(pr0, lt, tm, tn);
-                const CUtensorMap* mI = map_of<SCHED, MAP_I0>(args, pi);
-                if (is_table(SCHED) && pi != seen_pi) {
-                    ptx::tmap_acquire(mI);
-                    seen_pi = pi;
-                }
-                const int m0 = tm * (BM * CG) + BM * (int)rank;
-                const int j0 = tn * BN;
-                for (int c = 0; c < C::CHUNKS; ++c) {
-                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, tmo, err, abort_flag, ERR_AUX)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = ein_full_bar(slot);
-                    ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
-                    last_parity[slot] = (int)phase;
-                    const uint32_t dst = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
-                    ptx::tma_load_3d(dst, mI, fb, j0 + c * C::CK, 0, m0);
-                    ptx::tma_load_3d(dst + C::EIN_HALF, mI, fb, j0 + c * C::CK, 1, m0);
-                    if (++slot == C::EIN_SLOTS) {
-                        slot = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                for (int s = 0; s < C::EIN_SLOTS; ++s)
-                    if (last_parity[s] >= 0) drain_wait(ein_full_bar(s), (uint32_t)last_parity[s], tmo);
-            }
-        }
         if (EPI == EPI_STORE_ADD && lane == 0) {
             // the residual [M, N] tiles of the problems that carry one, 128 rows x 32 columns
             // per chunk, in the order the epilogue warps consume them
@@ -772,6 +743,165 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             }
         }
         __syncwarp();
+    } else if (warp >= EPI_WARP0 && C::BWD) {
+        // ------------------------------------------------------------ fused backward epilogue
+        // Each warp drains its 32 accumulator rows in chunks of PRE_COLS columns through its
+        // own slot of shared memory: lane 0 TMA-loads the chunk's saved preact (left into
+        // the first tile, gate into the second, 128-byte rows); every lane copies its row to
+        // registers; the warp computes dleft, dgate and h from the accumulator, writes dleft
+        // and dgate over the preact it no longer needs and stores them, then h into the
+        // first tile once dleft's store has read it; once h's store has read the slot, the
+        // next chunk's preact is loaded into it (the next tile's first chunk after the last).
+        const int wq = warp & 3;                 // TMEM lane quadrant = tile rows [32wq, 32wq+32)
+        const int wi = warp - EPI_WARP0;
+        const uint32_t slot = base + C::OFF_OUT + wi * C::OUT_WARP_BYTES;
+        const uint32_t slot_g = slot + C::OUT_TILE;
+        const uint32_t sbar = slot_full_bar(wi);
+        const uint32_t srow = (uint32_t)lane * 128u;   // this lane's row in a slot tile
+        uint32_t spar = 0;         // parity of the slot barrier's next phase
+        bool pending = false;      // a preact load is in flight into the slot
+        auto load_chunk = [&](const CUtensorMap* mI, int j, int mrow) {
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(sbar, 2 * C::OUT_TILE);
+                ptx::tma_load_3d(slot, mI, sbar, j, 0, mrow);     // left
+                ptx::tma_load_3d(slot_g, mI, sbar, j, 1, mrow);   // gate
+            }
+            pending = true;
+        };
+        int local = 0;
+        bool ok = true;
+        int seen_pi = -1;
+        for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
+            int pi, lt;
+            const Problem pr = problem_at<SCHED>(args, it, pi, lt);
+            const CUtensorMap* mO0 = map_of<SCHED, MAP_O0>(args, pi);
+            const CUtensorMap* mO1 = map_of<SCHED, MAP_O1>(args, pi);
+            const CUtensorMap* mI = map_of<SCHED, MAP_I0>(args, pi);
+            if (is_table(SCHED) && pi != seen_pi && lane == 0) {
+                ptx::tmap_acquire(mO0);
+                ptx::tmap_acquire(mO1);
+                ptx::tmap_acquire(mI);
+            }
+            seen_pi = pi;
+            int tm, tn;
+            tile_coords(pr, lt, tm, tn);
+            const int mrow0 = tm * (BM * CG) + BM * (int)rank + 32 * wq;   // first row of this warp
+            const bool rows_live = mrow0 < pr.M;
+            if (!pending) load_chunk(mI, tn * BN, mrow0);   // (later tiles: loaded during the last)
+            const int ab = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, tmo, err, abort_flag,
+                                                                  ERR_EPILOGUE));
+            if (!got) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
+            for (int q = 0; q < NPRE; ++q) {
+                const bool in_ok = __all_sync(0xffffffffu, wait_bounded(sbar, spar, tmo, err, abort_flag, ERR_EPILOGUE));
+                if (!in_ok) {
+                    ok = false;
+                    break;
+                }
+                spar ^= 1u;
+                pending = false;
+                // this row's 64 left and 64 gate values (128-byte swizzle)
+                uint32_t lft[32], gte[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t off = srow + (uint32_t)((u ^ (lane & 7)) << 4);
+                    const uint4 l4 = ptx::lds128(slot + off);
+                    const uint4 g4 = ptx::lds128(slot_g + off);
+                    lft[4 * u + 0] = l4.x; lft[4 * u + 1] = l4.y; lft[4 * u + 2] = l4.z; lft[4 * u + 3] = l4.w;
+                    gte[4 * u + 0] = g4.x; gte[4 * u + 1] = g4.y; gte[4 * u + 2] = g4.z; gte[4 * u + 3] = g4.w;
+                }
+                uint32_t hb[32];   // h of the chunk, packed bf16 pairs, staged after dleft's store
+#pragma unroll
+                for (int i = 0; i < PRE_COLS / C::CK; ++i) {
+                    uint32_t acc[16];
+                    ptx::tmem_ld_32x32b_x16(t_row + q * PRE_COLS + i * C::CK, acc);
+                    ptx::tmem_ld_wait();
+                    if (q == NPRE - 1 && i == PRE_COLS / C::CK - 1) {
+                        // accumulator fully read: hand it back to the MMA warp (of the leader CTA)
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(ab), 0));
+                            else ptx::mbar_arrive(tempty_bar(ab));
+                        }
+                    }
+                    uint32_t dl[8], dg[8];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const uint32_t lw = lft[8 * i + w], gw = gte[8 * i + w];
+                        float dlv[2], dgv[2], hv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float gh = __uint_as_float(acc[2 * w + e]);
+                            const float l = e ? bf16_hi(lw) : bf16_lo(lw);
+                            const float g = e ? bf16_hi(gw) : bf16_lo(gw);
+                            const float sig = sigmoid_mufu(g);
+                            const float silu = g * sig;
+                            const float silu_p = sig + silu * (1.0f - sig);
+                            dlv[e] = gh * silu;
+                            dgv[e] = gh * l * silu_p;
+                            hv[e] = l * round_bf16(silu);
+                        }
+                        dl[w] = pack_bf16(dlv[0], dlv[1]);
+                        dg[w] = pack_bf16(dgv[0], dgv[1]);
+                        hb[8 * i + w] = pack_bf16(hv[0], hv[1]);
+                    }
+                    // dleft and dgate over this lane's own (already copied) preact row
+                    const uint32_t u0 = srow + (uint32_t)(((2 * i) ^ (lane & 7)) << 4);
+                    const uint32_t u1 = srow + (uint32_t)(((2 * i + 1) ^ (lane & 7)) << 4);
+                    ptx::sts128(slot + u0, make_uint4(dl[0], dl[1], dl[2], dl[3]));
+                    ptx::sts128(slot + u1, make_uint4(dl[4], dl[5], dl[6], dl[7]));
+                    ptx::sts128(slot_g + u0, make_uint4(dg[0], dg[1], dg[2], dg[3]));
+                    ptx::sts128(slot_g + u1, make_uint4(dg[4], dg[5], dg[6], dg[7]));
+                }
+                const int j = tn * BN + q * PRE_COLS;
+                const bool live = rows_live && j < pr.N;
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (live) ptx::tma_store_3d(mO0, slot, j, 0, mrow0);     // dleft
+                    ptx::bulk_commit_group();
+                    if (live) ptx::tma_store_3d(mO0, slot_g, j, 1, mrow0);   // dgate
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_group_read<1>();                         // dleft's tile read
+                }
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    ptx::sts128(slot + srow + (uint32_t)((u ^ (lane & 7)) << 4),
+                                make_uint4(hb[4 * u], hb[4 * u + 1], hb[4 * u + 2], hb[4 * u + 3]));
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (live) ptx::tma_store_2d(mO1, slot, j, mrow0);        // h
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_group_read<0>();                         // the slot is free
+                }
+                __syncwarp();
+                // the next chunk's preact into the slot: this tile's next, or the next tile's first
+                if (q + 1 < NPRE) {
+                    load_chunk(mI, j + PRE_COLS, mrow0);
+                } else if (it + t_step < t_end) {
+                    int pn, ln, tmn, tnn;
+                    const Problem pnx = problem_at<SCHED>(args, it + t_step, pn, ln);
+                    tile_coords(pnx, ln, tmn, tnn);
+                    const CUtensorMap* mIn = map_of<SCHED, MAP_I0>(args, pn);
+                    if (is_table(SCHED) && pn != seen_pi && lane == 0) ptx::tmap_acquire(mIn);
+                    load_chunk(mIn, tnn * BN, tmn * (BM * CG) + BM * (int)rank + 32 * wq);
+                }
+            }
+        }
+        // let a preact load still in flight land before the shared memory goes away
+        if (pending) drain_wait(sbar, spar, tmo);
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        ptx::tc_fence_before();
+        __syncwarp();
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue
         const int wq = warp & 3;                 // TMEM lane quadrant = tile rows [32wq, 32wq+32)
@@ -779,8 +909,6 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         const int grp = (warp - EPI_WARP0) >> 2; // which of the quadrant's warps (store-only: 0 or 1)
         constexpr int GROUPS = C::EPI_WARPS / 4;
         const uint32_t out_base = base + C::OFF_OUT + (warp - EPI_WARP0) * C::OUT_WARP_BYTES;
-        int ein_slot = 0;
-        uint32_t ein_phase = 0;
         int res_tiles = 0;   // EPI_STORE_ADD: residual tiles drained so far (slot bookkeeping)
         int ob = 0;
         int local = 0;
@@ -821,8 +949,6 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 if (EPI == EPI_SWIGLU_FWD) {
                     ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
                     ptx::tmem_ld_32x32b_x32(t_row + BN / 2 + c * CHUNK, acc2);
-                } else if (C::CK == 16) {
-                    ptx::tmem_ld_32x32b_x16(t_row + c * C::CK, *reinterpret_cast<uint32_t(*)[16]>(acc));
                 } else {
                     ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
                 }
@@ -837,9 +963,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     }
                 }
 
-                // epilogue inputs (backward): the saved preact left/gate for these 32 columns;
-                // (residual store) the residual's 32 columns
-                uint32_t lft[16], gte[16];
+                // epilogue input of the residual store: the residual's 32 columns
+                uint32_t lft[16];
                 if (EPI == EPI_STORE_ADD && pr.res) {
                     constexpr int NSLOT = C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1;
                     const int q = res_tiles * C::CHUNKS + c;
@@ -860,29 +985,6 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(ein_empty_bar(slot));
                 }
-                if (EPI == EPI_SWIGLU_BWD) {
-                    const bool in_ok = __all_sync(
-                        0xffffffffu, wait_bounded(ein_full_bar(ein_slot), ein_phase, tmo, err, abort_flag, ERR_EPILOGUE));
-                    if (!in_ok) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t slot_base = base + C::OFF_EIN + ein_slot * C::EIN_SLOT_BYTES;
-#pragma unroll
-                    for (int q = 0; q < C::CK / 8; ++q) {
-                        const uint4 l4 = ptx::lds128(slot_base + stage_offset<C::CK>(row, q));
-                        const uint4 g4 = ptx::lds128(slot_base + C::EIN_HALF + stage_offset<C::CK>(row, q));
-                        lft[4 * q + 0] = l4.x; lft[4 * q + 1] = l4.y; lft[4 * q + 2] = l4.z; lft[4 * q + 3] = l4.w;
-                        gte[4 * q + 0] = g4.x; gte[4 * q + 1] = g4.y; gte[4 * q + 2] = g4.z; gte[4 * q + 3] = g4.w;
-                    }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ein_empty_bar(ein_slot));
-                    if (++ein_slot == C::EIN_SLOTS) {
-                        ein_slot = 0;
-                        ein_phase ^= 1u;
-                    }
-                }
-
                 // outputs for this chunk, packed bf16 pairs (the FP8 forward's h: 4 codes a word)
                 uint32_t o0[16], o1[16], o2[16];
                 if (OP == OP_E4M3) {
@@ -929,26 +1031,6 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         } else {
                             o2[i] = pack_bf16(hv[0], hv[1]);
                         }
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < C::CK / 2; ++i) {
-                        float dl[2], dg[2], hv[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const float gh = __uint_as_float(acc[2 * i + e]);
-                            const float l = e ? bf16_hi(lft[i]) : bf16_lo(lft[i]);
-                            const float g = e ? bf16_hi(gte[i]) : bf16_lo(gte[i]);
-                            const float sig = sigmoid_mufu(g);
-                            const float silu = g * sig;
-                            const float silu_p = sig + silu * (1.0f - sig);
-                            dl[e] = gh * silu;
-                            dg[e] = gh * l * silu_p;
-                            hv[e] = l * round_bf16(silu);
-                        }
-                        o0[i] = pack_bf16(dl[0], dl[1]);
-                        o1[i] = pack_bf16(dg[0], dg[1]);
-                        o2[i] = pack_bf16(hv[0], hv[1]);
                     }
                 }
 

@@ -145,9 +145,9 @@ bool encode_operand(CUtensorMap* m, const void* ptr, int64_t mn, int64_t k, bool
 }
 
 // Epilogue tiles are `box_cols` bf16 wide: 32 columns (64-byte rows, 64-byte swizzle) or
-// the fused backward's 16 (32-byte rows, 32-byte swizzle).
+// the fused backward's PRE_COLS = 64 (128-byte rows, 128-byte swizzle).
 CUtensorMapSwizzle epi_swizzle(uint32_t box_cols) {
-    return box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+    return box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
 }
 
 // [M, 2H] tensor seen as (j, half, m): element (j, half, m) = base[m*2H + half*H + j].
@@ -541,11 +541,10 @@ swiglu_status run_fused_bwd(DeviceState* st, const void* dy, const void* W2, con
     // B(n = j, k = o) = W2[o, j]: MN-major
     bool b3d = false;
     if (!encode_operand(&a.b[0], W2, H, Dout, true, BN / cg, &b3d)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (b)");
-    constexpr uint32_t ck = Cfg<EPI_SWIGLU_BWD, 2>::CK;
-    static_assert(ck == Cfg<EPI_SWIGLU_BWD, 1>::CK, "one chunk width for both tile sizes");
-    if (!encode_paired(&a.o0[0], grad_preact, M, H, 32, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
-    if (!encode_out_2d(&a.o1, h, M, H, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
-    if (!encode_paired(&a.i0, preact, M, H, BM, ck)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
+    // each epilogue warp moves 32 rows x PRE_COLS columns (128-byte rows) of preact and outputs
+    if (!encode_paired(&a.o0[0], grad_preact, M, H, 32, PRE_COLS)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o0)");
+    if (!encode_out_2d(&a.o1, h, M, H, PRE_COLS)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (o1)");
+    if (!encode_paired(&a.i0, preact, M, H, 32, PRE_COLS)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (i0)");
     a.num_problems = 1;
     a.prob[0] = make_problem(M, H, Dout, (H + BN - 1) / BN, false, true, cg);
     a.prob[0].b3d = b3d ? 1 : 0;
@@ -1451,10 +1450,9 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
         bool b3d = false;
         bool ok = encode_operand(&t.a, at_row<uint8_t>(dy, off[e], Dout), m, Dout, false, BM);
         ok = ok && encode_operand(&t.b, at_row<uint8_t>(W2, e * Dout, H), H, Dout, true, BN / cg, &b3d);
-        constexpr uint32_t ck = Cfg<EPI_SWIGLU_BWD, 2>::CK;
-        ok = ok && encode_paired(&t.o0, at_row<uint8_t>(gp, off[e], 2 * H), m, H, 32, ck);
-        ok = ok && encode_out_2d(&t.o1, at_row<uint8_t>(h, off[e], H), m, H, ck);
-        ok = ok && encode_paired(&t.i0, at_row<uint8_t>(preact, off[e], 2 * H), m, H, BM, ck);
+        ok = ok && encode_paired(&t.o0, at_row<uint8_t>(gp, off[e], 2 * H), m, H, 32, PRE_COLS);
+        ok = ok && encode_out_2d(&t.o1, at_row<uint8_t>(h, off[e], H), m, H, PRE_COLS);
+        ok = ok && encode_paired(&t.i0, at_row<uint8_t>(preact, off[e], 2 * H), m, H, 32, PRE_COLS);
         if (!ok) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe grad_h)");
         t.prob = make_problem(m, H, Dout, (H + BN - 1) / BN, false, true, cg);
         t.prob.b3d = b3d ? 1 : 0;
