@@ -1,13 +1,14 @@
-"""Turn an ncu CSV of DRAM counters into profiles/traffic.json for bench.py.
+"""Turn ncu CSVs of DRAM counters into profiles/traffic.json for bench.py.
 
-    python -m bwd_gemm_epilogue_gb300.traffic_summary dram.csv "<the ncu command>"
+    python -m bwd_gemm_epilogue_gb300.traffic_summary "<how the CSVs were taken>" a.csv [b.csv ...]
 
-The CSV comes from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,
-gpu__time_duration.sum --csv --log-file dram.csv python bench.py ...` over launches of
-the target step.  Launches are mapped to kernel kinds by their template arguments
-(gemm_kernel<EPI, CG, SCHED, OP>, bf16 operands), averaged per kind, and written with a hash of the
-kernel sources: bench.py reports a kind's traffic only while the sources still hash
-the same (a changed kernel invalidates its counters).
+Each CSV comes from one ncu capture of `--metrics dram__bytes_read.sum,
+dram__bytes_write.sum,gpu__time_duration.sum` (one pass) on one or more launches of the
+target block's kernels.  Launches are mapped to kernel kinds by their template arguments
+(gemm_kernel<EPI, CG, SCHED, OP>, bf16 operands; plain or demangled kernel names),
+averaged per kind, and written with a hash of the kernel sources: bench.py reports a
+kind's traffic only while the sources still hash the same (a changed kernel invalidates
+its counters).
 """
 from __future__ import annotations
 
@@ -36,7 +37,8 @@ def summarize(path: str) -> dict:
     for r in rows[hi + 1:]:
         if len(r) <= vi:
             continue
-        m = re.search(r"gemm_kernel<(\d+), (\d+), (\d+)(?:, (\d+))?>", r[ki])
+        m = re.search(r"gemm_kernel<(?:\(int\))?(\d+), (?:\(int\))?(\d+), (?:\(int\))?(\d+)(?:, (?:\(int\))?(\d+))?>",
+                      r[ki])
         if not m or m.group(4) not in (None, "0") or m.groups()[:3] not in KINDS:
             continue
         d = per_launch.setdefault(r[ii], {"kind": KINDS[m.groups()[:3]]})
@@ -56,9 +58,12 @@ def summarize(path: str) -> dict:
 
 def main():
     import bench
-    path, command = sys.argv[1], sys.argv[2]
+    command, paths = sys.argv[1], sys.argv[2:]
+    kernels = {}
+    for path in paths:
+        kernels.update(summarize(path))
     out = {"source_hash": bench.kernel_source_hash(), "command": command,
-           "workload": "target step: M=11136, D=Dout=3584, H=14336", "kernels": summarize(path)}
+           "workload": "target step: M=11136, D=Dout=3584, H=14336", "kernels": kernels}
     dst = os.path.join(ROOT, "profiles", "traffic.json")
     json.dump(out, open(dst, "w"), indent=1)
     print(json.dumps(out, indent=1))
