@@ -60,7 +60,7 @@ def parse():
                     help="time the residual block y = x + MLP(x) (residual-add epilogues; D == Dout)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=25.0, help="CPU time the oracle sample is sized for (it tends to finish in about 60 %% of it)")
     return ap.parse_args()
 
 
@@ -155,18 +155,20 @@ def oracle_sample(s, x, W1, W2, dy, preact, n_rows: int, n_cols: int, seed: int 
 
 
 def cpu_baseline(s, x, W1, W2, dy, preact, seconds: float):
-    """Size a sample to about `seconds` of CPU time from a one-row calibration, then time it."""
-    dt1, f1, _ = oracle_sample(s, x, W1, W2, dy, preact, 2, 0, seed=99)
-    rate = f1 / max(dt1, 1e-6)
-    per_row = f1 / 2
-    per_col = 2 * s.M * s.Dout * 2 + 2 * 2 * s.M * s.D
-    budget = rate * seconds
-    n_cols = max(1, int(0.25 * budget / per_col))
-    n_rows = max(1, int((budget - n_cols * per_col) / per_row))
-    dt, flops, threads = oracle_sample(s, x, W1, W2, dy, preact, n_rows, n_cols)
+    """Size a sample to about `seconds` of CPU time (three quarters token rows, one quarter
+    hidden columns) from a calibration on as many rows and columns as the oracle has
+    threads (it runs rows, or columns, in parallel), then time it."""
+    import oracle
+    nt = max(1, oracle.num_threads())
+    dt_r, f_r, _ = oracle_sample(s, x, W1, W2, dy, preact, nt, 0, seed=99)
+    dt_c, f_c, _ = oracle_sample(s, x, W1, W2, dy, preact, 0, nt, seed=98)
+    n_rows = max(1, int(0.75 * seconds / max(dt_r / nt, 1e-6)))
+    n_cols = max(1, int(0.25 * seconds / max(dt_c / nt, 1e-6)))
+    dt, flops, threads = oracle_sample(s, x, W1, W2, dy, preact, min(n_rows, s.M), min(n_cols, s.H))
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"fwd + row-wise bwd for {n_rows} of {s.M} token rows and weight grads for {n_cols} "
-                      f"of {s.H} hidden columns of the target block ({flops / 1e9:.1f} GFLOP in {dt:.1f} s, fp64)"}
+            "sample": f"fwd + row-wise bwd for {min(n_rows, s.M)} of {s.M} token rows and weight grads for "
+                      f"{min(n_cols, s.H)} of {s.H} hidden columns of the target block ({flops / 1e9:.1f} GFLOP in "
+                      f"{dt:.1f} s, fp64)"}
 
 
 # ----------------------------------------------------------------------------- profile summary
