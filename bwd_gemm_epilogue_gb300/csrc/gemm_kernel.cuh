@@ -12,10 +12,10 @@
 //
 //   warp 0      TMA producer: A/B k-blocks into a STAGES-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma into one of two TMEM
-//               accumulators (2 x 256 fp32 columns = all 512 TMEM columns)
-//   warp 2      epilogue-input producer (SWIGLU_BWD and STORE_ADD): TMA-prefetches
-//               the saved preact left/gate sub-tiles, or the residual tiles, that
-//               the epilogue consumes
+//               accumulators (2 x 256 fp32 columns = all 512 TMEM columns), or into
+//               both for one 256 x 512 tile (EPI_STORE_W)
+//   warp 2      epilogue-input producer (STORE_ADD): TMA-prefetches the residual
+//               tiles that the epilogue consumes
 //   warp 3      idle
 //   warps 4..   epilogue (4 warps; 8 for the store-only epilogues, two per quadrant):
 //               TMEM -> registers (lane quadrant = warp % 4), the epilogue math,
@@ -32,6 +32,12 @@
 //
 // Epilogues:
 //   EPI_STORE       C = acc rounded to bf16.
+//   EPI_STORE_W     the same epilogue over 256 x 512 tiles (CTA pairs): both TMEM
+//                   accumulators hold one tile, each A k-block feeds two N = 256 MMAs,
+//                   so a k-block's operands carry 3/4 of the bytes per FLOP of a
+//                   256 x 256 tile.  The accumulators form a ring of two 256-column
+//                   slots: a tile takes two slots (one at a ragged N edge), the epilogue
+//                   drains and returns them one at a time.
 //   EPI_SWIGLU_FWD  B holds two W1 row slabs, [j0, j0+128) and [H+j0, H+j0+128), so
 //                   accumulator columns [0,128) are `left` and [128,256) the matching
 //                   `gate`.  Stores preact (both halves, bf16) and
@@ -41,10 +47,11 @@
 //                   "Transformer MLP, GEMM and operator fusion" lesson, section 24: the down
 //                   projection adds the block input; the backward's dx adds dy).
 //   EPI_SWIGLU_BWD  acc = grad_h[m0:, j0:j0+256] (dy @ W2), never written out.  With the
-//                   prefetched left/gate: dleft = grad_h * silu(gate),
+//                   saved left/gate (each epilogue warp TMA-loads its own 32 x 64 chunks
+//                   into its own slot): dleft = grad_h * silu(gate),
 //                   dgate = grad_h * left * silu'(gate), silu' = sigma + silu*(1 - sigma),
 //                   h = bf16(left * bf16(silu(gate))); stores grad_preact = [dleft|dgate]
-//                   and h, draining 16-column chunks.
+//                   and h through the same slot, in 64-column tiles.
 // With FP8 operands (OP_E4M3, the quantised GEMM epilogue of the lesson above, section
 // 26) the epilogue first multiplies the accumulator by the operands' scale product, and
 // the SwiGLU forward stores h quantised to E4M3, sat8(round(h / s_h)).
@@ -68,7 +75,7 @@
 
 namespace swiglu {
 
-enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_STORE_ADD = 3 };
+enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_STORE_ADD = 3, EPI_STORE_W = 4 };
 
 // Operand type of the MMAs: bf16 (kind::f16) or FP8 E4M3 (kind::f8f6f4).  Both fill a
 // 128-byte swizzle row per k-block -- 64 bf16 or 128 FP8 values -- so the stage
@@ -179,22 +186,26 @@ struct TableArgs {
 template <int EPI, int CG>
 struct Cfg {
     // Mainloop depth is what these kernels are most sensitive to, so the epilogue
-    // buffers get what is left (CTA-pair SWIGLU_BWD: 5 stages, 2 preact slots and
-    // single-buffered output tiles measured 7% faster than 4 / 3 / 2; single-CTA
-    // SWIGLU_FWD: 4 stages and single-buffered outputs 11% faster than 3 / 2).
-    // The fused backward drains 16-column chunks (x16 TMEM loads, 32-byte staging rows):
-    // its preact slots and output tiles then take half the space, which buys a sixth
-    // operand stage for CTA pairs (a fourth for single CTAs).
+    // buffers get what is left (single-CTA SWIGLU_FWD: 4 stages and single-buffered
+    // outputs measured 11% faster than 3 / 2).  The fused backward reads its accumulator
+    // 16 columns at a time (x16 TMEM loads) and moves preact and its outputs through one
+    // 8 KB slot per epilogue warp, which leaves room for six operand stages (CTA pairs).
     static constexpr int CK = EPI == EPI_SWIGLU_BWD ? 16 : CHUNK;   // epilogue columns per chunk
+    // 256 x 512 tiles (EPI_STORE_W): two 256-column accumulator slots per tile
+    static constexpr bool WIDE = EPI == EPI_STORE_W;
+    static_assert(!WIDE || CG == 2, "256 x 512 tiles are CTA-pair tiles");
+    static constexpr int SLOTS = WIDE ? 2 : 1;
+    static constexpr int TILE_N = SLOTS * BN;                     // output columns per tile
     static constexpr int STAGES =
-        CG == 1 ? ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) ? 4 : 3)
-                : ((EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD) ? 6 : 5);
-    static constexpr bool STORE_ONLY = EPI == EPI_STORE || EPI == EPI_STORE_ADD;   // one bf16 output
+        WIDE ? 4
+             : CG == 1 ? ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) ? 4 : 3)
+                       : ((EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD) ? 6 : 5);
+    static constexpr bool STORE_ONLY = EPI == EPI_STORE || EPI == EPI_STORE_ADD || WIDE;   // one bf16 output
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_ROWS = BN / CG;                        // B rows (N) held by this CTA
-    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int B_ROWS = BN / CG;                        // B rows (N) per slot held by this CTA
+    static constexpr int B_SLOT_BYTES = B_ROWS * BK * 2;
+    static constexpr int B_BYTES = SLOTS * B_SLOT_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TX_BYTES = STAGE_BYTES * CG;             // what the leader's stage barrier waits for
     static constexpr bool BWD = EPI == EPI_SWIGLU_BWD;
     static constexpr int NOUT = (STORE_ONLY || BWD) ? 1 : 3;
     // Store-only epilogues (64 registers) run two warps per TMEM lane quadrant, each
@@ -269,6 +280,14 @@ __device__ __forceinline__ void tile_coords(const Problem& p, int t, int& tm, in
     const int w = min(p.band, p.tiles_n - n0);
     tm = r / w;
     tn = n0 + (r - tm * w);
+}
+
+// Accumulator slots (256 columns each) of the tile in column-tile tn: two for a 256 x 512
+// tile unless its second half lies wholly past N.
+template <class C>
+__device__ __forceinline__ int tile_slots(const Problem& p, int tn) {
+    if constexpr (C::WIDE) return tn * C::TILE_N + BN < p.N ? 2 : 1;
+    else return 1;
 }
 
 // Which problem a launch-wide tile index belongs to.
@@ -434,6 +453,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     using C = Cfg<EPI, CG>;
     static_assert(OP == OP_BF16 || ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) && SCHED == SRC_SINGLE),
                   "FP8 operands: forward kernels, one problem per launch");
+    static_assert(!C::WIDE || !is_table(SCHED), "256 x 512 tiles: parameter-block launches");
     constexpr int BKE = OP == OP_E4M3 ? 2 * BK : BK;   // k values per 128-byte k-block
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -537,6 +557,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     int tm, tn;
                     tile_coords(p, lt, tm, tn);
                     const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
+                    const int w = tile_slots<C>(p, tn);
+                    const uint32_t tx = (uint32_t)((C::A_BYTES + w * C::B_SLOT_BYTES) * CG);
                     for (int kb = 0; kb < k_blocks; ++kb) {
                         if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
                             ok = false;
@@ -545,7 +567,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         const uint32_t fb_local = full_bar(stage);
                         // CG == 2: both CTAs' copies complete on the leader's stage barrier.
                         const uint32_t fb = CG == 2 ? full_bar_leader + 8u * stage : fb_local;
-                        if (leader) ptx::mbar_arrive_expect_tx(fb_local, C::TX_BYTES);
+                        if (leader) ptx::mbar_arrive_expect_tx(fb_local, tx);
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         const int k0 = kb * BKE;
@@ -578,16 +600,20 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                                 ptx::tma_load_3d(sB, mb, fb, k0, j0, 0);
                                 ptx::tma_load_3d(sB + C::B_BYTES / 2, mb, fb, k0, j0, 1);
                             }
-                        } else if (b_mn) {
-                            const int n0 = tn * BN + C::B_ROWS * (int)rank;
-                            if (b3d) {
-                                load3(sB, mb, k0, n0 >> 6);   // all 64-row blocks in one copy
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sB + i * 8192, mb, n0 + 64 * i, k0);
-                            }
                         } else {
-                            load2(sB, mb, k0, tn * BN + C::B_ROWS * (int)rank);
+                            // slot j of the tile: B rows [n0 + j * BN, + BN), this CTA's B_ROWS of them
+                            for (int j = 0; j < w; ++j) {
+                                const int n0 = tn * C::TILE_N + j * BN + C::B_ROWS * (int)rank;
+                                const uint32_t sBj = sB + j * C::B_SLOT_BYTES;
+                                if (!b_mn) {
+                                    load2(sBj, mb, k0, n0);
+                                } else if (b3d) {
+                                    load3(sBj, mb, k0, n0 >> 6);   // all 64-row blocks in one copy
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < C::B_ROWS / 64; ++i) load2(sBj + i * 8192, mb, n0 + 64 * i, k0);
+                                }
+                            }
                         }
                         if (++stage == C::STAGES) {
                             stage = 0;
@@ -634,8 +660,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int local = 0;
-            for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
+            uint32_t slot_seq = 0;   // accumulator slots taken so far (slot slot_seq & 1 is next)
+            for (int it = t_first; it < t_end && ok; it += t_step) {
                 int pi, lt;
                 const Problem pq = problem_at<SCHED>(args, it, pi, lt);
                 const int k_blocks = pq.k_blocks;
@@ -651,14 +677,22 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                                               : umma_desc_sw128(base + C::OFF_B, 16, 1024);
                 const int a_kstep = a_mn ? (2048 >> 4) : (32 >> 4);
                 const int b_kstep = b_mn ? (2048 >> 4) : (32 >> 4);
-                const int ab = local & 1;
-                const uint32_t use = (uint32_t)(local >> 1);
-                if (!wait_bounded(tempty_bar(ab), (use & 1u) ^ 1u, tmo, err, abort_flag, ERR_MMA)) {
-                    ok = false;
-                    break;
+                int w = 1;
+                if constexpr (C::WIDE) {
+                    int tm, tn;
+                    tile_coords(pq, lt, tm, tn);
+                    w = tile_slots<C>(pq, tn);
                 }
+                // the tile's slots, drained by the epilogue (use u of slot b: its (u+1)-th tile)
+                for (int j = 0; j < w && ok; ++j) {
+                    const uint32_t s = slot_seq + (uint32_t)j;
+                    if (!wait_bounded(tempty_bar(s & 1u), ((s >> 1) & 1u) ^ 1u, tmo, err, abort_flag, ERR_MMA))
+                        ok = false;
+                }
+                if (!ok) break;
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(ab * BN);
+                const uint32_t d_tmem = tmem_base + (slot_seq & 1u) * BN;           // slot 0 of the tile
+                const uint32_t d_tmem1 = tmem_base + ((slot_seq + 1u) & 1u) * BN;   // slot 1 (wide tiles)
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, tmo, err, abort_flag, ERR_MMA)) {
                         ok = false;
@@ -678,6 +712,9 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         } else {
                             if (CG == 2) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc_flag);
                             else ptx::mma_bf16(d_tmem, ad, bd, idesc, acc_flag);
+                            if (C::WIDE && w == 2)   // the same A k-step against the second B slot
+                                ptx::mma_bf16_pair(d_tmem1, ad, bd + (uint64_t)(C::B_SLOT_BYTES >> 4), idesc,
+                                                   acc_flag);
                         }
                     }
                     if (CG == 2) ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
@@ -688,8 +725,12 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                if (CG == 2) ptx::mma_commit_pair_mc(tfull_bar(ab), 0x3);
-                else ptx::mma_commit(tfull_bar(ab));
+                for (int j = 0; j < w; ++j) {
+                    const uint32_t b = (slot_seq + (uint32_t)j) & 1u;
+                    if (CG == 2) ptx::mma_commit_pair_mc(tfull_bar(b), 0x3);
+                    else ptx::mma_commit(tfull_bar(b));
+                }
+                slot_seq += (uint32_t)w;
             }
             if (!ok) {
                 if (CG == 2) ptx::mma_commit_pair_mc(drain_bar, 0x1);
@@ -911,10 +952,10 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         const uint32_t out_base = base + C::OFF_OUT + (warp - EPI_WARP0) * C::OUT_WARP_BYTES;
         int res_tiles = 0;   // EPI_STORE_ADD: residual tiles drained so far (slot bookkeeping)
         int ob = 0;
-        int local = 0;
+        uint32_t slot_seq = 0;   // accumulator slots drained so far
         bool ok = true;
         int seen_pi = -1;
-        for (int it = t_first; it < t_end && ok; it += t_step, ++local) {
+        for (int it = t_first; it < t_end && ok; it += t_step) {
             int pi, lt;
             // registers (asm statements clobber memory)
             const Problem pr = problem_at<SCHED>(args, it, pi, lt);
@@ -931,149 +972,155 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             const int m0 = tm * (BM * CG) + BM * (int)rank;
             const int mrow0 = m0 + 32 * wq;     // first output row of this warp's slice
             const bool rows_live = mrow0 < pr.M;
-            const int ab = local & 1;
-            const uint32_t use = (uint32_t)(local >> 1);
-            // every lane observes the barrier itself (acquire), the warp agrees on the outcome
-            const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, tmo, err, abort_flag,
-                                                                  ERR_EPILOGUE));
-            if (!got) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
+            // the tile's accumulator slots, in the order the MMA warp filled them
+            const int w = tile_slots<C>(pr, tn);
+            for (int sl = 0; sl < w && ok; ++sl) {
+                const uint32_t s = slot_seq + (uint32_t)sl;
+                const int ab = (int)(s & 1u);
+                const uint32_t use = s >> 1;
+                // every lane observes the barrier itself (acquire), the warp agrees on the outcome
+                const bool got = __all_sync(0xffffffffu, wait_bounded(tfull_bar(ab), use & 1u, tmo, err, abort_flag,
+                                                                      ERR_EPILOGUE));
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
 
-            for (int c = grp; c < C::CHUNKS; c += GROUPS) {
-                uint32_t acc[32];
-                uint32_t acc2[32];
-                if (EPI == EPI_SWIGLU_FWD) {
-                    ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
-                    ptx::tmem_ld_32x32b_x32(t_row + BN / 2 + c * CHUNK, acc2);
-                } else {
-                    ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
-                }
-                ptx::tmem_ld_wait();
-                if (c + GROUPS >= C::CHUNKS) {   // this warp's last chunk of the tile
-                    // Accumulator fully read: hand it back to the MMA warp (of the leader CTA).
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(ab), 0));
-                        else ptx::mbar_arrive(tempty_bar(ab));
-                    }
-                }
-
-                // epilogue input of the residual store: the residual's 32 columns
-                uint32_t lft[16];
-                if (EPI == EPI_STORE_ADD && pr.res) {
-                    constexpr int NSLOT = C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1;
-                    const int q = res_tiles * C::CHUNKS + c;
-                    const int slot = q % NSLOT;
-                    const bool in_ok = __all_sync(0xffffffffu, wait_bounded(ein_full_bar(slot),
-                                                                            (uint32_t)((q / NSLOT) & 1), tmo,
-                                                                            err, abort_flag, ERR_EPILOGUE));
-                    if (!in_ok) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t slot_base = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint4 r4 = ptx::lds128(slot_base + sw64_offset(row, q4));
-                        lft[4 * q4 + 0] = r4.x; lft[4 * q4 + 1] = r4.y; lft[4 * q4 + 2] = r4.z; lft[4 * q4 + 3] = r4.w;
-                    }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ein_empty_bar(slot));
-                }
-                // outputs for this chunk, packed bf16 pairs (the FP8 forward's h: 4 codes a word)
-                uint32_t o0[16], o1[16], o2[16];
-                if (OP == OP_E4M3) {
-                    // FP8 operands: the accumulator carries the product of the operands' scales
-                    float sa = 1.0f;
-                    if constexpr (OP == OP_E4M3) sa = args.scale_acc;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        acc[i] = __float_as_uint(__uint_as_float(acc[i]) * sa);
-                        if (EPI == EPI_SWIGLU_FWD) acc2[i] = __float_as_uint(__uint_as_float(acc2[i]) * sa);
-                    }
-                }
-                if (EPI == EPI_STORE || (EPI == EPI_STORE_ADD && !pr.res)) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        o0[i] = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
-                } else if (EPI == EPI_STORE_ADD) {
-                    // residual add: C = acc + R, summed in fp32 and rounded once
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        o0[i] = pack_bf16(__uint_as_float(acc[2 * i]) + bf16_lo(lft[i]),
-                                          __uint_as_float(acc[2 * i + 1]) + bf16_hi(lft[i]));
-                } else if (EPI == EPI_SWIGLU_FWD) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint32_t lb = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
-                        const uint32_t gb = pack_bf16(__uint_as_float(acc2[2 * i]), __uint_as_float(acc2[2 * i + 1]));
-                        o0[i] = lb;
-                        o1[i] = gb;
-                        float hv[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const float l = e ? bf16_hi(lb) : bf16_lo(lb);
-                            const float g = e ? bf16_hi(gb) : bf16_lo(gb);
-                            const float silu = g * sigmoid_mufu(g);
-                            hv[e] = l * round_bf16(silu);
-                        }
-                        if (OP == OP_E4M3) {
-                            // the quantising epilogue: h8 = sat8(round(h / s_h)), two codes per 16 bits
-                            float so = 1.0f;
-                            if constexpr (OP == OP_E4M3) so = args.scale_out;
-                            const uint32_t q2 = ptx::cvt_e4m3x2(hv[0] * so, hv[1] * so);
-                            o2[i >> 1] = (i & 1) ? (o2[i >> 1] | (q2 << 16)) : q2;
-                        } else {
-                            o2[i] = pack_bf16(hv[0], hv[1]);
-                        }
-                    }
-                }
-
-                // stage in shared memory (64-byte swizzle) and TMA-store this warp's 32x32 tiles
-                if (lane == 0) ptx::bulk_wait_group_read<C::OUT_BUFS - 1>();
-                __syncwarp();
-                const uint32_t ob_base = out_base + ob * (C::NOUT * C::OUT_TILE);
-#pragma unroll
-                for (int o = 0; o < C::NOUT; ++o) {
-                    const uint32_t* src = (o == 0) ? o0 : (o == 1) ? o1 : o2;
-                    const uint32_t tile = ob_base + o * C::OUT_TILE;
-                    if (OP == OP_E4M3 && o == 2) {
-                        // the FP8 h tile: 32 rows of 32 bytes, unswizzled
-                        ptx::sts128(tile + lane * 32, make_uint4(src[0], src[1], src[2], src[3]));
-                        ptx::sts128(tile + lane * 32 + 16, make_uint4(src[4], src[5], src[6], src[7]));
-                        continue;
-                    }
-#pragma unroll
-                    for (int q = 0; q < C::CK / 8; ++q)
-                        ptx::sts128(tile + stage_offset<C::CK>(lane, q),
-                                    make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]));
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && rows_live) {
-                    if (C::STORE_ONLY) {
-                        const int n = tn * BN + c * CHUNK;
-                        if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
+                for (int c = grp; c < C::CHUNKS; c += GROUPS) {
+                    uint32_t acc[32];
+                    uint32_t acc2[32];
+                    if (EPI == EPI_SWIGLU_FWD) {
+                        ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
+                        ptx::tmem_ld_32x32b_x32(t_row + BN / 2 + c * CHUNK, acc2);
                     } else {
-                        const int jw = (EPI == EPI_SWIGLU_FWD) ? BN / 2 : BN;
-                        const int j = tn * jw + c * C::CK;
-                        if (j < n_limit) {
-                            if (!pr.no_o0) {
-                                ptx::tma_store_3d(mO0, ob_base, j, 0, mrow0);
-                                ptx::tma_store_3d(mO0, ob_base + C::OUT_TILE, j, 1, mrow0);
-                            }
-                            ptx::tma_store_2d(mO1, ob_base + 2 * C::OUT_TILE, j, mrow0);
+                        ptx::tmem_ld_32x32b_x32(t_row + c * CHUNK, acc);
+                    }
+                    ptx::tmem_ld_wait();
+                    if (c + GROUPS >= C::CHUNKS) {   // this warp's last chunk of the slot
+                        // Accumulator fully read: hand it back to the MMA warp (of the leader CTA).
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(ab), 0));
+                            else ptx::mbar_arrive(tempty_bar(ab));
                         }
                     }
+
+                    // epilogue input of the residual store: the residual's 32 columns
+                    uint32_t lft[16];
+                    if (EPI == EPI_STORE_ADD && pr.res) {
+                        constexpr int NSLOT = C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1;
+                        const int q = res_tiles * C::CHUNKS + c;
+                        const int slot = q % NSLOT;
+                        const bool in_ok = __all_sync(0xffffffffu, wait_bounded(ein_full_bar(slot),
+                                                                                (uint32_t)((q / NSLOT) & 1), tmo,
+                                                                                err, abort_flag, ERR_EPILOGUE));
+                        if (!in_ok) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t slot_base = base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const uint4 r4 = ptx::lds128(slot_base + sw64_offset(row, q4));
+                            lft[4 * q4 + 0] = r4.x; lft[4 * q4 + 1] = r4.y; lft[4 * q4 + 2] = r4.z; lft[4 * q4 + 3] = r4.w;
+                        }
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ein_empty_bar(slot));
+                    }
+                    // outputs for this chunk, packed bf16 pairs (the FP8 forward's h: 4 codes a word)
+                    uint32_t o0[16], o1[16], o2[16];
+                    if (OP == OP_E4M3) {
+                        // FP8 operands: the accumulator carries the product of the operands' scales
+                        float sa = 1.0f;
+                        if constexpr (OP == OP_E4M3) sa = args.scale_acc;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            acc[i] = __float_as_uint(__uint_as_float(acc[i]) * sa);
+                            if (EPI == EPI_SWIGLU_FWD) acc2[i] = __float_as_uint(__uint_as_float(acc2[i]) * sa);
+                        }
+                    }
+                    if (EPI == EPI_STORE || EPI == EPI_STORE_W || (EPI == EPI_STORE_ADD && !pr.res)) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            o0[i] = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+                    } else if (EPI == EPI_STORE_ADD) {
+                        // residual add: C = acc + R, summed in fp32 and rounded once
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            o0[i] = pack_bf16(__uint_as_float(acc[2 * i]) + bf16_lo(lft[i]),
+                                              __uint_as_float(acc[2 * i + 1]) + bf16_hi(lft[i]));
+                    } else if (EPI == EPI_SWIGLU_FWD) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const uint32_t lb = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+                            const uint32_t gb = pack_bf16(__uint_as_float(acc2[2 * i]), __uint_as_float(acc2[2 * i + 1]));
+                            o0[i] = lb;
+                            o1[i] = gb;
+                            float hv[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float l = e ? bf16_hi(lb) : bf16_lo(lb);
+                                const float g = e ? bf16_hi(gb) : bf16_lo(gb);
+                                const float silu = g * sigmoid_mufu(g);
+                                hv[e] = l * round_bf16(silu);
+                            }
+                            if (OP == OP_E4M3) {
+                                // the quantising epilogue: h8 = sat8(round(h / s_h)), two codes per 16 bits
+                                float so = 1.0f;
+                                if constexpr (OP == OP_E4M3) so = args.scale_out;
+                                const uint32_t q2 = ptx::cvt_e4m3x2(hv[0] * so, hv[1] * so);
+                                o2[i >> 1] = (i & 1) ? (o2[i >> 1] | (q2 << 16)) : q2;
+                            } else {
+                                o2[i] = pack_bf16(hv[0], hv[1]);
+                            }
+                        }
+                    }
+
+                    // stage in shared memory (64-byte swizzle) and TMA-store this warp's 32x32 tiles
+                    if (lane == 0) ptx::bulk_wait_group_read<C::OUT_BUFS - 1>();
+                    __syncwarp();
+                    const uint32_t ob_base = out_base + ob * (C::NOUT * C::OUT_TILE);
+#pragma unroll
+                    for (int o = 0; o < C::NOUT; ++o) {
+                        const uint32_t* src = (o == 0) ? o0 : (o == 1) ? o1 : o2;
+                        const uint32_t tile = ob_base + o * C::OUT_TILE;
+                        if (OP == OP_E4M3 && o == 2) {
+                            // the FP8 h tile: 32 rows of 32 bytes, unswizzled
+                            ptx::sts128(tile + lane * 32, make_uint4(src[0], src[1], src[2], src[3]));
+                            ptx::sts128(tile + lane * 32 + 16, make_uint4(src[4], src[5], src[6], src[7]));
+                            continue;
+                        }
+#pragma unroll
+                        for (int q = 0; q < C::CK / 8; ++q)
+                            ptx::sts128(tile + stage_offset<C::CK>(lane, q),
+                                        make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]));
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_live) {
+                        if (C::STORE_ONLY) {
+                            const int n = tn * C::TILE_N + sl * BN + c * CHUNK;
+                            if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
+                        } else {
+                            const int jw = (EPI == EPI_SWIGLU_FWD) ? BN / 2 : BN;
+                            const int j = tn * jw + c * C::CK;
+                            if (j < n_limit) {
+                                if (!pr.no_o0) {
+                                    ptx::tma_store_3d(mO0, ob_base, j, 0, mrow0);
+                                    ptx::tma_store_3d(mO0, ob_base + C::OUT_TILE, j, 1, mrow0);
+                                }
+                                ptx::tma_store_2d(mO1, ob_base + 2 * C::OUT_TILE, j, mrow0);
+                            }
+                        }
+                    }
+                    if (lane == 0) ptx::bulk_commit_group();
+                    ob = (ob + 1) % C::OUT_BUFS;
                 }
-                if (lane == 0) ptx::bulk_commit_group();
-                ob = (ob + 1) % C::OUT_BUFS;
             }
+            slot_seq += (uint32_t)w;
             if (EPI == EPI_STORE_ADD && pr.res) ++res_tiles;
         }
         if (lane == 0) ptx::bulk_wait_group<0>();

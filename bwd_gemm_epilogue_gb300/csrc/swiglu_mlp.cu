@@ -174,6 +174,11 @@ int pick_cg(int64_t M) {
 // Host-only test hook bit: the backward's dW2, dx and dW1 run as three launches.
 constexpr int DEBUG_UNGROUPED = 4;
 
+// Host-only test hook bits: plain GEMMs of CTA pairs always with 256 x 256 tiles, or
+// with 256 x 512 tiles wherever N > 256 (instead of the choice below).
+constexpr int DEBUG_NARROW_TILES = 16;
+constexpr int DEBUG_WIDE_TILES = 32;
+
 Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn, bool b_mn, int cg) {
     Problem p;
     p.M = (int)M;
@@ -181,7 +186,9 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     p.K = (int)K;
     p.tiles_m = (int)((M + BM * cg - 1) / (BM * cg));
     p.tiles_n = (int)tiles_n;
-    const int band = g_raster_band.load() > 0 ? g_raster_band.load() : 8;
+    // raster band: 8 column tiles of 256 (2048 columns); 256 x 512 tiles take half as many
+    int band = g_raster_band.load() > 0 ? g_raster_band.load() : 8;
+    if ((int64_t)tiles_n * BN < N) band = band > 1 ? band / 2 : 1;
     p.band = p.tiles_n < band ? p.tiles_n : band;
     p.k_blocks = (int)((K + BK - 1) / BK);
     p.a_mn = a_mn ? 1 : 0;
@@ -194,15 +201,21 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     return p;
 }
 
+// MMA work of one tile of problem p, in 256 x 256 x 64 units: k-blocks times the tile's
+// 256-column slots (two for a 256 x 512 tile; the ragged last column tile counted as two).
+long long tile_work(const Problem& p) {
+    return (long long)p.k_blocks * ((long long)p.tiles_n * BN < p.N ? 2 : 1);
+}
+
 // Longest-processing-time assignment of the launch's tiles to `units` clusters:
-// tiles in order of decreasing k-blocks (stable within a problem), each to the
+// tiles in order of decreasing work (stable within a problem), each to the
 // least-loaded cluster.  Returns false if the lists do not fit the parameter block.
 bool build_schedule(ScheduledArgs& a, int units) {
     if (units > MAX_CLUSTERS || a.num_tiles > MAX_SCHED || a.num_tiles > 65535) return false;
     int order[MAX_PROBLEMS];
     for (int q = 0; q < a.num_problems; ++q) order[q] = q;
     std::stable_sort(order, order + a.num_problems,
-                     [&](int x, int y) { return a.prob[x].k_blocks > a.prob[y].k_blocks; });
+                     [&](int x, int y) { return tile_work(a.prob[x]) > tile_work(a.prob[y]); });
     std::vector<std::vector<uint16_t>> lists(units);
     using Slot = std::pair<long long, int>;   // (load, cluster)
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
@@ -214,7 +227,7 @@ bool build_schedule(ScheduledArgs& a, int units) {
             Slot s = heap.top();
             heap.pop();
             lists[s.second].push_back((uint16_t)(p.tile_begin + t));
-            heap.push({s.first + p.k_blocks, s.second});
+            heap.push({s.first + tile_work(p), s.second});
         }
     }
     int off = 0;
@@ -563,12 +576,58 @@ struct GemmSpec {
 
 // Fill problem q of `a`: C [M,N] = A * B^T (+ R) with either operand K-major or MN-major.
 // A residual goes through the launch's single residual map i0.
-bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg) {
+// How much faster a 256 x 512 tile's mainloop runs per FLOP than a 256 x 256 tile's: its
+// k-blocks carry a quarter fewer operand bytes per FLOP.  With 256 x 256 tiles the tensor
+// pipe waits on operands; with twice the MMA work per operand byte it ran 12-15 % faster
+// (measured at 11136 x 3584 x 14336, 11136 x 3584 x 28672 and 8192^3).
+constexpr double kWideGain = 1.10;
+
+// Whether one plain GEMM of CTA pairs is faster in 256 x 512 tiles: rounds of tiles over
+// the persistent clusters (a wide tile takes 2 / kWideGain narrow-tile times).  Wide
+// tiles halve the tile count, so they lose where they leave a last round nearly empty.
+bool wide_pays(DeviceState* st, int64_t M, int64_t N) {
+    const int flags = g_debug_flags.load();
+    if ((flags & DEBUG_NARROW_TILES) || N <= BN) return false;
+    if (flags & DEBUG_WIDE_TILES) return true;
+    const int units = cluster_slots<EPI_STORE, 2, SRC_SINGLE>(st);
+    if (units <= 0) return false;
+    const long long tm = (M + 2 * BM - 1) / (2 * BM);
+    const long long narrow = tm * ((N + BN - 1) / BN), wide = tm * ((N + 2 * BN - 1) / (2 * BN));
+    const double t_narrow = (double)((narrow + units - 1) / units);
+    const double t_wide = (double)((wide + units - 1) / units) * 2.0 / kWideGain;
+    return t_wide < t_narrow;
+}
+
+// The same choice for a group of GEMMs under the longest-first schedule, whose makespan
+// is about the larger of the even share of the work and the longest tile.
+bool wide_pays_group(DeviceState* st, const GemmSpec* g, int n) {
+    const int flags = g_debug_flags.load();
+    if (flags & DEBUG_NARROW_TILES) return false;
+    bool any = false;
+    for (int q = 0; q < n; ++q) any = any || g[q].N > BN;
+    if (!any) return false;
+    if (flags & DEBUG_WIDE_TILES) return true;
+    const int units = cluster_slots<EPI_STORE, 2, SRC_PARAMS>(st);
+    if (units <= 0) return false;
+    double work = 0, longest = 0;
+    for (int q = 0; q < n; ++q) {
+        const double kb = (double)((g[q].K + BK - 1) / BK);
+        work += kb * (double)((g[q].M + 2 * BM - 1) / (2 * BM)) * (double)((g[q].N + BN - 1) / BN);
+        longest = kb > longest ? kb : longest;
+    }
+    const double t_narrow = std::max(work / units, longest);
+    const double t_wide = std::max(work / units, 2 * longest) / kWideGain;
+    return t_wide < t_narrow;
+}
+
+// wide: 256 x 512 tiles (EPI_STORE_W launches).
+bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg, bool wide = false) {
     bool a3d = false, b3d = false;
     if (!encode_operand(&a.a[q], g.A, g.M, g.K, g.a_mn, BM, &a3d)) return false;
     if (!encode_operand(&a.b[q], g.B, g.N, g.K, g.b_mn, BN / cg, &b3d)) return false;
     if (!encode_out_2d(&a.o0[q], g.C, g.M, g.N)) return false;
-    a.prob[q] = make_problem(g.M, g.N, g.K, (g.N + BN - 1) / BN, g.a_mn, g.b_mn, cg);
+    const int64_t tile_n = wide ? 2 * BN : BN;
+    a.prob[q] = make_problem(g.M, g.N, g.K, (g.N + tile_n - 1) / tile_n, g.a_mn, g.b_mn, cg);
     a.prob[q].a3d = a3d ? 1 : 0;
     a.prob[q].b3d = b3d ? 1 : 0;
     if (g.R) {
@@ -587,12 +646,14 @@ swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, 
     std::memset(&a, 0, sizeof a);
     GemmSpec g{A, B, Cp, M, N, K, a_mn, b_mn};
     g.R = R;
-    if (!add_problem(a, 0, g, cg)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
+    const bool wide = !R && cg == 2 && wide_pays(st, M, N);
+    if (!add_problem(a, 0, g, cg, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
     a.num_problems = 1;
     if (R) {
         if (cg == 2) return launch<EPI_STORE_ADD, 2, SRC_SINGLE>(st, kind, a, s);
         return launch<EPI_STORE_ADD, 1, SRC_SINGLE>(st, kind, a, s);
     }
+    if (wide) return launch<EPI_STORE_W, 2, SRC_SINGLE>(st, kind, a, s);
     if (cg == 2) return launch<EPI_STORE, 2, SRC_SINGLE>(st, kind, a, s);
     return launch<EPI_STORE, 1, SRC_SINGLE>(st, kind, a, s);
 }
@@ -607,10 +668,13 @@ swiglu_status run_gemm_group(DeviceState* st, int kind, const GemmSpec* g, int n
     for (int q = 0; q < n; ++q) {
         if (g[q].R && res) return fail(SWIGLU_ERR_INVALID_ARG, "group: more than one residual");
         res = res || g[q].R != nullptr;
-        if (!add_problem(a, q, g[q], 2)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (group)");
     }
+    const bool wide = !res && wide_pays_group(st, g, n);
+    for (int q = 0; q < n; ++q)
+        if (!add_problem(a, q, g[q], 2, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (group)");
     a.num_problems = n;
     if (res) return launch<EPI_STORE_ADD, 2, SRC_PARAMS>(st, kind, a, s);
+    if (wide) return launch<EPI_STORE_W, 2, SRC_PARAMS>(st, kind, a, s);
     return launch<EPI_STORE, 2, SRC_PARAMS>(st, kind, a, s);
 }
 
