@@ -453,7 +453,6 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     using C = Cfg<EPI, CG>;
     static_assert(OP == OP_BF16 || ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) && SCHED == SRC_SINGLE),
                   "FP8 operands: forward kernels, one problem per launch");
-    static_assert(!C::WIDE || !is_table(SCHED), "256 x 512 tiles: parameter-block launches");
     constexpr int BKE = OP == OP_E4M3 ? 2 * BK : BK;   // k values per 128-byte k-block
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);

@@ -176,8 +176,8 @@ constexpr int DEBUG_UNGROUPED = 4;
 
 // Host-only test hook bits: plain GEMMs of CTA pairs always with 256 x 256 tiles, or
 // with 256 x 512 tiles wherever N > 256 (instead of the choice below).
-constexpr int DEBUG_NARROW_TILES = 16;
-constexpr int DEBUG_WIDE_TILES = 32;
+constexpr int DEBUG_NARROW_TILES = 32;
+constexpr int DEBUG_WIDE_TILES = 64;
 
 Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn, bool b_mn, int cg) {
     Problem p;
@@ -576,48 +576,51 @@ struct GemmSpec {
 
 // Fill problem q of `a`: C [M,N] = A * B^T (+ R) with either operand K-major or MN-major.
 // A residual goes through the launch's single residual map i0.
-// How much faster a 256 x 512 tile's mainloop runs per FLOP than a 256 x 256 tile's: its
-// k-blocks carry a quarter fewer operand bytes per FLOP.  With 256 x 256 tiles the tensor
-// pipe waits on operands; with twice the MMA work per operand byte it ran 12-15 % faster
-// (measured at 11136 x 3584 x 14336, 11136 x 3584 x 28672 and 8192^3).
-constexpr double kWideGain = 1.10;
+// 256 x 512 tiles against 256 x 256 tiles.  A wide tile's k-blocks carry a quarter fewer
+// operand bytes per FLOP: the tensor pipe runs faster while fed (with twice the MMA work
+// per operand byte it ran 12-15 % faster at 11136 x 3584 x 14336, 11136 x 3584 x 28672 and
+// 8192^3) and a FLOP costs less energy.  But a wide tile holds both TMEM accumulators, so
+// the MMA issuer waits for the previous tile's whole drain, and the tile count halves.
+// Measured in the step: wide tiles win in long launches that run at the power cap (the
+// target block's grouped backward 3436 -> 3258 us, 8 experts of 2048 rows 6490 -> 6028 us),
+// tie or lose in short ones at full clock (4096-token block 1017 -> 1034 us; 64 experts of
+// ~384 rows), and lose in the forward's down projection (3-11 % slower, dense and MoE,
+// which therefore keeps 256 x 256 tiles).  So: wide tiles for launches of at least
+// kWideMinClusterKBlocks k-block times per cluster whose products are not short, whose
+// longest wide tile fits the even share, and (one GEMM, static round-robin tiles) whose
+// last round of wide tiles costs no more than the narrow tiles' rounds.
+constexpr double kWideGain = 1.05;                 // mainloop speed-up per FLOP
+constexpr double kWideDrain = 9.0;                 // exposed drain per wide tile, in k-block times
+constexpr double kWideMinKBlocks = 24;             // least mean k-blocks per 256 x 256 tile
+constexpr double kWideMinClusterKBlocks = 4000;    // least k-block times per cluster (~1.3 ms)
 
-// Whether one plain GEMM of CTA pairs is faster in 256 x 512 tiles: rounds of tiles over
-// the persistent clusters (a wide tile takes 2 / kWideGain narrow-tile times).  Wide
-// tiles halve the tile count, so they lose where they leave a last round nearly empty.
-bool wide_pays(DeviceState* st, int64_t M, int64_t N) {
-    const int flags = g_debug_flags.load();
-    if ((flags & DEBUG_NARROW_TILES) || N <= BN) return false;
-    if (flags & DEBUG_WIDE_TILES) return true;
-    const int units = cluster_slots<EPI_STORE, 2, SRC_SINGLE>(st);
-    if (units <= 0) return false;
-    const long long tm = (M + 2 * BM - 1) / (2 * BM);
-    const long long narrow = tm * ((N + BN - 1) / BN), wide = tm * ((N + 2 * BN - 1) / (2 * BN));
-    const double t_narrow = (double)((narrow + units - 1) / units);
-    const double t_wide = (double)((wide + units - 1) / units) * 2.0 / kWideGain;
-    return t_wide < t_narrow;
-}
-
-// The same choice for a group of GEMMs under the longest-first schedule, whose makespan
-// is about the larger of the even share of the work and the longest tile.
-bool wide_pays_group(DeviceState* st, const GemmSpec* g, int n) {
+bool wide_pays_group(DeviceState* st, const GemmSpec* g, int n, bool round_robin = false) {
     const int flags = g_debug_flags.load();
     if (flags & DEBUG_NARROW_TILES) return false;
     bool any = false;
     for (int q = 0; q < n; ++q) any = any || g[q].N > BN;
     if (!any) return false;
     if (flags & DEBUG_WIDE_TILES) return true;
-    const int units = cluster_slots<EPI_STORE, 2, SRC_PARAMS>(st);
+    const int units = cluster_slots<EPI_STORE, 2, SRC_SINGLE>(st);
     if (units <= 0) return false;
-    double work = 0, longest = 0;
+    double work = 0, tiles = 0, longest = 0;
     for (int q = 0; q < n; ++q) {
         const double kb = (double)((g[q].K + BK - 1) / BK);
-        work += kb * (double)((g[q].M + 2 * BM - 1) / (2 * BM)) * (double)((g[q].N + BN - 1) / BN);
+        const double t = (double)((g[q].M + 2 * BM - 1) / (2 * BM)) * (double)((g[q].N + BN - 1) / BN);
+        work += kb * t;
+        tiles += t;
         longest = kb > longest ? kb : longest;
     }
-    const double t_narrow = std::max(work / units, longest);
-    const double t_wide = std::max(work / units, 2 * longest) / kWideGain;
-    return t_wide < t_narrow;
+    if (work < kWideMinClusterKBlocks * units || work < kWideMinKBlocks * tiles) return false;
+    if (2 * longest / kWideGain + kWideDrain > work / units) return false;
+    if (round_robin && n == 1) {
+        const long long tm = (g[0].M + 2 * BM - 1) / (2 * BM);
+        const long long narrow = tm * ((g[0].N + BN - 1) / BN), wide = tm * ((g[0].N + 2 * BN - 1) / (2 * BN));
+        const double t_narrow = (double)((narrow + units - 1) / units) * longest;
+        const double t_wide = (double)((wide + units - 1) / units) * (2 * longest / kWideGain + kWideDrain);
+        if (t_wide >= t_narrow) return false;
+    }
+    return true;
 }
 
 // wide: 256 x 512 tiles (EPI_STORE_W launches).
@@ -638,7 +641,8 @@ bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg, bool wide = fa
     return true;
 }
 
-// One plain GEMM, optionally with a residual added in its epilogue.
+// One plain GEMM, optionally with a residual added in its epilogue.  The forward's down
+// projection (kind FWD_DOWN) keeps 256 x 256 tiles unless the test hook asks for wide ones.
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
                        int64_t K, bool a_mn, bool b_mn, cudaStream_t s, const void* R = nullptr) {
     const int cg = pick_cg(M);
@@ -646,7 +650,8 @@ swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, 
     std::memset(&a, 0, sizeof a);
     GemmSpec g{A, B, Cp, M, N, K, a_mn, b_mn};
     g.R = R;
-    const bool wide = !R && cg == 2 && wide_pays(st, M, N);
+    const bool may_wide = kind != SWIGLU_KERNEL_FWD_DOWN || (g_debug_flags.load() & DEBUG_WIDE_TILES);
+    const bool wide = !R && cg == 2 && may_wide && wide_pays_group(st, &g, 1, true);
     if (!add_problem(a, 0, g, cg, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
     a.num_problems = 1;
     if (R) {
@@ -1246,12 +1251,13 @@ swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& e
     if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
     const int units = (int)std::min<long long>(tiles, std::min(slots, kMaxUnits));
 
-    // longest-processing-time: problems by decreasing k-blocks, each tile to the
-    // least-loaded cluster (a tile costs its k-blocks plus one for its epilogue)
+    // longest-processing-time: problems by decreasing work, each tile to the least-loaded
+    // cluster (a tile costs its work plus one per accumulator slot for its epilogue)
+    auto cost = [&](const Problem& p) { return tile_work(p) + tile_work(p) / p.k_blocks; };
     std::vector<int> order(n);
     for (int i = 0; i < n; ++i) order[i] = i;
     std::stable_sort(order.begin(), order.end(),
-                     [&](int a, int b) { return ents[a].prob.k_blocks > ents[b].prob.k_blocks; });
+                     [&](int a, int b) { return cost(ents[a].prob) > cost(ents[b].prob); });
     std::vector<std::vector<int>> lists(units);
     using Slot = std::pair<long long, int>;
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
@@ -1263,7 +1269,7 @@ swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& e
             Slot sl = heap.top();
             heap.pop();
             lists[sl.second].push_back((pi << TABLE_TILE_BITS) | t);
-            heap.push({sl.first + p.k_blocks + 1, sl.second});
+            heap.push({sl.first + cost(p), sl.second});
         }
     }
     const size_t off_sched_off = round256((size_t)n * sizeof(TableEntry));
@@ -1359,13 +1365,15 @@ size_t moe_bwd_tables(const std::vector<int64_t>& off, const MoeDims& d, size_t*
 }
 
 // Plain-GEMM entry: C [M,N] = A * B^T, either operand K-major or MN-major.
-bool fill_gemm(TableEntry& t, const GemmSpec& g, int cg) {
+// wide: 256 x 512 tiles (EPI_STORE_W launches).
+bool fill_gemm(TableEntry& t, const GemmSpec& g, int cg, bool wide = false) {
     std::memset(&t, 0, sizeof t);
     bool a3d = false, b3d = false;
     if (!encode_operand(&t.a, g.A, g.M, g.K, g.a_mn, BM, &a3d)) return false;
     if (!encode_operand(&t.b, g.B, g.N, g.K, g.b_mn, BN / cg, &b3d)) return false;
     if (!encode_out_2d(&t.o0, g.C, g.M, g.N)) return false;
-    t.prob = make_problem(g.M, g.N, g.K, (g.N + BN - 1) / BN, g.a_mn, g.b_mn, cg);
+    const int64_t tile_n = wide ? 2 * BN : BN;
+    t.prob = make_problem(g.M, g.N, g.K, (g.N + tile_n - 1) / tile_n, g.a_mn, g.b_mn, cg);
     t.prob.a3d = a3d ? 1 : 0;
     t.prob.b3d = b3d ? 1 : 0;
     return true;
@@ -1453,15 +1461,22 @@ swiglu_status swiglu_moe_fwd(const void* x, const void* W1, const void* W2, void
     rc = cg == 2 ? launch_table<EPI_SWIGLU_FWD, 2>(st, SWIGLU_KERNEL_FWD_PREACT, ents, table_a, tab_a, s)
                  : launch_table<EPI_SWIGLU_FWD, 1>(st, SWIGLU_KERNEL_FWD_PREACT, ents, table_a, tab_a, s);
     if (rc != SWIGLU_OK) return rc;
-    ents.clear();
+    std::vector<GemmSpec> specs;
     for (int64_t e = 0; e < E; ++e) {        // y_e = h_e @ W2[e]^T
         const int64_t m = off[e + 1] - off[e];
         if (m == 0) continue;
-        ents.emplace_back();
-        const GemmSpec g{at_row<uint8_t>(h, off[e], H), at_row<uint8_t>(W2, e * Dout, H),
-                         at_row<uint8_t>(y, off[e], Dout), m, Dout, H, false, false};
-        if (!fill_gemm(ents.back(), g, cg)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe fwd_down)");
+        specs.push_back(GemmSpec{at_row<uint8_t>(h, off[e], H), at_row<uint8_t>(W2, e * Dout, H),
+                                 at_row<uint8_t>(y, off[e], Dout), m, Dout, H, false, false});
     }
+    // the down projection keeps 256 x 256 tiles unless the test hook asks for wide ones
+    const bool wide = cg == 2 && (g_debug_flags.load() & DEBUG_WIDE_TILES) &&
+                      wide_pays_group(st, specs.data(), (int)specs.size());
+    ents.clear();
+    for (const GemmSpec& g : specs) {
+        ents.emplace_back();
+        if (!fill_gemm(ents.back(), g, cg, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe fwd_down)");
+    }
+    if (wide) return launch_table<EPI_STORE_W, 2>(st, SWIGLU_KERNEL_FWD_DOWN, ents, table_b, tabs - tab_a, s);
     return cg == 2 ? launch_table<EPI_STORE, 2>(st, SWIGLU_KERNEL_FWD_DOWN, ents, table_b, tabs - tab_a, s)
                    : launch_table<EPI_STORE, 1>(st, SWIGLU_KERNEL_FWD_DOWN, ents, table_b, tabs - tab_a, s);
 }
@@ -1530,8 +1545,9 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
     const int cgw = (g_debug_flags.load() & DEBUG_FORCE_SINGLE_CTA) ? 1 : 2;
     const bool grouped = !(g_debug_flags.load() & DEBUG_UNGROUPED);
     const int kinds[3] = {SWIGLU_KERNEL_BWD_DW2, SWIGLU_KERNEL_BWD_DX, SWIGLU_KERNEL_BWD_DW1};
+    std::vector<GemmSpec> specs;
     for (int part = grouped ? -1 : 0; part < (grouped ? 0 : 3); ++part) {
-        ents.clear();
+        specs.clear();
         for (int64_t e = 0; e < E; ++e) {
             const int64_t m = off[e + 1] - off[e];
             if (m == 0) continue;
@@ -1542,15 +1558,20 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
                 {gpe, at_row<uint8_t>(W1, e * 2 * H, D), at_row<uint8_t>(dx, off[e], D), m, D, 2 * H, false, true},
                 {gpe, at_row<uint8_t>(x, off[e], D), at_row<uint8_t>(dW1, e * 2 * H, D), 2 * H, D, m, true, true},
             };
-            for (int q = 0; q < 3; ++q) {
-                if (part >= 0 && q != part) continue;
-                ents.emplace_back();
-                if (!fill_gemm(ents.back(), g[q], cgw)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe bwd)");
-            }
+            for (int q = 0; q < 3; ++q)
+                if (part < 0 || q == part) specs.push_back(g[q]);
+        }
+        // 256 x 512 tiles where the longest-first schedule over the experts favours them
+        const bool wide = cgw == 2 && wide_pays_group(st, specs.data(), (int)specs.size());
+        ents.clear();
+        for (const GemmSpec& g : specs) {
+            ents.emplace_back();
+            if (!fill_gemm(ents.back(), g, cgw, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (moe bwd)");
         }
         const int kind = part < 0 ? SWIGLU_KERNEL_BWD_GEMMS : kinds[part];
-        rc = cgw == 2 ? launch_table<EPI_STORE, 2>(st, kind, ents, table_b, tabs - tab_a, s)
-                      : launch_table<EPI_STORE, 1>(st, kind, ents, table_b, tabs - tab_a, s);
+        rc = wide ? launch_table<EPI_STORE_W, 2>(st, kind, ents, table_b, tabs - tab_a, s)
+             : cgw == 2 ? launch_table<EPI_STORE, 2>(st, kind, ents, table_b, tabs - tab_a, s)
+                        : launch_table<EPI_STORE, 1>(st, kind, ents, table_b, tabs - tab_a, s);
         if (rc != SWIGLU_OK) return rc;
     }
     return SWIGLU_OK;

@@ -282,14 +282,16 @@ void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
  * tiles.  Bit 2: the backward launches dW2, dx and dW1 separately instead of as
  * one grouped launch.  Bit 3: M <= 64 keeps the 128-row tile path instead of the
  * small-M path.  Bit 4: MoE launches keep CTA-pair tiles even when 128-row tiles
- * would compute fewer padded rows.  (Every setting computes the same result; the
+ * would compute fewer padded rows.  Bit 5: plain GEMMs of CTA pairs always use
+ * 256 x 256 tiles; bit 6: they use 256 x 512 tiles wherever N > 256 (by default
+ * the library picks per launch).  (Every setting computes the same result; the
  * bits exist to test each path.) */
 void swiglu_mlp_set_debug_flags(int flags);
 
-/* Tuning knob, process-wide: the width, in 256-column tiles, of the bands the tile
+/* Tuning knob, process-wide: the width, in 256-column units, of the bands the tile
  * kernels walk their output in (all rows of a band before the next band, so a band's
- * B slabs stay in L2 while the A slabs stream past).  0 (the default) = 8.  Any
- * value >= 1 computes the same result. */
+ * B slabs stay in L2 while the A slabs stream past; 256 x 512 tiles take half as many
+ * tiles per band).  0 (the default) = 8.  Any value >= 1 computes the same result. */
 void swiglu_mlp_set_raster_band(int n_tiles);
 
 /* Kernel kinds reported by the launch trace. */

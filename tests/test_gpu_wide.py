@@ -3,7 +3,7 @@
 Both tile shapes accumulate every output element over the same k-steps in the same order
 with the same MMA shape (M = 256, N = 256, K = 16), so their results must agree bit for
 bit; the wide tiles are also checked against the fp64 product and the oracle.  The test
-hook bits force one tile shape (16: 256 x 256 everywhere, 32: 256 x 512 wherever N > 256)
+hook bits force one tile shape (32: 256 x 256 everywhere, 64: 256 x 512 wherever N > 256)
 instead of the library's choice.
 """
 import pytest
@@ -15,7 +15,7 @@ from bwd_gemm_epilogue_gb300.workloads import Shape
 from helpers import ensure_library, parity
 
 pytestmark = pytest.mark.gpu
-NARROW, WIDE = 16, 32
+NARROW, WIDE = 32, 64
 
 
 @pytest.fixture(scope="module")
@@ -110,3 +110,28 @@ def test_wide_tile_wait_times_out_and_context_survives(b):
     assert b.swiglu_mlp_device_status() == 0
     C = with_flags(b, WIDE, lambda: b.swiglu_mlp_gemm_bf16(A, B, 512, 768, 128, False, False))
     parity(C, (A.double() @ B.double().T).cpu().numpy(), "C after timeout")
+
+
+@pytest.mark.parametrize("case", ["pages_counts", "ragged", "one_expert", "many_small"])
+def test_moe_layer_with_wide_tiles_matches_narrow_bits(b, case):
+    # the experts' down projections and weight-gradient / dx products in one table launch
+    from test_gpu_moe import CASES, _experts
+    counts, D, H, Dout = CASES[case]
+    x, W1, W2, dy, preact = _experts(counts, D, H, Dout, seed=83)
+    xd, W1d, W2d, dyd, pred = dev(x), dev(W1), dev(W2), dev(dy), dev(preact)
+    res = {}
+    for name, flags in (("narrow", NARROW), ("wide", WIDE), ("wide, three launches", WIDE | 4)):
+        fwd = with_flags(b, flags, lambda: b.swiglu_moe_fwd(xd, W1d, W2d, counts))
+        bwd = with_flags(b, flags, lambda: b.swiglu_moe_bwd(xd, W1d, W2d, pred, dyd, counts))
+        res[name] = fwd + bwd
+    for name in ("wide", "wide, three launches"):
+        for u, v, what in zip(res["narrow"], res[name], ("preact", "y", "dx", "dW1", "dW2")):
+            assert torch.equal(u, v), f"{what}: {name} tiles differ from narrow tiles ({case})"
+    y_ref = oracle.moe_fwd(x, W1, W2, counts)[2]
+    parity(res["wide"][1], y_ref, f"y, wide tiles ({case})")
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.moe_bwd_full(x, W1, W2, preact, dy, counts)
+    parity(res["wide"][2], dx_ref, f"dx, wide tiles ({case})")
+    for e in range(len(counts)):
+        if counts[e]:
+            parity(res["wide"][3][e], dW1_ref[e], f"dW1[{e}], wide tiles ({case})")
+            parity(res["wide"][4][e], dW2_ref[e], f"dW2[{e}], wide tiles ({case})")
