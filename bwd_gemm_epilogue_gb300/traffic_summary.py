@@ -23,8 +23,9 @@ ROOT = os.path.dirname(HERE)
 sys.path.insert(0, ROOT)
 
 # template arguments of the target step's four launches -> bench kind names
+# (EPI 4: the store epilogue over 256 x 512 tiles, which the grouped backward uses at this size)
 KINDS = {("1", "2", "0"): "fwd_preact", ("0", "2", "0"): "fwd_down", ("2", "2", "0"): "bwd_grad_h",
-         ("0", "2", "1"): "bwd_gemms"}
+         ("0", "2", "1"): "bwd_gemms", ("4", "2", "1"): "bwd_gemms", ("4", "2", "0"): "fwd_down"}
 
 
 def summarize(path: str) -> dict:
