@@ -987,6 +987,47 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 ptx::tc_fence_after();
                 const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
 
+                if constexpr ((EPI == EPI_STORE || EPI == EPI_STORE_W) && OP == OP_BF16) {
+                    // Plain bf16 stores: all of this warp's chunks of the slot into registers as
+                    // packed bf16 first, then the slot goes back to the MMA warp, then the
+                    // stores.  A 256 x 512 tile's next mainloop waits for its slots' release.
+                    constexpr int NCH = C::CHUNKS / GROUPS;
+                    uint32_t pk[NCH][16];
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) {
+                        uint32_t acc[32];
+                        ptx::tmem_ld_32x32b_x32(t_row + (grp + i * GROUPS) * CHUNK, acc);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            pk[i][j] = pack_bf16(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(ab), 0));
+                        else ptx::mbar_arrive(tempty_bar(ab));
+                    }
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) {
+                        const int c = grp + i * GROUPS;
+                        if (lane == 0) ptx::bulk_wait_group_read<C::OUT_BUFS - 1>();
+                        __syncwarp();
+                        const uint32_t ob_base = out_base + ob * (C::NOUT * C::OUT_TILE);
+#pragma unroll
+                        for (int q = 0; q < C::CK / 8; ++q)
+                            ptx::sts128(ob_base + stage_offset<C::CK>(lane, q),
+                                        make_uint4(pk[i][4 * q], pk[i][4 * q + 1], pk[i][4 * q + 2], pk[i][4 * q + 3]));
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && rows_live) {
+                            const int n = tn * C::TILE_N + sl * BN + c * CHUNK;
+                            if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
+                        }
+                        if (lane == 0) ptx::bulk_commit_group();
+                        ob = (ob + 1) % C::OUT_BUFS;
+                    }
+                } else {
                 for (int c = grp; c < C::CHUNKS; c += GROUPS) {
                     uint32_t acc[32];
                     uint32_t acc2[32];
@@ -1117,6 +1158,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     }
                     if (lane == 0) ptx::bulk_commit_group();
                     ob = (ob + 1) % C::OUT_BUFS;
+                }
                 }
             }
             slot_seq += (uint32_t)w;

@@ -579,48 +579,58 @@ struct GemmSpec {
 // 256 x 512 tiles against 256 x 256 tiles.  A wide tile's k-blocks carry a quarter fewer
 // operand bytes per FLOP: the tensor pipe runs faster while fed (with twice the MMA work
 // per operand byte it ran 12-15 % faster at 11136 x 3584 x 14336, 11136 x 3584 x 28672 and
-// 8192^3) and a FLOP costs less energy.  But a wide tile holds both TMEM accumulators, so
-// the MMA issuer waits for the previous tile's whole drain, and the tile count halves.
-// Measured in the step: wide tiles win in long launches that run at the power cap (the
-// target block's grouped backward 3436 -> 3258 us, 8 experts of 2048 rows 6490 -> 6028 us),
-// tie or lose in short ones at full clock (4096-token block 1017 -> 1034 us; 64 experts of
-// ~384 rows), and lose in the forward's down projection (3-11 % slower, dense and MoE,
-// which therefore keeps 256 x 256 tiles).  So: wide tiles for launches of at least
-// kWideMinClusterKBlocks k-block times per cluster whose products are not short, whose
-// longest wide tile fits the even share, and (one GEMM, static round-robin tiles) whose
-// last round of wide tiles costs no more than the narrow tiles' rounds.
-constexpr double kWideGain = 1.05;                 // mainloop speed-up per FLOP
-constexpr double kWideDrain = 9.0;                 // exposed drain per wide tile, in k-block times
-constexpr double kWideMinKBlocks = 24;             // least mean k-blocks per 256 x 256 tile
-constexpr double kWideMinClusterKBlocks = 4000;    // least k-block times per cluster (~1.3 ms)
+// 8192^3) and a FLOP costs less energy, which counts double while the step runs at the
+// power cap.  But a wide tile holds both TMEM accumulators, so the MMA issuer waits for the
+// epilogue to read the previous tile's slots, and the tile count halves.  The rules below
+// are fitted to steps measured with each choice (narrow / chosen / wide everywhere):
+//   target block (11136 tokens)   6549 / 6211 / 6135 us
+//   8 experts of 2048 rows          11774 / 11142 / 11017 us
+//   4096-token block                1984 / 1990 / 2000 us (its grouped backward loses 1.5 %,
+//                                   its down projection gains 4 %)
+//   64 experts of ~384 rows         1311 / 1311 / 1289 us (grouped backward 681 -> 656 us,
+//                                   down projection 130 -> 135 us)
+// The backward's dW2 / dx / dW1 group, longest-first over the parameter block: wide if there
+// are at least kWideMinClusterKBlocks k-block times of work per CTA pair, at least
+// kWideMinKBlocks per 256 x 256 tile on average, and the longest wide tile fits the even
+// share.  The same group over a table of experts: wide tiles always (half the tiles means
+// half the per-tile problem switches, which cost more there than the slot reads).
+constexpr double kWideMinKBlocks = 24;
+constexpr double kWideMinClusterKBlocks = 4000;
+// Down projections and other single products: wide if their reduction is long (at least
+// kWideMinKBlocksLong k-blocks per tile, so the exposed slot reads stay near 1 % of a tile)
+// and the wide tiles still fill every CTA pair once.
+constexpr double kWideMinKBlocksLong = 100;
 
-bool wide_pays_group(DeviceState* st, const GemmSpec* g, int n, bool round_robin = false) {
+struct WideStats {
+    double work = 0, tiles = 0, longest = 0, wide_tiles = 0;
+};
+WideStats wide_stats(const GemmSpec* g, int n) {
+    WideStats w;
+    for (int q = 0; q < n; ++q) {
+        const double kb = (double)((g[q].K + BK - 1) / BK);
+        const double tm = (double)((g[q].M + 2 * BM - 1) / (2 * BM));
+        w.work += kb * tm * (double)((g[q].N + BN - 1) / BN);
+        w.tiles += tm * (double)((g[q].N + BN - 1) / BN);
+        w.wide_tiles += tm * (double)((g[q].N + 2 * BN - 1) / (2 * BN));
+        w.longest = kb > w.longest ? kb : w.longest;
+    }
+    return w;
+}
+
+enum WideRule { WIDE_GROUP, WIDE_TABLE_GROUP, WIDE_LONG_K };
+bool wide_pays(DeviceState* st, const GemmSpec* g, int n, WideRule rule) {
     const int flags = g_debug_flags.load();
     if (flags & DEBUG_NARROW_TILES) return false;
     bool any = false;
     for (int q = 0; q < n; ++q) any = any || g[q].N > BN;
     if (!any) return false;
-    if (flags & DEBUG_WIDE_TILES) return true;
+    if ((flags & DEBUG_WIDE_TILES) || rule == WIDE_TABLE_GROUP) return true;
     const int units = cluster_slots<EPI_STORE, 2, SRC_SINGLE>(st);
     if (units <= 0) return false;
-    double work = 0, tiles = 0, longest = 0;
-    for (int q = 0; q < n; ++q) {
-        const double kb = (double)((g[q].K + BK - 1) / BK);
-        const double t = (double)((g[q].M + 2 * BM - 1) / (2 * BM)) * (double)((g[q].N + BN - 1) / BN);
-        work += kb * t;
-        tiles += t;
-        longest = kb > longest ? kb : longest;
-    }
-    if (work < kWideMinClusterKBlocks * units || work < kWideMinKBlocks * tiles) return false;
-    if (2 * longest / kWideGain + kWideDrain > work / units) return false;
-    if (round_robin && n == 1) {
-        const long long tm = (g[0].M + 2 * BM - 1) / (2 * BM);
-        const long long narrow = tm * ((g[0].N + BN - 1) / BN), wide = tm * ((g[0].N + 2 * BN - 1) / (2 * BN));
-        const double t_narrow = (double)((narrow + units - 1) / units) * longest;
-        const double t_wide = (double)((wide + units - 1) / units) * (2 * longest / kWideGain + kWideDrain);
-        if (t_wide >= t_narrow) return false;
-    }
-    return true;
+    const WideStats w = wide_stats(g, n);
+    if (rule == WIDE_LONG_K) return w.work >= kWideMinKBlocksLong * w.tiles && w.wide_tiles >= units;
+    return w.work >= kWideMinClusterKBlocks * units && w.work >= kWideMinKBlocks * w.tiles &&
+           2 * w.longest <= w.work / units;
 }
 
 // wide: 256 x 512 tiles (EPI_STORE_W launches).
@@ -641,8 +651,7 @@ bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg, bool wide = fa
     return true;
 }
 
-// One plain GEMM, optionally with a residual added in its epilogue.  The forward's down
-// projection (kind FWD_DOWN) keeps 256 x 256 tiles unless the test hook asks for wide ones.
+// One plain GEMM, optionally with a residual added in its epilogue.
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
                        int64_t K, bool a_mn, bool b_mn, cudaStream_t s, const void* R = nullptr) {
     const int cg = pick_cg(M);
@@ -650,8 +659,7 @@ swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, 
     std::memset(&a, 0, sizeof a);
     GemmSpec g{A, B, Cp, M, N, K, a_mn, b_mn};
     g.R = R;
-    const bool may_wide = kind != SWIGLU_KERNEL_FWD_DOWN || (g_debug_flags.load() & DEBUG_WIDE_TILES);
-    const bool wide = !R && cg == 2 && may_wide && wide_pays_group(st, &g, 1, true);
+    const bool wide = !R && cg == 2 && wide_pays(st, &g, 1, WIDE_LONG_K);
     if (!add_problem(a, 0, g, cg, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
     a.num_problems = 1;
     if (R) {
@@ -674,7 +682,7 @@ swiglu_status run_gemm_group(DeviceState* st, int kind, const GemmSpec* g, int n
         if (g[q].R && res) return fail(SWIGLU_ERR_INVALID_ARG, "group: more than one residual");
         res = res || g[q].R != nullptr;
     }
-    const bool wide = !res && wide_pays_group(st, g, n);
+    const bool wide = !res && wide_pays(st, g, n, WIDE_GROUP);
     for (int q = 0; q < n; ++q)
         if (!add_problem(a, q, g[q], 2, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (group)");
     a.num_problems = n;
@@ -1468,9 +1476,7 @@ swiglu_status swiglu_moe_fwd(const void* x, const void* W1, const void* W2, void
         specs.push_back(GemmSpec{at_row<uint8_t>(h, off[e], H), at_row<uint8_t>(W2, e * Dout, H),
                                  at_row<uint8_t>(y, off[e], Dout), m, Dout, H, false, false});
     }
-    // the down projection keeps 256 x 256 tiles unless the test hook asks for wide ones
-    const bool wide = cg == 2 && (g_debug_flags.load() & DEBUG_WIDE_TILES) &&
-                      wide_pays_group(st, specs.data(), (int)specs.size());
+    const bool wide = cg == 2 && wide_pays(st, specs.data(), (int)specs.size(), WIDE_LONG_K);
     ents.clear();
     for (const GemmSpec& g : specs) {
         ents.emplace_back();
@@ -1561,8 +1567,7 @@ swiglu_status swiglu_moe_bwd(const void* x, const void* W1, const void* W2, cons
             for (int q = 0; q < 3; ++q)
                 if (part < 0 || q == part) specs.push_back(g[q]);
         }
-        // 256 x 512 tiles where the longest-first schedule over the experts favours them
-        const bool wide = cgw == 2 && wide_pays_group(st, specs.data(), (int)specs.size());
+        const bool wide = cgw == 2 && wide_pays(st, specs.data(), (int)specs.size(), WIDE_TABLE_GROUP);
         ents.clear();
         for (const GemmSpec& g : specs) {
             ents.emplace_back();
