@@ -118,6 +118,7 @@ struct Problem {
     int res;          // EPI_STORE_ADD: add the residual tensor (tensor map i0) to this problem's output
     int tile_begin;   // index of this problem's first tile in the launch
     int no_o0;        // EPI_SWIGLU_FWD: do not store preact (o0), only h
+    int slots;        // EPI_STORE_W: 256-column accumulator slots per tile (2: 256 x 512 tiles; 1: 256 x 256)
 };
 
 struct KernelArgs {
@@ -195,7 +196,6 @@ struct Cfg {
     static constexpr bool WIDE = EPI == EPI_STORE_W;
     static_assert(!WIDE || CG == 2, "256 x 512 tiles are CTA-pair tiles");
     static constexpr int SLOTS = WIDE ? 2 : 1;
-    static constexpr int TILE_N = SLOTS * BN;                     // output columns per tile
     static constexpr int STAGES =
         WIDE ? 4
              : CG == 1 ? ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) ? 4 : 3)
@@ -282,11 +282,19 @@ __device__ __forceinline__ void tile_coords(const Problem& p, int t, int& tm, in
     tn = n0 + (r - tm * w);
 }
 
+// Output columns per tile of problem p: 512 for a problem of 256 x 512 tiles, else 256
+// (a launch of 256 x 512 tiles may carry problems of 256 x 256 tiles beside them).
+template <class C>
+__device__ __forceinline__ int tile_cols(const Problem& p) {
+    if constexpr (C::WIDE) return p.slots * BN;
+    else return BN;
+}
+
 // Accumulator slots (256 columns each) of the tile in column-tile tn: two for a 256 x 512
 // tile unless its second half lies wholly past N.
 template <class C>
 __device__ __forceinline__ int tile_slots(const Problem& p, int tn) {
-    if constexpr (C::WIDE) return tn * C::TILE_N + BN < p.N ? 2 : 1;
+    if constexpr (C::WIDE) return p.slots == 2 && tn * 2 * BN + BN < p.N ? 2 : 1;
     else return 1;
 }
 
@@ -602,7 +610,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         } else {
                             // slot j of the tile: B rows [n0 + j * BN, + BN), this CTA's B_ROWS of them
                             for (int j = 0; j < w; ++j) {
-                                const int n0 = tn * C::TILE_N + j * BN + C::B_ROWS * (int)rank;
+                                const int n0 = tn * tile_cols<C>(p) + j * BN + C::B_ROWS * (int)rank;
                                 const uint32_t sBj = sB + j * C::B_SLOT_BYTES;
                                 if (!b_mn) {
                                     load2(sBj, mb, k0, n0);
@@ -1021,7 +1029,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0 && rows_live) {
-                            const int n = tn * C::TILE_N + sl * BN + c * CHUNK;
+                            const int n = tn * tile_cols<C>(pr) + sl * BN + c * CHUNK;
                             if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
                         }
                         if (lane == 0) ptx::bulk_commit_group();
@@ -1142,7 +1150,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     __syncwarp();
                     if (lane == 0 && rows_live) {
                         if (C::STORE_ONLY) {
-                            const int n = tn * C::TILE_N + sl * BN + c * CHUNK;
+                            const int n = tn * tile_cols<C>(pr) + sl * BN + c * CHUNK;
                             if (n < n_limit) ptx::tma_store_2d(mO0, ob_base, n, mrow0);
                         } else {
                             const int jw = (EPI == EPI_SWIGLU_FWD) ? BN / 2 : BN;

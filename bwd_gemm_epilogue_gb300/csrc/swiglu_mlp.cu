@@ -179,7 +179,8 @@ constexpr int DEBUG_UNGROUPED = 4;
 constexpr int DEBUG_NARROW_TILES = 32;
 constexpr int DEBUG_WIDE_TILES = 64;
 
-Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn, bool b_mn, int cg) {
+// slots: 2 for a problem of 256 x 512 tiles (EPI_STORE_W launches), else 1.
+Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn, bool b_mn, int cg, int slots = 1) {
     Problem p;
     p.M = (int)M;
     p.N = (int)N;
@@ -188,7 +189,7 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     p.tiles_n = (int)tiles_n;
     // raster band: 8 column tiles of 256 (2048 columns); 256 x 512 tiles take half as many
     int band = g_raster_band.load() > 0 ? g_raster_band.load() : 8;
-    if ((int64_t)tiles_n * BN < N) band = band > 1 ? band / 2 : 1;
+    if (slots == 2) band = band > 1 ? band / 2 : 1;
     p.band = p.tiles_n < band ? p.tiles_n : band;
     p.k_blocks = (int)((K + BK - 1) / BK);
     p.a_mn = a_mn ? 1 : 0;
@@ -198,13 +199,20 @@ Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn
     p.res = 0;
     p.tile_begin = 0;
     p.no_o0 = 0;
+    p.slots = slots;
     return p;
 }
 
-// MMA work of one tile of problem p, in 256 x 256 x 64 units: k-blocks times the tile's
-// 256-column slots (two for a 256 x 512 tile; the ragged last column tile counted as two).
-long long tile_work(const Problem& p) {
-    return (long long)p.k_blocks * ((long long)p.tiles_n * BN < p.N ? 2 : 1);
+// A 256 x 512 tile's mainloop runs this much faster per FLOP than a 256 x 256 tile's (its
+// k-blocks carry a quarter fewer operand bytes per FLOP), and the MMA issuer then waits
+// about this many k-block times for the epilogue to read the previous tile's slots.
+constexpr double kWideGain = 1.05;
+constexpr double kWideDrain = 9.0;
+
+// Time of one tile of problem p in 256 x 256 x 64 k-block times (the ragged last column
+// tile of a 256 x 512 problem counted as a whole one).
+double tile_cost(const Problem& p) {
+    return p.slots == 2 ? 2.0 * p.k_blocks / kWideGain + kWideDrain : (double)p.k_blocks;
 }
 
 // Longest-processing-time assignment of the launch's tiles to `units` clusters:
@@ -215,9 +223,9 @@ bool build_schedule(ScheduledArgs& a, int units) {
     int order[MAX_PROBLEMS];
     for (int q = 0; q < a.num_problems; ++q) order[q] = q;
     std::stable_sort(order, order + a.num_problems,
-                     [&](int x, int y) { return tile_work(a.prob[x]) > tile_work(a.prob[y]); });
+                     [&](int x, int y) { return tile_cost(a.prob[x]) > tile_cost(a.prob[y]); });
     std::vector<std::vector<uint16_t>> lists(units);
-    using Slot = std::pair<long long, int>;   // (load, cluster)
+    using Slot = std::pair<double, int>;   // (load, cluster)
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
     for (int u = 0; u < units; ++u) heap.push({0, u});
     for (int oi = 0; oi < a.num_problems; ++oi) {
@@ -227,7 +235,7 @@ bool build_schedule(ScheduledArgs& a, int units) {
             Slot s = heap.top();
             heap.pop();
             lists[s.second].push_back((uint16_t)(p.tile_begin + t));
-            heap.push({s.first + tile_work(p), s.second});
+            heap.push({s.first + tile_cost(p), s.second});
         }
     }
     int off = 0;
@@ -640,7 +648,7 @@ bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg, bool wide = fa
     if (!encode_operand(&a.b[q], g.B, g.N, g.K, g.b_mn, BN / cg, &b3d)) return false;
     if (!encode_out_2d(&a.o0[q], g.C, g.M, g.N)) return false;
     const int64_t tile_n = wide ? 2 * BN : BN;
-    a.prob[q] = make_problem(g.M, g.N, g.K, (g.N + tile_n - 1) / tile_n, g.a_mn, g.b_mn, cg);
+    a.prob[q] = make_problem(g.M, g.N, g.K, (g.N + tile_n - 1) / tile_n, g.a_mn, g.b_mn, cg, wide ? 2 : 1);
     a.prob[q].a3d = a3d ? 1 : 0;
     a.prob[q].b3d = b3d ? 1 : 0;
     if (g.R) {
@@ -651,6 +659,53 @@ bool add_problem(KernelArgs& a, int q, const GemmSpec& g, int cg, bool wide = fa
     return true;
 }
 
+// Rows of a single GEMM in 256 x 512 tiles (K-major A) to keep in those tiles when the rows
+// after them run as 256 x 256 tiles in the same launch: with few wide tiles per CTA pair the
+// last round of a launch of wide tiles can be nearly empty (the target block's down
+// projection: 308 tiles = 4.05 rounds over 76 pairs), and narrow tiles fill it.  The rows
+// (all of M, or a multiple of 256) whose longest-first schedule has the shortest makespan in
+// tile_cost units; 0 when plain 256 x 256 tiles do best.  Cached per shape and thread.
+int64_t wide_rows(DeviceState* st, int64_t M, int64_t N, int64_t K) {
+    const int units = cluster_slots<EPI_STORE_W, 2, SRC_PARAMS>(st);
+    const int64_t tm = (M + 2 * BM - 1) / (2 * BM), tn_n = (N + BN - 1) / BN, tn_w = (N + 2 * BN - 1) / (2 * BN);
+    if (units <= 0 || units > MAX_CLUSTERS || tm * tn_w >= 8LL * units || tm * tn_n > MAX_SCHED) return M;
+    struct Entry {
+        int64_t M, N, K;
+        int units;
+        int64_t rows;
+    };
+    thread_local std::vector<Entry> cache;
+    for (const Entry& e : cache)
+        if (e.M == M && e.N == N && e.K == K && e.units == units) return e.rows;
+    const double kb = (double)((K + BK - 1) / BK);
+    const double cw = 2.0 * kb / kWideGain + kWideDrain, cn = kb;
+    double best = 0;
+    int64_t best_a = tm;
+    for (int64_t a = tm; a >= 0 && a >= tm - 16; --a) {
+        std::priority_queue<double, std::vector<double>, std::greater<double>> load;
+        for (int u = 0; u < units; ++u) load.push(0.0);
+        auto put = [&](double c, int64_t n) {
+            for (int64_t i = 0; i < n; ++i) {
+                const double l = load.top();
+                load.pop();
+                load.push(l + c);
+            }
+        };
+        put(cw, a * tn_w);       // longest tiles first, as build_schedule does
+        put(cn, (tm - a) * tn_n);
+        double ms = 0;
+        for (; !load.empty(); load.pop()) ms = std::max(ms, load.top());
+        if (a == tm || ms < best * (1 - 1e-9)) {
+            best = ms;
+            best_a = a;
+        }
+    }
+    const int64_t rows = best_a >= tm ? M : best_a * 2 * BM;
+    if (cache.size() >= 64) cache.erase(cache.begin());
+    cache.push_back(Entry{M, N, K, units, rows});
+    return rows;
+}
+
 // One plain GEMM, optionally with a residual added in its epilogue.
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
                        int64_t K, bool a_mn, bool b_mn, cudaStream_t s, const void* R = nullptr) {
@@ -659,7 +714,22 @@ swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, 
     std::memset(&a, 0, sizeof a);
     GemmSpec g{A, B, Cp, M, N, K, a_mn, b_mn};
     g.R = R;
-    const bool wide = !R && cg == 2 && wide_pays(st, &g, 1, WIDE_LONG_K);
+    bool wide = !R && cg == 2 && wide_pays(st, &g, 1, WIDE_LONG_K);
+    const int64_t rows = wide && !a_mn && !(g_debug_flags.load() & DEBUG_WIDE_TILES) ? wide_rows(st, M, N, K) : M;
+    if (rows == 0) wide = false;
+    if (wide && rows < M) {
+        // the first `rows` rows in 256 x 512 tiles, the rest in 256 x 256 tiles, one launch
+        static thread_local ScheduledArgs sa;
+        std::memset(static_cast<KernelArgs*>(&sa), 0, sizeof(KernelArgs));
+        const GemmSpec g1{static_cast<const uint8_t*>(A) + rows * K * 2, B, static_cast<uint8_t*>(Cp) + rows * N * 2,
+                          M - rows, N, K, a_mn, b_mn};
+        GemmSpec g0 = g;
+        g0.M = rows;
+        if (!add_problem(sa, 0, g0, 2, true) || !add_problem(sa, 1, g1, 2, false))
+            return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
+        sa.num_problems = 2;
+        return launch<EPI_STORE_W, 2, SRC_PARAMS>(st, kind, sa, s);
+    }
     if (!add_problem(a, 0, g, cg, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
     a.num_problems = 1;
     if (R) {
@@ -1259,17 +1329,17 @@ swiglu_status launch_table(DeviceState* st, int kind, std::vector<TableEntry>& e
     if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
     const int units = (int)std::min<long long>(tiles, std::min(slots, kMaxUnits));
 
-    // longest-processing-time: problems by decreasing work, each tile to the least-loaded
-    // cluster (a tile costs its work plus one per accumulator slot for its epilogue)
-    auto cost = [&](const Problem& p) { return tile_work(p) + tile_work(p) / p.k_blocks; };
+    // longest-processing-time: problems by decreasing tile time, each tile to the least-loaded
+    // cluster (a tile costs its mainloop plus one k-block time per accumulator slot for its epilogue)
+    auto cost = [&](const Problem& p) { return tile_cost(p) + p.slots; };
     std::vector<int> order(n);
     for (int i = 0; i < n; ++i) order[i] = i;
     std::stable_sort(order.begin(), order.end(),
                      [&](int a, int b) { return cost(ents[a].prob) > cost(ents[b].prob); });
     std::vector<std::vector<int>> lists(units);
-    using Slot = std::pair<long long, int>;
+    using Slot = std::pair<double, int>;
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-    for (int u = 0; u < units; ++u) heap.push({0, u});
+    for (int u = 0; u < units; ++u) heap.push({0.0, u});
     for (int pi : order) {
         const Problem& p = ents[pi].prob;
         const int nt = p.tiles_m * p.tiles_n;
@@ -1381,7 +1451,7 @@ bool fill_gemm(TableEntry& t, const GemmSpec& g, int cg, bool wide = false) {
     if (!encode_operand(&t.b, g.B, g.N, g.K, g.b_mn, BN / cg, &b3d)) return false;
     if (!encode_out_2d(&t.o0, g.C, g.M, g.N)) return false;
     const int64_t tile_n = wide ? 2 * BN : BN;
-    t.prob = make_problem(g.M, g.N, g.K, (g.N + tile_n - 1) / tile_n, g.a_mn, g.b_mn, cg);
+    t.prob = make_problem(g.M, g.N, g.K, (g.N + tile_n - 1) / tile_n, g.a_mn, g.b_mn, cg, wide ? 2 : 1);
     t.prob.a3d = a3d ? 1 : 0;
     t.prob.b3d = b3d ? 1 : 0;
     return true;
