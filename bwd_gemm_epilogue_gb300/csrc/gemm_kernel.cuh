@@ -38,6 +38,7 @@
 //                   256 x 256 tile.  The accumulators form a ring of two 256-column
 //                   slots: a tile takes two slots (one at a ragged N edge), the epilogue
 //                   drains and returns them one at a time.
+//   EPI_STORE_ADD_W EPI_STORE_ADD over 256 x 512 tiles (the residual block's grouped backward).
 //   EPI_SWIGLU_FWD  B holds two W1 row slabs, [j0, j0+128) and [H+j0, H+j0+128), so
 //                   accumulator columns [0,128) are `left` and [128,256) the matching
 //                   `gate`.  Stores preact (both halves, bf16) and
@@ -75,7 +76,9 @@
 
 namespace swiglu {
 
-enum EpiKind : int { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_STORE_ADD = 3, EPI_STORE_W = 4 };
+enum EpiKind : int {
+    EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2, EPI_STORE_ADD = 3, EPI_STORE_W = 4, EPI_STORE_ADD_W = 5
+};
 
 // Operand type of the MMAs: bf16 (kind::f16) or FP8 E4M3 (kind::f8f6f4).  Both fill a
 // 128-byte swizzle row per k-block -- 64 bf16 or 128 FP8 values -- so the stage
@@ -193,14 +196,15 @@ struct Cfg {
     // 8 KB slot per epilogue warp, which leaves room for six operand stages (CTA pairs).
     static constexpr int CK = EPI == EPI_SWIGLU_BWD ? 16 : CHUNK;   // epilogue columns per chunk
     // 256 x 512 tiles (EPI_STORE_W): two 256-column accumulator slots per tile
-    static constexpr bool WIDE = EPI == EPI_STORE_W;
+    static constexpr bool WIDE = EPI == EPI_STORE_W || EPI == EPI_STORE_ADD_W;
+    static constexpr bool ADD = EPI == EPI_STORE_ADD || EPI == EPI_STORE_ADD_W;   // residual-add store
     static_assert(!WIDE || CG == 2, "256 x 512 tiles are CTA-pair tiles");
     static constexpr int SLOTS = WIDE ? 2 : 1;
     static constexpr int STAGES =
         WIDE ? 4
              : CG == 1 ? ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) ? 4 : 3)
                        : ((EPI == EPI_STORE || EPI == EPI_SWIGLU_BWD) ? 6 : 5);
-    static constexpr bool STORE_ONLY = EPI == EPI_STORE || EPI == EPI_STORE_ADD || WIDE;   // one bf16 output
+    static constexpr bool STORE_ONLY = EPI == EPI_STORE || ADD || WIDE;   // one bf16 output
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_ROWS = BN / CG;                        // B rows (N) per slot held by this CTA
     static constexpr int B_SLOT_BYTES = B_ROWS * BK * 2;
@@ -217,10 +221,12 @@ struct Cfg {
     // one slot of two 32 x PRE_COLS tiles that first receive their preact chunk (left, gate)
     // and then stage its outputs (dleft, dgate, then h in the first tile)
     static constexpr int OUT_TILE = 32 * (BWD ? PRE_COLS : CK) * 2;
-    static constexpr int OUT_BUFS = (BWD || !(EPI == EPI_SWIGLU_FWD && CG == 1)) ? 2 : 1;
+    // (single-buffered for 256 x 512 residual tiles: 4 stages of 48 KB + the residual slots
+    // leave room for no more)
+    static constexpr int OUT_BUFS = (EPI == EPI_STORE_ADD_W || (EPI == EPI_SWIGLU_FWD && CG == 1)) ? 1 : 2;
     static constexpr int OUT_WARP_BYTES = OUT_BUFS * NOUT * OUT_TILE;
     // epilogue-input slots of the residual (STORE_ADD): 128 rows x CK cols bf16
-    static constexpr int EIN_SLOTS = EPI == EPI_STORE_ADD ? 2 : 0;
+    static constexpr int EIN_SLOTS = ADD ? 2 : 0;
     static constexpr int EIN_SLOT_BYTES = BM * CK * 2;
     static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CK : BN / CK;
 
@@ -519,7 +525,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 }
             }
             if (!C::STORE_ONLY) ptx::prefetch_tmap(&args.o1);
-            if (EPI == EPI_SWIGLU_BWD || EPI == EPI_STORE_ADD) ptx::prefetch_tmap(&args.i0);
+            if (EPI == EPI_SWIGLU_BWD || C::ADD) ptx::prefetch_tmap(&args.i0);
         }
     }
     if (warp == 1) {
@@ -748,9 +754,9 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------------ epilogue-input producer
-        if (EPI == EPI_STORE_ADD && lane == 0) {
+        if (C::ADD && lane == 0) {
             // the residual [M, N] tiles of the problems that carry one, 128 rows x 32 columns
-            // per chunk, in the order the epilogue warps consume them
+            // per chunk, slot by slot, in the order the epilogue warps consume them
             int slot = 0;
             uint32_t phase = 0;
             int last_parity[C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1];
@@ -769,19 +775,22 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 int tm, tn;
                 tile_coords(pr, lt, tm, tn);
                 const int m0 = tm * (BM * CG) + BM * (int)rank;
-                const int n0 = tn * BN;
-                for (int c = 0; c < C::CHUNKS; ++c) {
-                    if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, tmo, err, abort_flag, ERR_AUX)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = ein_full_bar(slot);
-                    ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
-                    last_parity[slot] = (int)phase;
-                    ptx::tma_load_2d(base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES, mI, fb, n0 + c * CHUNK, m0);
-                    if (++slot == C::EIN_SLOTS) {
-                        slot = 0;
-                        phase ^= 1u;
+                const int w = tile_slots<C>(pr, tn);
+                for (int j = 0; j < w && ok; ++j) {
+                    const int n0 = tn * tile_cols<C>(pr) + j * BN;
+                    for (int c = 0; c < C::CHUNKS; ++c) {
+                        if (!wait_bounded(ein_empty_bar(slot), phase ^ 1u, tmo, err, abort_flag, ERR_AUX)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = ein_full_bar(slot);
+                        ptx::mbar_arrive_expect_tx(fb, C::EIN_SLOT_BYTES);
+                        last_parity[slot] = (int)phase;
+                        ptx::tma_load_2d(base + C::OFF_EIN + slot * C::EIN_SLOT_BYTES, mI, fb, n0 + c * CHUNK, m0);
+                        if (++slot == C::EIN_SLOTS) {
+                            slot = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
             }
@@ -957,7 +966,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
         const int grp = (warp - EPI_WARP0) >> 2; // which of the quadrant's warps (store-only: 0 or 1)
         constexpr int GROUPS = C::EPI_WARPS / 4;
         const uint32_t out_base = base + C::OFF_OUT + (warp - EPI_WARP0) * C::OUT_WARP_BYTES;
-        int res_tiles = 0;   // EPI_STORE_ADD: residual tiles drained so far (slot bookkeeping)
+        int res_slots = 0;   // residual-add stores: accumulator slots of residual problems drained so far
         int ob = 0;
         uint32_t slot_seq = 0;   // accumulator slots drained so far
         bool ok = true;
@@ -995,7 +1004,8 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 ptx::tc_fence_after();
                 const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
 
-                if constexpr ((EPI == EPI_STORE || EPI == EPI_STORE_W) && OP == OP_BF16) {
+                constexpr bool FAST = (EPI == EPI_STORE || EPI == EPI_STORE_W || EPI == EPI_STORE_ADD_W) && OP == OP_BF16;
+                if (FAST && !(C::ADD && pr.res)) {
                     // Plain bf16 stores: all of this warp's chunks of the slot into registers as
                     // packed bf16 first, then the slot goes back to the MMA warp, then the
                     // stores.  A 256 x 512 tile's next mainloop waits for its slots' release.
@@ -1058,9 +1068,9 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
 
                     // epilogue input of the residual store: the residual's 32 columns
                     uint32_t lft[16];
-                    if (EPI == EPI_STORE_ADD && pr.res) {
+                    if (C::ADD && pr.res) {
                         constexpr int NSLOT = C::EIN_SLOTS > 0 ? C::EIN_SLOTS : 1;
-                        const int q = res_tiles * C::CHUNKS + c;
+                        const int q = res_slots * C::CHUNKS + c;
                         const int slot = q % NSLOT;
                         const bool in_ok = __all_sync(0xffffffffu, wait_bounded(ein_full_bar(slot),
                                                                                 (uint32_t)((q / NSLOT) & 1), tmo,
@@ -1090,11 +1100,11 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                             if (EPI == EPI_SWIGLU_FWD) acc2[i] = __float_as_uint(__uint_as_float(acc2[i]) * sa);
                         }
                     }
-                    if (EPI == EPI_STORE || EPI == EPI_STORE_W || (EPI == EPI_STORE_ADD && !pr.res)) {
+                    if (EPI == EPI_STORE || EPI == EPI_STORE_W || (C::ADD && !pr.res)) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             o0[i] = pack_bf16(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
-                    } else if (EPI == EPI_STORE_ADD) {
+                    } else if (C::ADD) {
                         // residual add: C = acc + R, summed in fp32 and rounded once
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -1168,9 +1178,10 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     ob = (ob + 1) % C::OUT_BUFS;
                 }
                 }
+                if (C::ADD && pr.res) ++res_slots;
             }
             slot_seq += (uint32_t)w;
-            if (EPI == EPI_STORE_ADD && pr.res) ++res_tiles;
+
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
         ptx::tc_fence_before();

@@ -752,10 +752,11 @@ swiglu_status run_gemm_group(DeviceState* st, int kind, const GemmSpec* g, int n
         if (g[q].R && res) return fail(SWIGLU_ERR_INVALID_ARG, "group: more than one residual");
         res = res || g[q].R != nullptr;
     }
-    const bool wide = !res && wide_pays(st, g, n, WIDE_GROUP);
+    const bool wide = wide_pays(st, g, n, WIDE_GROUP);
     for (int q = 0; q < n; ++q)
         if (!add_problem(a, q, g[q], 2, wide)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (group)");
     a.num_problems = n;
+    if (res && wide) return launch<EPI_STORE_ADD_W, 2, SRC_PARAMS>(st, kind, a, s);
     if (res) return launch<EPI_STORE_ADD, 2, SRC_PARAMS>(st, kind, a, s);
     if (wide) return launch<EPI_STORE_W, 2, SRC_PARAMS>(st, kind, a, s);
     return launch<EPI_STORE, 2, SRC_PARAMS>(st, kind, a, s);

@@ -86,14 +86,29 @@ def test_block_with_wide_tiles_matches_oracle_and_narrow_bits(b, s):
     parity(dW2, dW2_ref, "dW2")
 
 
-def test_wide_tiles_residual_block_falls_back_to_narrow(b):
-    # the residual epilogue keeps 256 x 256 tiles; forcing wide tiles changes nothing there
-    s = Shape(300, 256, 512, 256)
+@pytest.mark.parametrize("s", [Shape(300, 256, 520, 256), Shape(1000, 256, 768, 256)],
+                         ids=lambda s: f"M{s.M}_D{s.D}_H{s.H}")
+def test_residual_block_with_wide_tiles(b, s):
+    # The residual block: its backward group adds dy into dx in the residual epilogue, in
+    # 256 x 512 tiles when forced (the single residual down projection keeps 256 x 256).
     _, x, W1, W2, dy = workloads.make_block(s, seed=62)
-    xd, W1d, W2d = dev(x), dev(W1), dev(W2)
-    y0 = with_flags(b, NARROW, lambda: b.swiglu_mlp_fwd(xd, W1d, W2d, residual=True))[1]
-    y1 = with_flags(b, WIDE, lambda: b.swiglu_mlp_fwd(xd, W1d, W2d, residual=True))[1]
-    assert torch.equal(y0, y1)
+    p_ref, _, y_ref = oracle.fwd(x, W1, W2, residual=True)
+    pre = torch.from_numpy(p_ref).to(torch.bfloat16)
+    _, _, _, dx_ref, dW1_ref, dW2_ref = oracle.bwd_full(x, W1, W2, pre, dy, residual=True)
+    xd, W1d, W2d, dyd, pred = dev(x), dev(W1), dev(W2), dev(dy), dev(pre)
+    res = {}
+    for name, flags in (("narrow", NARROW), ("wide", WIDE), ("wide, three launches", WIDE | 4)):
+        fwd = with_flags(b, flags, lambda: b.swiglu_mlp_fwd(xd, W1d, W2d, residual=True))
+        bwd = with_flags(b, flags, lambda: b.swiglu_mlp_bwd(xd, W1d, W2d, pred, dyd, residual=True))
+        res[name] = fwd + bwd
+    for name in ("wide", "wide, three launches"):
+        for u, v, what in zip(res["narrow"], res[name], ("preact", "y", "dx", "dW1", "dW2")):
+            assert torch.equal(u, v), f"{what} (residual): {name} tiles differ from narrow tiles"
+    _, y, dx, dW1, dW2 = res["wide"]
+    parity(y, y_ref, "y (residual)")
+    parity(dx, dx_ref, "dx (residual, wide tiles)")
+    parity(dW1, dW1_ref, "dW1 (residual block, wide tiles)")
+    parity(dW2, dW2_ref, "dW2 (residual block, wide tiles)")
 
 
 def test_wide_tile_wait_times_out_and_context_survives(b):
