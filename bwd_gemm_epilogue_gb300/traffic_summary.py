@@ -1,12 +1,13 @@
 """Turn ncu CSVs of DRAM counters into profiles/traffic.json for bench.py.
 
-    python -m bwd_gemm_epilogue_gb300.traffic_summary "<how the CSVs were taken>" a.csv [b.csv ...]
+    python -m bwd_gemm_epilogue_gb300.traffic_summary "<how the CSVs were taken>" [kind=]a.csv [[kind=]b.csv ...]
 
 Each CSV comes from one ncu capture of `--metrics dram__bytes_read.sum,
 dram__bytes_write.sum,gpu__time_duration.sum` (one pass) on one or more launches of the
 target block's kernels.  Launches are mapped to kernel kinds by their template arguments
-(gemm_kernel<EPI, CG, SCHED, OP>, bf16 operands; plain or demangled kernel names),
-averaged per kind, and written with a hash of the kernel sources: bench.py reports a
+(gemm_kernel<EPI, CG, SCHED, OP>, bf16 operands; plain or demangled kernel names) unless
+the argument names the kind (`fwd_down=dram_fwd_down.csv`: the down projection and the grouped
+backward can both run as <4, 2, 1, 0>, a list launch of 256 x 512 tiles), averaged per kind, and written with a hash of the kernel sources: bench.py reports a
 kind's traffic only while the sources still hash the same (a changed kernel invalidates
 its counters).
 """
@@ -28,7 +29,7 @@ KINDS = {("1", "2", "0"): "fwd_preact", ("0", "2", "0"): "fwd_down", ("2", "2", 
          ("0", "2", "1"): "bwd_gemms", ("4", "2", "1"): "bwd_gemms", ("4", "2", "0"): "fwd_down"}
 
 
-def summarize(path: str) -> dict:
+def summarize(path: str, kind: str | None = None) -> dict:
     rows = list(csv.reader(open(path)))
     hi = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
     h = rows[hi]
@@ -40,9 +41,9 @@ def summarize(path: str) -> dict:
             continue
         m = re.search(r"gemm_kernel<(?:\(int\))?(\d+), (?:\(int\))?(\d+), (?:\(int\))?(\d+)(?:, (?:\(int\))?(\d+))?>",
                       r[ki])
-        if not m or m.group(4) not in (None, "0") or m.groups()[:3] not in KINDS:
+        if not m or m.group(4) not in (None, "0") or (kind is None and m.groups()[:3] not in KINDS):
             continue
-        d = per_launch.setdefault(r[ii], {"kind": KINDS[m.groups()[:3]]})
+        d = per_launch.setdefault(r[ii], {"kind": kind or KINDS[m.groups()[:3]]})
         d[r[mi]] = float(r[vi].replace(",", "")) * scale.get(r[ui], 1)
     acc = {}
     for d in per_launch.values():
@@ -61,8 +62,9 @@ def main():
     import bench
     command, paths = sys.argv[1], sys.argv[2:]
     kernels = {}
-    for path in paths:
-        kernels.update(summarize(path))
+    for arg in paths:
+        kind, sep, path = arg.partition("=")
+        kernels.update(summarize(path, kind) if sep else summarize(arg))
     out = {"source_hash": bench.kernel_source_hash(), "command": command,
            "workload": "target step: M=11136, D=Dout=3584, H=14336", "kernels": kernels}
     dst = os.path.join(ROOT, "profiles", "traffic.json")
