@@ -152,11 +152,12 @@ def test_moe_layer_with_wide_tiles_matches_narrow_bits(b, case):
             parity(res["wide"][4][e], dW2_ref[e], f"dW2[{e}], wide tiles ({case})")
 
 
-@pytest.mark.parametrize("M,N,K", [(5568, 3584, 7168), (11136, 3584, 14336)], ids=lambda v: str(v))
+@pytest.mark.parametrize("M,N,K", [(5568, 3584, 7168), (11136, 3584, 14336), (2816, 3848, 6400)], ids=lambda v: str(v))
 def test_mixed_tile_widths_in_one_launch(b, M, N, K):
     # A long-K product with few 256 x 512 tiles per CTA pair: the library keeps its first rows
     # in 256 x 512 tiles and runs the last row tiles as 256 x 256 tiles in the same launch
-    # (for these shapes: rows 0..5375 / 0..11007 wide).  Bits as with 256 x 256 tiles only,
+    # (for these shapes: rows 0..5375 / 0..11007 / 0..2303 wide; the last N ends 8 columns into a
+    # tile's second slot and into a 256 x 256 tile).  Bits as with 256 x 256 tiles only,
     # rows on both sides of the split against the fp64 product.
     g = torch.Generator().manual_seed(M + N + K)
     A = (torch.randn(M, K, generator=g) * K ** -0.25).to(torch.bfloat16)
@@ -165,7 +166,7 @@ def test_mixed_tile_widths_in_one_launch(b, M, N, K):
     c_auto = with_flags(b, 0, lambda: b.swiglu_mlp_gemm_bf16(Ad, Bd, M, N, K, False, False))
     c_narrow = with_flags(b, NARROW, lambda: b.swiglu_mlp_gemm_bf16(Ad, Bd, M, N, K, False, False))
     assert torch.equal(c_auto, c_narrow)
-    split = {5568: 5376, 11136: 11008}[M]
+    split = {5568: 5376, 11136: 11008, 2816: 2304}[M]
     rows = torch.tensor(sorted({0, 255, 256, split - 257, split - 1, split, split + 1, M - 1, M // 2}))
     ref = A[rows].double() @ B.double().T
     parity(c_auto[rows.cuda()], ref.numpy(), "C rows around the split")
