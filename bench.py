@@ -48,14 +48,17 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["target", "prefill", "decode", "stack4", "moe8", "moe64",
-                                           "fp8_target", "fp8_prefill", "fp8_decode"],
+                                           "fp8_target", "fp8_prefill", "fp8_decode", "tp2"],
                     default="target",
                     help="target: the block at the pages' target shape (the headline line); "
                          "prefill / decode: the 4096- and 16-token LLaMA-7B-shaped blocks; "
                          "stack4: four target blocks trained end to end (with memory); "
                          "moe8 / moe64: mixture-of-experts layers, grouped launches over the experts; "
                          "fp8_*: the FP8 forward (E4M3, quantising epilogue) at the target / prefill / "
-                         "decode shapes, with the bf16 forward timed beside it")
+                         "decode shapes, with the bf16 forward timed beside it; "
+                         "tp2: one rank's shard of the target block split over two tensor-parallel "
+                         "ranks (its chunked forward and evented backward against the same shard in "
+                         "one piece; the reductions need a second GPU)")
     ap.add_argument("--residual", action="store_true",
                     help="time the residual block y = x + MLP(x) (residual-add epilogues; D == Dout)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -633,6 +636,83 @@ def run_stack(args):
         "gpu_launches_per_step": 4 * (2 + 2), "clocks": clk}), flush=True)
 
 
+def run_tp2(args):
+    """One rank's compute of the target block split over two tensor-parallel ranks: the
+    shard's forward with the down projection in row chunks (a CUDA event per chunk, where a
+    communication stream would start each chunk's reduction) and backward with dx first (its
+    event), against the same shard through the one-piece entry points, in alternating blocks.
+    The reductions themselves need the second rank's GPU and are not timed here."""
+    import torch
+
+    from bwd_gemm_epilogue_gb300 import binding, ledger, workloads
+    from bwd_gemm_epilogue_gb300.tensor_parallel import shard_bounds
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s, x_h, W1_h, W2_h, dy_h = workloads.make_block("target")
+    world, n_chunks = 2, 4
+    j0, Hs = shard_bounds(s.H, world, 0)
+    x, dy = x_h.to(dev), dy_h.to(dev)
+    W1s, W2s = binding.swiglu_mlp_tp_shard_pack(W1_h.to(dev), W2_h.to(dev), j0, Hs)
+    M, D, Do = s.M, s.D, s.Dout
+    preact = torch.empty(M, 2 * Hs, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(M, Do, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty(M, D, dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty(2 * Hs, D, dtype=torch.bfloat16, device=dev)
+    dW2 = torch.empty(Do, Hs, dtype=torch.bfloat16, device=dev)
+    ws_f = torch.empty(binding.swiglu_mlp_fwd_workspace_size(M, D, Hs, Do), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(binding.swiglu_mlp_bwd_workspace_size(M, D, Hs, Do), dtype=torch.uint8, device=dev)
+    events = [torch.cuda.Event() for _ in range(n_chunks)]
+    dx_ev = torch.cuda.Event()
+
+    def step_tp():
+        binding.swiglu_mlp_tp_fwd(x, W1s, W2s, preact, y, ws_f, n_chunks=n_chunks, chunk_events=events)
+        binding.swiglu_mlp_tp_bwd(x, W1s, W2s, preact, dy, dx, dW1, dW2, ws_b, dx_event=dx_ev)
+
+    def step_plain():
+        binding.swiglu_mlp_fwd(x, W1s, W2s, preact, y, ws_f)
+        binding.swiglu_mlp_bwd(x, W1s, W2s, preact, dy, dx, dW1, dW2, ws_b)
+
+    for _ in range(args.warmup):
+        step_tp()
+        step_plain()
+    torch.cuda.synchronize(dev)
+    blocks, per = 6, max(1, args.steps // 12)
+    t_tp, t_plain = [], []
+    clocks = ClockSampler(dev.index)
+    for b in range(blocks):
+        for name in (("tp", "plain") if b % 2 == 0 else ("plain", "tp")):
+            fn = step_tp if name == "tp" else step_plain
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(per):
+                fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            (t_tp if name == "tp" else t_plain).append(e0.elapsed_time(e1) / per)
+    clk = clocks.stop()
+    if binding.swiglu_mlp_device_status(dev) != 0:
+        raise RuntimeError("tensor-parallel shard steps failed")
+    ms_tp, ms_plain = sum(t_tp) / len(t_tp), sum(t_plain) / len(t_plain)
+    flops = ledger.gemm_flops(M, D, Hs, Do)["step"]
+    ring = 2 * (world - 1) / world   # bytes a ring all-reduce sends per byte of the summed tensor
+    print(json.dumps({
+        "metric": "SwiGLU MLP tensor-parallel shard fwd+bwd TFLOP/s (bf16, one of 2 ranks of 11136x3584x14336)",
+        "value": round(flops / (ms_tp * 1e-3) / 1e12, 1), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": per * blocks, "warmup": args.warmup, "ms_per_step": round(ms_tp, 4), "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"tp2: rank 0 of 2, hidden units [{j0}, {j0 + Hs}) of H={s.H}; M={M} D={D} "
+                               f"Dout={Do}; forward in {n_chunks} row chunks with events, backward dx first "
+                               f"with an event"},
+        "one_piece_ms_per_step": round(ms_plain, 4),
+        "chunking_cost": round(ms_tp / ms_plain - 1.0, 4),
+        "reductions": {"measured": False,
+                       "why": "the partial y and dx are summed across the ranks' GPUs; every run here has one GPU",
+                       "bytes_summed_per_step": 2 * M * (Do + D),
+                       "ring_all_reduce_bytes_sent_per_rank": round(ring * 2 * M * (Do + D))},
+        "gpu_launches_per_step": 1 + n_chunks + 3, "clocks": clk}), flush=True)
+
+
 def run_moe(args):
     """A mixture-of-experts layer (tokens grouped by expert): forward + backward of
     every expert, each step one grouped launch over all experts."""
@@ -829,6 +909,8 @@ def main():
         run_moe(args)
     elif args.workload.startswith("fp8_"):
         run_fp8(args)
+    elif args.workload == "tp2":
+        run_tp2(args)
     else:
         run_ours(args)
 
