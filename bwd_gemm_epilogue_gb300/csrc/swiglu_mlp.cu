@@ -599,11 +599,11 @@ struct GemmSpec {
 //                                   down projection 130 -> 135 us)
 // The backward's dW2 / dx / dW1 group, longest-first over the parameter block: wide if there
 // are at least kWideMinClusterKBlocks k-block times of work per CTA pair, at least
-// kWideMinKBlocks per 256 x 256 tile on average, and the longest wide tile fits the even
-// share.  The same group over a table of experts: wide tiles always (half the tiles means
+// kWideMinKBlocks per 256 x 256 tile on average (the 4096-token block's group, mostly tiles of
+// 64 k-blocks, is not), and the longest wide tile fits the even share.  The same group over a table of experts: wide tiles always (half the tiles means
 // half the per-tile problem switches, which cost more there than the slot reads).
-constexpr double kWideMinKBlocks = 24;
-constexpr double kWideMinClusterKBlocks = 4000;
+constexpr double kWideMinKBlocks = 100;
+constexpr double kWideMinClusterKBlocks = 2000;
 // Down projections and other single products: wide if their reduction is long (at least
 // kWideMinKBlocksLong k-blocks per tile, so the exposed slot reads stay near 1 % of a tile)
 // and the wide tiles still fill every CTA pair once.
