@@ -1095,6 +1095,41 @@ swiglu_status swiglu_mlp_tp_shard_unpack_grads(const void* dW1_shard, const void
     return e == cudaSuccess ? SWIGLU_OK : fail(SWIGLU_ERR_CUDA, "swiglu_mlp_tp_shard_unpack_grads: copy", e);
 }
 
+}  // extern "C"
+
+namespace swiglu {
+namespace {
+// This thread's second stream on the current device, with an event to fork work onto it and
+// one to join it back (per thread, so concurrent callers never share them).
+swiglu_status side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join) {
+    struct Side {
+        cudaStream_t s = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+    };
+    thread_local Side per_dev[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_CUDA, "cudaGetDevice", e);
+    Side& d = per_dev[dev];
+    if (!d.s) {
+        e = cudaStreamCreateWithFlags(&d.s, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            d.s = nullptr;
+            return fail(SWIGLU_ERR_CUDA, "second stream for the chunked down projection", e);
+        }
+    }
+    *side = d.s;
+    *fork = d.fork;
+    *join = d.join;
+    return SWIGLU_OK;
+}
+}  // namespace
+}  // namespace swiglu
+
+extern "C" {
+
 swiglu_status swiglu_mlp_tp_fwd(const void* x, const void* W1_shard, const void* W2_shard, void* preact_shard,
                                 void* y_partial, int64_t M, int64_t D, int64_t Hs, int64_t Dout, int n_chunks,
                                 void* const* chunk_events, void* workspace, size_t workspace_bytes, void* stream) {
@@ -1132,21 +1167,35 @@ swiglu_status swiglu_mlp_tp_fwd(const void* x, const void* W1_shard, const void*
     rc = run_fwd_preact(st, x, W1_shard, preact_shard, h, M, D, Hs, s);   // every row: preact and h of the shard
     if (rc != SWIGLU_OK) return rc;
     // the down projection in row chunks of whole 256-row tiles; chunk c's partial y is
-    // complete when chunk_events[c] fires
+    // complete when chunk_events[c] fires.  Chunks alternate between the caller's stream and
+    // a second stream of this thread, so that each chunk's CTA pairs start on the SMs the
+    // previous chunk's last round leaves idle (one launch per chunk would otherwise end in a
+    // part-empty round each); the caller's stream waits for the second one at the end.
+    cudaStream_t side;
+    cudaEvent_t fork, join;
+    rc = side_stream(&side, &fork, &join);
+    if (rc != SWIGLU_OK) return rc;
+    cudaError_t e = cudaEventRecord(fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "swiglu_mlp_tp_fwd: fork onto the second stream", e);
     const int64_t per = ((M + n_chunks - 1) / n_chunks + 2 * BM - 1) / (2 * BM) * (2 * BM);
     for (int c = 0; c < n_chunks; ++c) {
+        cudaStream_t sc = (c & 1) ? side : s;
         const int64_t r0 = (int64_t)c * per;
         if (r0 < M) {
             const int64_t rows = std::min<int64_t>(per, M - r0);
             rc = run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h + (size_t)r0 * Hs * 2, W2_shard,
-                          static_cast<uint8_t*>(y_partial) + (size_t)r0 * Dout * 2, rows, Dout, Hs, false, false, s);
+                          static_cast<uint8_t*>(y_partial) + (size_t)r0 * Dout * 2, rows, Dout, Hs, false, false, sc);
             if (rc != SWIGLU_OK) return rc;
         }
         if (chunk_events) {
-            rc = record_event(chunk_events[c], s);
+            rc = record_event(chunk_events[c], sc);
             if (rc != SWIGLU_OK) return rc;
         }
     }
+    e = cudaEventRecord(join, side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, join, 0);
+    if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "swiglu_mlp_tp_fwd: join the second stream", e);
     return SWIGLU_OK;
 }
 
