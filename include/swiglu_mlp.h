@@ -210,10 +210,14 @@ swiglu_status swiglu_mlp_tp_shard_unpack_grads(const void* dW1_shard, const void
  * The down projection runs in n_chunks row chunks (1..1024) of
  * swiglu_mlp_tp_chunk_rows(M, n_chunks) rows (whole 256-row tiles; the last chunk may be
  * shorter or empty); when chunk_events is not NULL it holds n_chunks cudaEvent_t handles
- * (caller-owned) and event c is recorded on `stream` once rows of chunk c of y_partial
- * are final, so a communication stream can start reducing chunk c while chunk c+1 is
- * computed.  For M <= 64 (and n_chunks = 1) the forward runs in one piece and every event
- * is recorded at its end.
+ * (caller-owned) and event c is recorded once rows of chunk c of y_partial are final, so a
+ * communication stream can start reducing chunk c while chunk c+1 is computed.  With more
+ * than one chunk, odd chunks run on a second stream the library keeps for the calling
+ * thread (forked from `stream` after the first GEMM, joined back into `stream` before the
+ * call returns), so that each chunk starts on the SMs the previous one leaves idle; event c
+ * is recorded on the stream that computed chunk c, and work enqueued on `stream` after the
+ * call sees every chunk.  For M <= 64 (and n_chunks = 1) the forward runs in one piece on
+ * `stream` and every event is recorded at its end.
  */
 swiglu_status swiglu_mlp_tp_fwd(const void* x, const void* W1_shard, const void* W2_shard, void* preact_shard,
                                 void* y_partial, int64_t M, int64_t D, int64_t Hs, int64_t Dout, int n_chunks,
