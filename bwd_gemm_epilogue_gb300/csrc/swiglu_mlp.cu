@@ -827,9 +827,36 @@ static swiglu_status record_event(void* event, cudaStream_t s) {
     return e == cudaSuccess ? SWIGLU_OK : fail(SWIGLU_ERR_CUDA, "cudaEventRecord", e);
 }
 
+// This thread's second stream on the current device, with an event to fork work onto it and
+// one to join it back (per thread, so concurrent callers never share them).
+static swiglu_status side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join) {
+    struct Side {
+        cudaStream_t s = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+    };
+    thread_local Side per_dev[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_CUDA, "cudaGetDevice", e);
+    Side& d = per_dev[dev];
+    if (!d.s) {
+        e = cudaStreamCreateWithFlags(&d.s, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            d.s = nullptr;
+            return fail(SWIGLU_ERR_CUDA, "a second stream of the calling thread", e);
+        }
+    }
+    *side = d.s;
+    *fork = d.fork;
+    *join = d.join;
+    return SWIGLU_OK;
+}
+
 // dx_event (tensor-parallel backward): when set, dx is computed by a launch of its own and
-// the event is recorded after it, before the weight gradients' launch, so that a caller
-// can reduce dx across ranks while dW1 and dW2 are computed.
+// the event is recorded after it, while the weight gradients run beside it on a second
+// stream, so that a caller can reduce dx across ranks while dW1 and dW2 are computed.
 static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, const void* preact, const void* dy,
                               void* dx, void* dW1, void* dW2, int64_t M, int64_t D, int64_t H, int64_t Dout,
                               void* workspace, size_t workspace_bytes, void* stream, bool residual,
@@ -898,7 +925,17 @@ static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, con
     };
     if (residual) g[1].R = dy;
     if (dx_event) {
-        // dx first, on its own; then dW2 and dW1 (one launch when both use CTA pairs)
+        // dx in a launch of its own on `s`, the event after it; dW2 and dW1 (which do not read
+        // dx; one launch when both use CTA pairs) on a second stream of this thread, so that
+        // each launch's CTA pairs take the SMs the other one's last round leaves idle; `s`
+        // waits for the second stream before the call returns
+        cudaStream_t side;
+        cudaEvent_t fork, join;
+        rc = side_stream(&side, &fork, &join);
+        if (rc != SWIGLU_OK) return rc;
+        cudaError_t e = cudaEventRecord(fork, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "backward: fork onto the second stream", e);
         rc = run_gemm(st, SWIGLU_KERNEL_BWD_DX, g[1].A, g[1].B, g[1].C, g[1].M, g[1].N, g[1].K, false, true, s, g[1].R);
         if (rc != SWIGLU_OK) return rc;
         rc = record_event(dx_event, s);
@@ -907,11 +944,17 @@ static swiglu_status bwd_impl(const void* x, const void* W1, const void* W2, con
         int64_t wtiles = 0;
         for (const GemmSpec& q : wg) wtiles += ((q.M + 2 * BM - 1) / (2 * BM)) * ((q.N + BN - 1) / BN);
         if (!(g_debug_flags.load() & (DEBUG_UNGROUPED | DEBUG_FORCE_SINGLE_CTA)) && Dout > BM && 2 * H > BM &&
-            wtiles <= MAX_SCHED)
-            return run_gemm_group(st, SWIGLU_KERNEL_BWD_GEMMS, wg, 2, s);
-        rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, g[0].A, g[0].B, g[0].C, g[0].M, g[0].N, g[0].K, true, true, s);
-        if (rc != SWIGLU_OK) return rc;
-        return run_gemm(st, SWIGLU_KERNEL_BWD_DW1, g[2].A, g[2].B, g[2].C, g[2].M, g[2].N, g[2].K, true, true, s);
+            wtiles <= MAX_SCHED) {
+            rc = run_gemm_group(st, SWIGLU_KERNEL_BWD_GEMMS, wg, 2, side);
+        } else {
+            rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW2, g[0].A, g[0].B, g[0].C, g[0].M, g[0].N, g[0].K, true, true, side);
+            if (rc == SWIGLU_OK)
+                rc = run_gemm(st, SWIGLU_KERNEL_BWD_DW1, g[2].A, g[2].B, g[2].C, g[2].M, g[2].N, g[2].K, true, true, side);
+        }
+        e = cudaEventRecord(join, side);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, join, 0);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "backward: join the second stream", e);
+        return rc;
     }
     int64_t pair_tiles = 0;   // tiles of the grouped launch (256-row CTA-pair tiles)
     for (const GemmSpec& q : g) pair_tiles += ((q.M + 2 * BM - 1) / (2 * BM)) * ((q.N + BN - 1) / BN);
@@ -1094,41 +1137,6 @@ swiglu_status swiglu_mlp_tp_shard_unpack_grads(const void* dW1_shard, const void
                               (size_t)Hs * 2, (size_t)Dout, cudaMemcpyDeviceToDevice, s);
     return e == cudaSuccess ? SWIGLU_OK : fail(SWIGLU_ERR_CUDA, "swiglu_mlp_tp_shard_unpack_grads: copy", e);
 }
-
-}  // extern "C"
-
-namespace swiglu {
-namespace {
-// This thread's second stream on the current device, with an event to fork work onto it and
-// one to join it back (per thread, so concurrent callers never share them).
-swiglu_status side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join) {
-    struct Side {
-        cudaStream_t s = nullptr;
-        cudaEvent_t fork = nullptr, join = nullptr;
-    };
-    thread_local Side per_dev[kMaxDevices];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_CUDA, "cudaGetDevice", e);
-    Side& d = per_dev[dev];
-    if (!d.s) {
-        e = cudaStreamCreateWithFlags(&d.s, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) {
-            d.s = nullptr;
-            return fail(SWIGLU_ERR_CUDA, "second stream for the chunked down projection", e);
-        }
-    }
-    *side = d.s;
-    *fork = d.fork;
-    *join = d.join;
-    return SWIGLU_OK;
-}
-}  // namespace
-}  // namespace swiglu
-
-extern "C" {
 
 swiglu_status swiglu_mlp_tp_fwd(const void* x, const void* W1_shard, const void* W2_shard, void* preact_shard,
                                 void* y_partial, int64_t M, int64_t D, int64_t Hs, int64_t Dout, int n_chunks,

@@ -227,10 +227,12 @@ int64_t swiglu_mlp_tp_chunk_rows(int64_t M, int n_chunks);
 /*
  * Shard backward: dx_partial [M, D] = grad_preact_J @ W1_shard (a partial sum over the
  * ranks), dW1_shard [2*Hs, D] and dW2_shard [Dout, Hs] (complete).  When dx_event (a
- * caller-owned cudaEvent_t) is not NULL, dx is computed by a launch of its own and the
- * event is recorded on `stream` when dx_partial is final, before the launch that computes
- * dW1_shard and dW2_shard, so that dx can be reduced across the ranks meanwhile.  With
- * dx_event NULL this is swiglu_mlp_bwd on the shard.
+ * caller-owned cudaEvent_t) is not NULL, dx is computed by a launch of its own on `stream`
+ * and the event is recorded on `stream` when dx_partial is final, while dW1_shard and
+ * dW2_shard are computed beside it on a second stream the library keeps for the calling
+ * thread (forked from `stream` after the fused kernel, joined back into `stream` before the
+ * call returns), so that dx can be reduced across the ranks meanwhile.  With dx_event NULL
+ * this is swiglu_mlp_bwd on the shard.
  */
 swiglu_status swiglu_mlp_tp_bwd(const void* x, const void* W1_shard, const void* W2_shard, const void* preact_shard,
                                 const void* dy, void* dx_partial, void* dW1_shard, void* dW2_shard, int64_t M,
