@@ -206,3 +206,45 @@ def test_library_shard_outputs_reduced_by_two_gloo_ranks(b):
     for rank in range(2):
         parity(res[rank][0], y_ref, f"y on gloo rank {rank}")
         parity(res[rank][1], dx_ref, f"dx on gloo rank {rank}")
+
+
+def test_shard_calls_capture_into_a_cuda_graph(b):
+    # The chunked forward and the evented backward fork onto the library's second stream and
+    # join back; captured into a CUDA graph, their replays give the direct calls' bits.
+    s = Shape(1000, 256, 768, 320)
+    _, x, W1, W2, dy = workloads.make_block(s, seed=98)
+    xd, W1d, W2d, dyd = dev(x), dev(W1), dev(W2), dev(dy)
+    j0, Hs = shard_bounds(s.H, 2, 1)
+    W1s, W2s = b.swiglu_mlp_tp_shard_pack(W1d, W2d, j0, Hs)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    pre, y = torch.empty(s.M, 2 * Hs, **bf), torch.empty(s.M, s.Dout, **bf)
+    dx, dW1, dW2 = torch.empty(s.M, s.D, **bf), torch.empty(2 * Hs, s.D, **bf), torch.empty(s.Dout, Hs, **bf)
+    wsf = torch.empty(b.swiglu_mlp_fwd_workspace_size(s.M, s.D, Hs, s.Dout), dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(b.swiglu_mlp_bwd_workspace_size(s.M, s.D, Hs, s.Dout), dtype=torch.uint8, device="cuda")
+    events = [torch.cuda.Event() for _ in range(4)]
+    ev = torch.cuda.Event()
+
+    def step():
+        b.swiglu_mlp_tp_fwd(xd, W1s, W2s, pre, y, wsf, n_chunks=4, chunk_events=events)
+        b.swiglu_mlp_tp_bwd(xd, W1s, W2s, pre, dyd, dx, dW1, dW2, wsb, dx_event=ev)
+
+    step()
+    torch.cuda.synchronize()
+    assert b.swiglu_mlp_device_status() == 0
+    ref = [t.clone() for t in (pre, y, dx, dW1, dW2)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        step()
+    for t in (pre, y, dx, dW1, dW2):
+        t.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert b.swiglu_mlp_device_status() == 0
+    for name, got, want in zip(("preact", "y", "dx", "dW1", "dW2"), (pre, y, dx, dW1, dW2), ref):
+        assert torch.equal(got, want), name
