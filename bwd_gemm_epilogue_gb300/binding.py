@@ -51,6 +51,7 @@ SIGNATURES = {
     "swiglu_mlp_set_wait_timeout_ns": (None, [_u64]),
     "swiglu_mlp_set_debug_flags": (None, [_i32]),
     "swiglu_mlp_set_raster_band": (None, [_i32]),
+    "swiglu_mlp_split_plan": (_i32, [_i64, _i64, _i64, _i32, _vp, _i32]),
     "swiglu_mlp_trace_begin": (None, [_vp, _vp, _i32]),
     "swiglu_mlp_trace_end": (_i32, []),
     "swiglu_mlp_abi_version": (_i32, []),
@@ -194,6 +195,18 @@ def swiglu_mlp_set_debug_flags(flags: int) -> None:
 
 def swiglu_mlp_set_raster_band(n_tiles: int) -> None:
     lib().swiglu_mlp_set_raster_band(int(n_tiles))
+
+
+def swiglu_mlp_split_plan(M: int, N: int, K: int, units: int):
+    """Tile lists of the down projection with split tiles (host only): a list of
+    (pair, tile, first k-block, end k-block, split index or -1), or None where the
+    forward splits no tiles for this shape."""
+    n = int(lib().swiglu_mlp_split_plan(int(M), int(N), int(K), int(units), None, 0))
+    if n < 0:
+        return None
+    buf = (ctypes.c_int32 * (5 * max(n, 1)))()
+    lib().swiglu_mlp_split_plan(int(M), int(N), int(K), int(units), ctypes.cast(buf, ctypes.c_void_p), n)
+    return [tuple(buf[5 * i:5 * i + 5]) for i in range(n)]
 
 
 def swiglu_mlp_abi_version() -> int:

@@ -141,11 +141,36 @@ struct KernelArgs {
 // the host): cluster c runs tiles sched[sched_off[c] .. sched_off[c + 1]).
 constexpr int MAX_CLUSTERS = 128;
 constexpr int MAX_SCHED = 12288;
+
+// Split tiles (one GEMM in 256 x 512 tiles, EPI_STORE_W with a host list).  The last
+// tiles of such a launch may each be shared by two CTA pairs, one summing the tile's first
+// k-blocks (its prefix piece), the other the rest (its suffix piece), so that every pair
+// gets the same number of k-blocks.  A list entry with SCHED_PIECE set is such a piece: its
+// k-block range and split index are split[c][0] (the suffix piece of cluster c) or
+// split[c][1] (with SCHED_PIECE_PREFIX).  Each epilogue warp of each piece owns one
+// counter pair per accumulator slot, zero before the launch: the warp that arrives first
+// writes its fp32 sums to split_sums and raises the second word; the other adds them to
+// its own and stores the tile.  fp32 addition of two terms is commutative, so the result
+// does not depend on which piece arrives first.
+constexpr int MAX_SPLIT = 80;
+constexpr int SCHED_TILE_MASK = 0x3FFF, SCHED_PIECE_PREFIX = 0x4000, SCHED_PIECE = 0x8000;
+constexpr int SPLIT_WARPS = 8, SPLIT_COLS = 128;   // epilogue warps of EPI_STORE_W; columns per warp and slot
+constexpr int SPLIT_UNITS = 2 * SPLIT_WARPS * 2;  // (CTA, epilogue warp, slot) blocks of one split tile
+constexpr int SPLIT_UNIT_FLOATS = 32 * SPLIT_COLS;
+struct SplitPiece {
+    uint16_t kb0, kb1;   // k-block range of the piece
+    uint16_t id;         // split index of the tile (< MAX_SPLIT)
+    uint16_t pad;
+};
 struct ScheduledArgs : KernelArgs {
     uint16_t sched_off[MAX_CLUSTERS + 1];
     uint16_t sched[MAX_SCHED];
+    SplitPiece split[MAX_CLUSTERS][2];
+    float* split_sums;   // [MAX_SPLIT][SPLIT_UNITS][SPLIT_UNIT_FLOATS]
+    int* split_flags;    // [MAX_SPLIT][SPLIT_UNITS][2]: arrivals, sums written
 };
 static_assert(sizeof(ScheduledArgs) <= 32764, "kernel parameter block limit");
+static_assert(MAX_SCHED <= SCHED_TILE_MASK + 1, "tile indices fit below the piece bits");
 
 // Where a launch finds its problems and tile order:
 //   SRC_SINGLE  one problem in the parameter block, tiles round robin over the clusters;
@@ -229,6 +254,7 @@ struct Cfg {
     static constexpr int EIN_SLOTS = ADD ? 2 : 0;
     static constexpr int EIN_SLOT_BYTES = BM * CK * 2;
     static constexpr int CHUNKS = (EPI == EPI_SWIGLU_FWD) ? (BN / 2) / CK : BN / CK;
+    static constexpr int BN_PER_WARP = CHUNKS / (EPI_WARPS / 4) * CK;   // accumulator columns a warp drains per slot
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -343,7 +369,7 @@ __device__ __forceinline__ Problem problem_at(const Args& a, int it, int& pi, in
         lt = v & ((1 << TABLE_TILE_BITS) - 1);
         return a.table[pi].prob;
     } else if constexpr (SRC == SRC_PARAMS) {
-        const int t = a.sched[it];
+        const int t = a.sched[it] & SCHED_TILE_MASK;
         pi = problem_of(a, t);
         const Problem pr = *pick3(pi, &a.prob[0], &a.prob[1], &a.prob[2]);
         lt = t - pr.tile_begin;
@@ -352,6 +378,39 @@ __device__ __forceinline__ Problem problem_at(const Args& a, int it, int& pi, in
         pi = 0;
         lt = it;
         return a.prob[0];
+    }
+}
+
+// k-block range [kb0, kb1) of the it-th entry of cluster c's list and, for a piece of a
+// split tile, the tile's split index (else -1).
+__device__ __forceinline__ int split_piece(const ScheduledArgs& a, int c, int it, int k_blocks, int& kb0, int& kb1) {
+    const int raw = a.sched[it];
+    if (!(raw & SCHED_PIECE)) {
+        kb0 = 0;
+        kb1 = k_blocks;
+        return -1;
+    }
+    const SplitPiece s = a.split[c][(raw & SCHED_PIECE_PREFIX) ? 1 : 0];
+    kb0 = s.kb0;
+    kb1 = s.kb1;
+    return s.id;
+}
+
+// Bounded wait for a flag another CTA of the launch raises (acquire).  False, with the
+// role recorded and the abort flag raised, when the limit runs out.
+__device__ __noinline__ bool wait_flag_bounded(const int* f, unsigned long long timeout_ns, int* err,
+                                               volatile int* abort_flag, int role) {
+    const uint64_t start = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::ld_acquire_gpu(f) != 0) return true;
+        if ((n & 63) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - start > timeout_ns) {
+                *abort_flag = 1;
+                atomicOr(err, role);
+                return false;
+            }
+        }
     }
 }
 
@@ -465,6 +524,10 @@ template <int EPI, int CG, int SCHED, int OP = OP_BF16>
 __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     gemm_kernel(const __grid_constant__ ArgsOf<EPI, CG, SCHED> args) {
     using C = Cfg<EPI, CG>;
+    // pieces of split tiles: one GEMM in 256 x 512 tiles over a host list
+    constexpr bool SPLIT = EPI == EPI_STORE_W && SCHED == SRC_PARAMS;
+    static_assert(!SPLIT || (C::EPI_WARPS == SPLIT_WARPS && C::BN_PER_WARP == SPLIT_COLS),
+                  "split-tile sums: one block of 32 rows x SPLIT_COLS per epilogue warp and slot");
     static_assert(OP == OP_BF16 || ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) && SCHED == SRC_SINGLE),
                   "FP8 operands: forward kernels, one problem per launch");
     constexpr int BKE = OP == OP_E4M3 ? 2 * BK : BK;   // k values per 128-byte k-block
@@ -565,14 +628,14 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 }
                 // One tile's k-blocks.  Called with parameter-block fields wherever the
                 // source allows it (see SRC_TABLE_COMMON).
-                auto tile = [&](const Problem& p, int k_blocks, bool a_mn, bool b_mn, bool a3d, bool b3d,
+                auto tile = [&](const Problem& p, int kb_begin, int kb_end, bool a_mn, bool b_mn, bool a3d, bool b3d,
                                 const CUtensorMap* ma, const CUtensorMap* mb) {
                     int tm, tn;
                     tile_coords(p, lt, tm, tn);
                     const int m0 = tm * (BM * CG) + BM * (int)rank;   // this CTA's A rows
                     const int w = tile_slots<C>(p, tn);
                     const uint32_t tx = (uint32_t)((C::A_BYTES + w * C::B_SLOT_BYTES) * CG);
-                    for (int kb = 0; kb < k_blocks; ++kb) {
+                    for (int kb = kb_begin; kb < kb_end; ++kb) {
                         if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, err, abort_flag, ERR_PRODUCER)) {
                             ok = false;
                             break;
@@ -637,23 +700,25 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 if constexpr (SCHED == SRC_PARAMS) {
                     // one copy per problem index: that problem's fields at fixed offsets
                     auto fixed = [&](const Problem& p, const CUtensorMap* ma, const CUtensorMap* mb) {
-                        tile(p, p.k_blocks, p.a_mn != 0, p.b_mn != 0, p.a3d != 0, p.b3d != 0, ma, mb);
+                        int kb0 = 0, kb1 = p.k_blocks;
+                        if constexpr (SPLIT) split_piece(args, cluster, it, p.k_blocks, kb0, kb1);
+                        tile(p, kb0, kb1, p.a_mn != 0, p.b_mn != 0, p.a3d != 0, p.b3d != 0, ma, mb);
                     };
                     if (pi == 0) fixed(args.prob[0], &args.a[0], &args.b[0]);
                     else if (pi == 1) fixed(args.prob[1], &args.a[1], &args.b[1]);
                     else fixed(args.prob[2], &args.a[2], &args.b[2]);
                 } else if constexpr (SCHED == SRC_TABLE_COMMON) {
-                    tile(pr, args.common_k_blocks, args.common_a_mn != 0, args.common_b_mn != 0, args.common_a3d != 0,
+                    tile(pr, 0, args.common_k_blocks, args.common_a_mn != 0, args.common_b_mn != 0, args.common_a3d != 0,
                          args.common_b3d != 0, mA, mB);
                 } else if constexpr (SCHED == SRC_TABLE) {
                     // one copy per operand layout: the layout as a compile-time constant
                     const bool am = pr.a_mn != 0, bm = pr.b_mn != 0, a3 = pr.a3d != 0, b3 = pr.b3d != 0;
-                    if (am && bm) tile(pr, pr.k_blocks, true, true, a3, b3, mA, mB);
-                    else if (am) tile(pr, pr.k_blocks, true, false, a3, false, mA, mB);
-                    else if (bm) tile(pr, pr.k_blocks, false, true, false, b3, mA, mB);
-                    else tile(pr, pr.k_blocks, false, false, false, false, mA, mB);
+                    if (am && bm) tile(pr, 0, pr.k_blocks, true, true, a3, b3, mA, mB);
+                    else if (am) tile(pr, 0, pr.k_blocks, true, false, a3, false, mA, mB);
+                    else if (bm) tile(pr, 0, pr.k_blocks, false, true, false, b3, mA, mB);
+                    else tile(pr, 0, pr.k_blocks, false, false, false, false, mA, mB);
                 } else {
-                    tile(pr, pr.k_blocks, pr.a_mn != 0, pr.b_mn != 0, pr.a3d != 0, pr.b3d != 0, mA, mB);
+                    tile(pr, 0, pr.k_blocks, pr.a_mn != 0, pr.b_mn != 0, pr.a3d != 0, pr.b3d != 0, mA, mB);
                 }
             }
             if (!ok) {
@@ -677,7 +742,12 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             for (int it = t_first; it < t_end && ok; it += t_step) {
                 int pi, lt;
                 const Problem pq = problem_at<SCHED>(args, it, pi, lt);
-                const int k_blocks = pq.k_blocks;
+                int k_blocks = pq.k_blocks;   // of this entry (a piece of a split tile: its range)
+                if constexpr (SPLIT) {
+                    int kb0, kb1;
+                    split_piece(args, cluster, it, pq.k_blocks, kb0, kb1);
+                    k_blocks = kb1 - kb0;
+                }
                 const bool a_mn = pq.a_mn != 0, b_mn = pq.b_mn != 0;
                 const uint32_t idesc = umma_idesc(a_mn, b_mn, CG, OP == OP_E4M3);
                 // Descriptors of stage 0, k = 0; a stage and a 16-k step only move the start
@@ -976,6 +1046,12 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
             // registers (asm statements clobber memory)
             const Problem pr = problem_at<SCHED>(args, it, pi, lt);
             const int n_limit = pr.N;
+            int sid = -1;   // split index of the tile when this entry is a piece of one
+            if constexpr (SPLIT) {
+                int kb0, kb1;
+                sid = split_piece(args, cluster, it, pr.k_blocks, kb0, kb1);
+            }
+            (void)sid;
             const CUtensorMap* mO0 = map_of<SCHED, MAP_O0>(args, pi);
             const CUtensorMap* mO1 = map_of<SCHED, MAP_O1>(args, pi);
             if (is_table(SCHED) && pi != seen_pi && lane == 0) {
@@ -1011,11 +1087,57 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     // stores.  A 256 x 512 tile's next mainloop waits for its slots' release.
                     constexpr int NCH = C::CHUNKS / GROUPS;
                     uint32_t pk[NCH][16];
+                    // piece of a split tile: 1 = arrived first, writes its fp32 sums; 2 = adds them
+                    int split_role = 0;
+                    float4* sums = nullptr;
+                    int* sflags = nullptr;
+                    if constexpr (SPLIT) {
+                        if (sid >= 0) {
+                            const int unit = ((sid * 2 + (int)rank) * SPLIT_WARPS + (warp - EPI_WARP0)) * 2 + sl;
+                            sflags = args.split_flags + 2 * unit;
+                            sums = reinterpret_cast<float4*>(args.split_sums) + (size_t)unit * (SPLIT_UNIT_FLOATS / 4);
+                            int old = 0;
+                            if (lane == 0) old = atomicAdd(sflags, 1);
+                            split_role = __shfl_sync(0xffffffffu, old, 0) == 0 ? 1 : 2;
+                            if (split_role == 2) {
+                                // the other piece arrived first and is writing its sums
+                                int ready = 1;
+                                if (lane == 0)
+                                    ready = wait_flag_bounded(sflags + 1, tmo, err, abort_flag, ERR_EPILOGUE) ? 1 : 0;
+                                if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                                    ok = false;
+                                    break;
+                                }
+                                __threadfence();
+                            }
+                        }
+                    }
 #pragma unroll
                     for (int i = 0; i < NCH; ++i) {
                         uint32_t acc[32];
                         ptx::tmem_ld_32x32b_x32(t_row + (grp + i * GROUPS) * CHUNK, acc);
                         ptx::tmem_ld_wait();
+                        if constexpr (SPLIT) {
+                            // sums as [chunk][16-byte group][lane]: each store covers 512 contiguous bytes
+                            if (split_role == 1) {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q)
+                                    __stcg(sums + (i * 8 + q) * 32 + lane,
+                                           make_float4(__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
+                                                       __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3])));
+                                continue;
+                            }
+                            if (split_role == 2) {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const float4 v = __ldcg(sums + (i * 8 + q) * 32 + lane);
+                                    acc[4 * q] = __float_as_uint(__uint_as_float(acc[4 * q]) + v.x);
+                                    acc[4 * q + 1] = __float_as_uint(__uint_as_float(acc[4 * q + 1]) + v.y);
+                                    acc[4 * q + 2] = __float_as_uint(__uint_as_float(acc[4 * q + 2]) + v.z);
+                                    acc[4 * q + 3] = __float_as_uint(__uint_as_float(acc[4 * q + 3]) + v.w);
+                                }
+                            }
+                        }
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             pk[i][j] = pack_bf16(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
@@ -1025,6 +1147,15 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     if (lane == 0) {
                         if (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(ab), 0));
                         else ptx::mbar_arrive(tempty_bar(ab));
+                    }
+                    if constexpr (SPLIT) {
+                        if (split_role == 1) {
+                            // sums written: release them to the other piece, which stores the tile
+                            __threadfence();
+                            __syncwarp();
+                            if (lane == 0) ptx::st_release_gpu(sflags + 1, 1);
+                            continue;
+                        }
                     }
 #pragma unroll
                     for (int i = 0; i < NCH; ++i) {

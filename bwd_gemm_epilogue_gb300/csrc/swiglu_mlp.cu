@@ -178,6 +178,8 @@ constexpr int DEBUG_UNGROUPED = 4;
 // with 256 x 512 tiles wherever N > 256 (instead of the choice below).
 constexpr int DEBUG_NARROW_TILES = 32;
 constexpr int DEBUG_WIDE_TILES = 64;
+// Host-only test hook bit: no split tiles (see plan_split).
+constexpr int DEBUG_NO_SPLIT = 128;
 
 // slots: 2 for a problem of 256 x 512 tiles (EPI_STORE_W launches), else 1.
 Problem make_problem(int64_t M, int64_t N, int64_t K, int64_t tiles_n, bool a_mn, bool b_mn, int cg, int slots = 1) {
@@ -706,15 +708,134 @@ int64_t wide_rows(DeviceState* st, int64_t M, int64_t N, int64_t K) {
     return rows;
 }
 
-// One plain GEMM, optionally with a residual added in its epilogue.
+// ---------------------------------------------------------------- split tiles
+// Pieces of split tiles are at least this many k-blocks long: a boundary that would cut a
+// shorter piece moves to the tile's edge.
+constexpr int kSplitMinPiece = 8;
+constexpr size_t kSplitFlagBytes = (size_t)MAX_SPLIT * SPLIT_UNITS * 2 * sizeof(int);
+
+// Workspace bytes the split tiles of one K-major GEMM in 256 x 512 tiles may use: the
+// counter pairs, then the fp32 sums ([MAX_SPLIT][SPLIT_UNITS][32 x SPLIT_COLS]).  Nonzero
+// where such a launch can have them: M >= 256, N a multiple of 512, a long reduction (the
+// rule for 256 x 512 tiles) and at least kSplitMinTiles tiles.
+constexpr int64_t kSplitMinTiles = 144;
+size_t split_ws_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M < 2 * BM || N <= 0 || N % (2 * BN) != 0 || (double)((K + BK - 1) / BK) < kWideMinKBlocksLong) return 0;
+    if ((M + 2 * BM - 1) / (2 * BM) * (N / (2 * BN)) < kSplitMinTiles) return 0;
+    return round256(kSplitFlagBytes) + (size_t)MAX_SPLIT * SPLIT_UNITS * SPLIT_UNIT_FLOATS * sizeof(float);
+}
+
+// Host lists for one GEMM in 256 x 512 tiles (a.prob[0], every tile with both slots).
+// Whole tiles go round robin for all rounds but the last; the k-blocks of the tiles left
+// (between one and two rounds of them) are then divided evenly over the `units` CTA
+// pairs, each pair taking a contiguous run of (tile, k-block).  A tile that a boundary cuts
+// is a split tile: its prefix piece (k-blocks [0, r)) ends one pair's run and its suffix
+// piece ([r, kb)) starts the next one's.  Longest-first lists of whole tiles leave the last
+// round of a launch with few long tiles per pair partly idle (the target block's down
+// projection: 308 tiles over 76 pairs = 4.05 rounds); split tiles fill it.  Even pairs run
+// their prefix piece first and their suffix piece last, odd pairs the reverse, so the two
+// pieces of a tile run at about the same time and the sums pass through L2.
+// At least two rounds of tiles: the pieces start at staggered k-blocks, so concurrent
+// tiles no longer read the same k-slices of A and B, and a launch made of pieces alone
+// (the 4096-token block's down projection: 128 tiles over 76 pairs) measured 3.6 % slower
+// than whole tiles with a partly idle second round.  Returns the number of split tiles,
+// or -1 where this plan does not apply (fewer than two rounds of tiles, a boundary that
+// would leave a tile with three pieces, or lists that do not fit the parameter block).
+int plan_split(ScheduledArgs& a, int units) {
+    const Problem& p = a.prob[0];
+    const int n = p.tiles_m * p.tiles_n, kb = p.k_blocks;
+    if (a.num_problems != 1 || p.slots != 2 || p.N % (2 * BN) != 0) return -1;
+    if (units < 2 || units > MAX_CLUSTERS || n < 2 * units || n + MAX_SPLIT > MAX_SCHED) return -1;
+    if (kb < 4 * kSplitMinPiece || kb > 65535) return -1;
+    const int t0 = (n / units - 1) * units;        // tiles of the whole rounds
+    const int64_t S = (int64_t)(n - t0) * kb;      // k-blocks after them
+    std::vector<int64_t> b(units + 1);
+    for (int u = 0; u <= units; ++u) {
+        int64_t v = (S * u + units / 2) / units;
+        const int64_t r = v % kb;
+        if (r > 0 && r < kSplitMinPiece) v -= r;
+        else if (r > kb - kSplitMinPiece) v += kb - r;
+        b[u] = v;
+    }
+    std::vector<int> id(n - t0, -1);
+    int n_split = 0;
+    for (int u = 1; u <= units; ++u) {
+        if (b[u] <= b[u - 1]) return -1;           // every pair gets k-blocks
+        if (b[u] % kb == 0) continue;
+        const int t = (int)(b[u] / kb);
+        if (id[t] >= 0) return -1;                 // a second boundary in one tile
+        id[t] = n_split++;
+    }
+    if (n_split > MAX_SPLIT) return -1;
+    std::vector<std::vector<uint16_t>> lists(units);
+    for (int t = 0; t < t0; ++t) lists[t % units].push_back((uint16_t)t);
+    for (int u = 0; u < units; ++u) {
+        const int64_t lo = b[u], hi = b[u + 1];
+        const int ta = (int)(lo / kb), oa = (int)(lo % kb);
+        const int tb = (int)((hi - 1) / kb), ob = (int)(hi - (int64_t)tb * kb);
+        const bool suffix = oa > 0, prefix = ob < kb;
+        a.split[u][0] = SplitPiece{(uint16_t)oa, (uint16_t)kb, (uint16_t)(suffix ? id[ta] : 0), 0};
+        a.split[u][1] = SplitPiece{0, (uint16_t)ob, (uint16_t)(prefix ? id[tb] : 0), 0};
+        const uint16_t suf = (uint16_t)((t0 + ta) | SCHED_PIECE);
+        const uint16_t pre = (uint16_t)((t0 + tb) | SCHED_PIECE | SCHED_PIECE_PREFIX);
+        const bool even = u % 2 == 0;
+        std::vector<uint16_t>& L = lists[u];
+        if (even ? prefix : suffix) L.push_back(even ? pre : suf);
+        for (int t = suffix ? ta + 1 : ta; t < (prefix ? tb : tb + 1); ++t) L.push_back((uint16_t)(t0 + t));
+        if (even ? suffix : prefix) L.push_back(even ? suf : pre);
+    }
+    int off = 0;
+    for (int u = 0; u < units; ++u) {
+        a.sched_off[u] = (uint16_t)off;
+        for (uint16_t t : lists[u]) a.sched[off++] = t;
+    }
+    a.sched_off[units] = (uint16_t)off;
+    return n_split;
+}
+
+// One K-major GEMM in 256 x 512 tiles with split tiles at the end of the launch (plan_split),
+// the split tiles' counters and sums in split_ws (split_ws_bytes of them).  Returns
+// SWIGLU_ERR_UNSUPPORTED_SHAPE, having enqueued nothing, where the plan does not apply.
+swiglu_status launch_split(DeviceState* st, int kind, const GemmSpec& g, void* split_ws, cudaStream_t s) {
+    static thread_local ScheduledArgs a;
+    std::memset(static_cast<KernelArgs*>(&a), 0, sizeof(KernelArgs));
+    if (!add_problem(a, 0, g, 2, true)) return fail(SWIGLU_ERR_LAUNCH, "tensor map encode (gemm)");
+    a.num_problems = 1;
+    a.prob[0].tile_begin = 0;
+    a.num_tiles = a.prob[0].tiles_m * a.prob[0].tiles_n;
+    const int slots = cluster_slots<EPI_STORE_W, 2, SRC_PARAMS>(st);
+    if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
+    const int units = a.num_tiles < slots ? a.num_tiles : slots;
+    const int n_split = plan_split(a, units);
+    if (n_split < 0) return SWIGLU_ERR_UNSUPPORTED_SHAPE;
+    a.timeout_ns = g_timeout_ns.load();
+    a.err = st->err_word;
+    a.debug_flags = g_debug_flags.load();
+    a.split_flags = static_cast<int*>(split_ws);
+    a.split_sums = reinterpret_cast<float*>(static_cast<uint8_t*>(split_ws) + round256(kSplitFlagBytes));
+    if (n_split > 0) {
+        const cudaError_t e = cudaMemsetAsync(a.split_flags, 0, (size_t)n_split * SPLIT_UNITS * 2 * sizeof(int), s);
+        if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync(split counters)", e);
+    }
+    return launch_grid<EPI_STORE_W, 2, SRC_PARAMS>(st, kind, a, units, s);
+}
+
+// One plain GEMM, optionally with a residual added in its epilogue.  split_ws: room for
+// split tiles (split_ws_bytes(M, N, K) bytes), or null.
 swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, void* Cp, int64_t M, int64_t N,
-                       int64_t K, bool a_mn, bool b_mn, cudaStream_t s, const void* R = nullptr) {
+                       int64_t K, bool a_mn, bool b_mn, cudaStream_t s, const void* R = nullptr,
+                       void* split_ws = nullptr) {
     const int cg = pick_cg(M);
     KernelArgs a;
     std::memset(&a, 0, sizeof a);
     GemmSpec g{A, B, Cp, M, N, K, a_mn, b_mn};
     g.R = R;
     bool wide = !R && cg == 2 && wide_pays(st, &g, 1, WIDE_LONG_K);
+    if (wide && split_ws && !a_mn && split_ws_bytes(M, N, K) > 0 &&
+        !(g_debug_flags.load() & (DEBUG_NO_SPLIT | DEBUG_WIDE_TILES))) {
+        const swiglu_status rc = launch_split(st, kind, g, split_ws, s);
+        if (rc != SWIGLU_ERR_UNSUPPORTED_SHAPE) return rc;
+    }
     const int64_t rows = wide && !a_mn && !(g_debug_flags.load() & DEBUG_WIDE_TILES) ? wide_rows(st, M, N, K) : M;
     if (rows == 0) wide = false;
     if (wide && rows < M) {
@@ -773,7 +894,7 @@ size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Do
     (void)D;
     if (M <= 0 || H <= 0) return 0;
     if (M <= SK_MAX_M && Dout > 0 && D > 0) return skinny_fwd_ws(M, D, H, Dout, nullptr, nullptr);
-    return round256((size_t)M * (size_t)H * 2);
+    return round256((size_t)M * (size_t)H * 2) + split_ws_bytes(M, Dout, H);
 }
 
 size_t swiglu_mlp_bwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout) {
@@ -803,8 +924,11 @@ static swiglu_status fwd_impl(const void* x, const void* W1, const void* W2, voi
     void* h = workspace;
     rc = run_fwd_preact(st, x, W1, preact, h, M, D, H, s);
     if (rc != SWIGLU_OK) return rc;
-    // y = h @ W2^T (+ x for the residual block, added in the epilogue)
-    return run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h, W2, y, M, Dout, H, false, false, s, residual ? x : nullptr);
+    // y = h @ W2^T (+ x for the residual block, added in the epilogue); split tiles' sums after h
+    void* split = split_ws_bytes(M, Dout, H) ? static_cast<uint8_t*>(workspace) + round256((size_t)M * (size_t)H * 2)
+                                             : nullptr;
+    return run_gemm(st, SWIGLU_KERNEL_FWD_DOWN, h, W2, y, M, Dout, H, false, false, s, residual ? x : nullptr,
+                    split);
 }
 
 swiglu_status swiglu_mlp_fwd(const void* x, const void* W1, const void* W2, void* preact, void* y, int64_t M,
@@ -1055,6 +1179,38 @@ void swiglu_mlp_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 
 void swiglu_mlp_set_debug_flags(int flags) { g_debug_flags.store(flags); }
 
 void swiglu_mlp_set_raster_band(int n_tiles) { g_raster_band.store(n_tiles > 0 ? n_tiles : 0); }
+
+int swiglu_mlp_split_plan(int64_t M, int64_t N, int64_t K, int units, int32_t* out, int cap) {
+    if (M <= 0 || N <= 0 || K <= 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return -1;
+    if (split_ws_bytes(M, N, K) == 0) return -1;
+    static thread_local ScheduledArgs a;
+    std::memset(static_cast<KernelArgs*>(&a), 0, sizeof(KernelArgs));
+    a.prob[0] = make_problem(M, N, K, (N + 2 * BN - 1) / (2 * BN), false, false, 2, 2);
+    a.num_problems = 1;
+    if (plan_split(a, units) < 0) return -1;
+    int rows = 0;
+    for (int u = 0; u < units; ++u) {
+        for (int it = a.sched_off[u]; it < a.sched_off[u + 1]; ++it, ++rows) {
+            if (!out || rows >= cap) continue;
+            const int raw = a.sched[it];
+            int32_t* r = out + 5 * rows;
+            r[0] = u;
+            r[1] = raw & SCHED_TILE_MASK;
+            if (raw & SCHED_PIECE) {
+                const SplitPiece& sp = a.split[u][(raw & SCHED_PIECE_PREFIX) ? 1 : 0];
+                r[2] = sp.kb0;
+                r[3] = sp.kb1;
+                r[4] = sp.id;
+            } else {
+                r[2] = 0;
+                r[3] = a.prob[0].k_blocks;
+                r[4] = -1;
+            }
+        }
+    }
+    return rows;
+}
 
 void swiglu_mlp_trace_begin(void** events, int* kinds, int capacity) {
     Trace& tr = g_trace;

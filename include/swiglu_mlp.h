@@ -59,7 +59,10 @@ typedef enum {
 /* Bytes of workspace swiglu_mlp_fwd needs: the transient h [M,H] bf16; for M <= 64
  * also the small-M path's fp32 partial sums of preact^T [2H, M16] and y^T [Dout, M16]
  * (M16 = M rounded up to 16), one plane per K split (the split counts are planned for
- * 152 SMs), each buffer on a 256-byte boundary. */
+ * 152 SMs), each buffer on a 256-byte boundary.  Where the down projection can split
+ * tiles (M >= 256, Dout a multiple of 512, H >= 6337, at least 144 tiles of 256 x 512;
+ * see swiglu_mlp_split_plan), h is followed by room for their counters and fp32 sums:
+ * 20,480 + 80 x 524,288 bytes. */
 size_t swiglu_mlp_fwd_workspace_size(int64_t M, int64_t D, int64_t H, int64_t Dout);
 
 /* Bytes of workspace swiglu_mlp_bwd needs: h [M,H] and grad_preact [M,2H], bf16,
@@ -290,9 +293,25 @@ void swiglu_mlp_set_wait_timeout_ns(uint64_t ns);
  * small-M path.  Bit 4: MoE launches keep CTA-pair tiles even when 128-row tiles
  * would compute fewer padded rows.  Bit 5: plain GEMMs of CTA pairs always use
  * 256 x 256 tiles; bit 6: they use 256 x 512 tiles wherever N > 256 (by default
- * the library picks per launch).  (Every setting computes the same result; the
- * bits exist to test each path.) */
+ * the library picks per launch).  Bit 7: the forward's down projection splits no
+ * tiles (see swiglu_mlp_split_plan).  (Every setting computes the same result, except
+ * that a split tile adds two fp32 partial sums, so its outputs can differ from the
+ * unsplit tile's in the last bit of rounding; the bits exist to test each path.) */
 void swiglu_mlp_set_debug_flags(int flags);
+
+/* Test hook (host only; needs no GPU): the tile lists of one K-major GEMM, M x N over K,
+ * in 256 x 512 tiles with split tiles, as the forward's down projection runs it on
+ * `units` CTA pairs when N is a multiple of 512 and there are at least two rounds of
+ * tiles (y = h @ W2^T: N = Dout, K = H).  Whole tiles go round robin for all rounds but
+ * the last; the k-blocks of the remaining tiles
+ * are divided evenly over the pairs, and a tile that a boundary cuts is shared by two
+ * pairs, one summing its first k-blocks, the other the rest, in fp32 (the pair finishing
+ * second adds the other's sums and stores the tile).  Writes up to `cap` rows of five
+ * int32: pair, tile (raster index), first k-block, end k-block (exclusive), split index
+ * (-1 for a whole tile); pairs in order, each pair's entries in the order it runs them.
+ * Returns the number of rows (also when above cap; out may be null), or -1 where the
+ * forward does not split tiles for this shape. */
+int swiglu_mlp_split_plan(int64_t M, int64_t N, int64_t K, int units, int32_t* out, int cap);
 
 /* Tuning knob, process-wide: the width, in 256-column units, of the bands the tile
  * kernels walk their output in (all rows of a band before the next band, so a band's

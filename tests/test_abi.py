@@ -26,7 +26,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_workspace_sizes():
     from bwd_gemm_epilogue_gb300 import binding as b
     M, D, H, Dout = 11136, 3584, 14336, 3584
-    assert b.swiglu_mlp_fwd_workspace_size(M, D, H, Dout) == M * H * 2
+    # h, then the down projection's split-tile counters and fp32 sums
+    assert b.swiglu_mlp_fwd_workspace_size(M, D, H, Dout) == M * H * 2 + 20480 + 80 * 524288
     assert b.swiglu_mlp_bwd_workspace_size(M, D, H, Dout) == M * H * 2 + M * 2 * H * 2
     assert b.swiglu_mlp_fwd_workspace_size(0, D, H, Dout) == 0
     # ragged: each buffer starts on a 256-byte boundary
