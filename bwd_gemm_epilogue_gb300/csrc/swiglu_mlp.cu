@@ -732,13 +732,14 @@ size_t split_ws_bytes(int64_t M, int64_t N, int64_t K) {
 // is a split tile: its prefix piece (k-blocks [0, r)) ends one pair's run and its suffix
 // piece ([r, kb)) starts the next one's.  Longest-first lists of whole tiles leave the last
 // round of a launch with few long tiles per pair partly idle (the target block's down
-// projection: 308 tiles over 76 pairs = 4.05 rounds); split tiles fill it.  Even pairs run
-// their prefix piece first and their suffix piece last, odd pairs the reverse, so the two
-// pieces of a tile run at about the same time and the sums pass through L2.
-// At least two rounds of tiles: the pieces start at staggered k-blocks, so concurrent
-// tiles no longer read the same k-slices of A and B, and a launch made of pieces alone
-// (the 4096-token block's down projection: 128 tiles over 76 pairs) measured 3.6 % slower
-// than whole tiles with a partly idle second round.  Returns the number of split tiles,
+// projection: 308 tiles over 76 pairs = 4.05 rounds); split tiles fill it.  Every pair
+// runs its prefix piece first and its suffix piece last: all pairs start the tail at
+// k-block 0, and a pair's suffix piece starts at about the k-block the others reach at
+// that time, so concurrent tiles keep reading the same k-slices of A and B (running one
+// pair's suffix first instead put the pairs at staggered k-blocks: 36 % more DRAM reads).
+// At least two rounds of tiles: a launch made of pieces alone (the 4096-token block's
+// down projection: 128 tiles over 76 pairs) measured 3.6 % slower than whole tiles with a
+// partly idle second round.  Returns the number of split tiles,
 // or -1 where this plan does not apply (fewer than two rounds of tiles, a boundary that
 // would leave a tile with three pieces, or lists that do not fit the parameter block).
 int plan_split(ScheduledArgs& a, int units) {
@@ -778,11 +779,10 @@ int plan_split(ScheduledArgs& a, int units) {
         a.split[u][1] = SplitPiece{0, (uint16_t)ob, (uint16_t)(prefix ? id[tb] : 0), 0};
         const uint16_t suf = (uint16_t)((t0 + ta) | SCHED_PIECE);
         const uint16_t pre = (uint16_t)((t0 + tb) | SCHED_PIECE | SCHED_PIECE_PREFIX);
-        const bool even = u % 2 == 0;
         std::vector<uint16_t>& L = lists[u];
-        if (even ? prefix : suffix) L.push_back(even ? pre : suf);
+        if (prefix) L.push_back(pre);
         for (int t = suffix ? ta + 1 : ta; t < (prefix ? tb : tb + 1); ++t) L.push_back((uint16_t)(t0 + t));
-        if (even ? suffix : prefix) L.push_back(even ? suf : pre);
+        if (suffix) L.push_back(suf);
     }
     int off = 0;
     for (int u = 0; u < units; ++u) {

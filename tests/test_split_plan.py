@@ -1,8 +1,8 @@
 """Host logic of the split tiles (no GPU): the tile lists the forward's down projection
 y = h @ W2^T runs in 256 x 512 tiles when the last round of whole tiles would leave CTA
 pairs idle.  Every tile's reduction must be covered exactly once, by one whole entry or by
-the two pieces of a split tile; the pairs' k-block counts must be even; and the two pieces
-of a split tile must run at about the same point of their pairs' lists."""
+the two pieces of a split tile; the pairs' k-block counts must be even; and each pair's
+tail must start with its prefix piece and end with its suffix piece."""
 import pytest
 
 from bwd_gemm_epilogue_gb300 import binding as b
@@ -48,14 +48,15 @@ def _check(M, N, K, units):
     for u in range(units):
         head = [t for t, k0, k1, sid in by_pair[u][:whole_rounds]]
         assert head == [u + r * units for r in range(whole_rounds)]
-    # the pieces of a tile: first in one list and first in the other, or last in both
-    for sid, (t, ua, uc) in pieces.items():
-        pos = []
-        for u in (ua, uc):
-            tail = by_pair[u][whole_rounds:]
-            i = [e[0] for e in tail].index(t)
-            pos.append("first" if i == 0 else "last" if i == len(tail) - 1 else "middle")
-        assert pos in (["first", "first"], ["last", "last"]), (sid, pos)
+    # every pair's tail starts with its prefix piece (k-block 0, with all other pairs) and
+    # ends with its suffix piece
+    for u in range(units):
+        tail = by_pair[u][whole_rounds:]
+        for i, (t, k0, k1, sid) in enumerate(tail):
+            if sid >= 0 and k0 == 0:
+                assert i == 0, (u, tail)
+            elif sid >= 0:
+                assert i == len(tail) - 1, (u, tail)
     return plan, pieces
 
 
