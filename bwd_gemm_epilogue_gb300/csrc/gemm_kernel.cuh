@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
     gemm_kernel(const __grid_constant__ ArgsOf<EPI, CG, SCHED> args) {
     using C = Cfg<EPI, CG>;
     // pieces of split tiles: one GEMM in 256 x 512 tiles over a host list
-    constexpr bool SPLIT = EPI == EPI_STORE_W && SCHED == SRC_PARAMS;
+    constexpr bool SPLIT = (EPI == EPI_STORE_W || EPI == EPI_STORE_ADD_W) && SCHED == SRC_PARAMS;
     static_assert(!SPLIT || (C::EPI_WARPS == SPLIT_WARPS && C::BN_PER_WARP == SPLIT_COLS),
                   "split-tile sums: one block of 32 rows x SPLIT_COLS per epilogue warp and slot");
     static_assert(OP == OP_BF16 || ((EPI == EPI_STORE || EPI == EPI_SWIGLU_FWD) && SCHED == SRC_SINGLE),
@@ -1080,6 +1080,34 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                 ptx::tc_fence_after();
                 const uint32_t t_row = tmem_base + ((uint32_t)(32 * wq) << 16) + (uint32_t)(ab * BN);
 
+                // piece of a split tile: 1 = arrived first, writes its fp32 sums; 2 = adds them
+                int split_role = 0;
+                float4* sums = nullptr;
+                int* sflags = nullptr;
+                if constexpr (SPLIT) {
+                    if (sid >= 0) {
+                        const int unit = ((sid * 2 + (int)rank) * SPLIT_WARPS + (warp - EPI_WARP0)) * 2 + sl;
+                        sflags = args.split_flags + 2 * unit;
+                        sums = reinterpret_cast<float4*>(args.split_sums) + (size_t)unit * (SPLIT_UNIT_FLOATS / 4);
+                        int old = 0;
+                        if (lane == 0) old = atomicAdd(sflags, 1);
+                        split_role = __shfl_sync(0xffffffffu, old, 0) == 0 ? 1 : 2;
+                        if (split_role == 2) {
+                            // the other piece arrived first and is writing its sums
+                            int ready = 1;
+                            if (lane == 0)
+                                ready = wait_flag_bounded(sflags + 1, tmo, err, abort_flag, ERR_EPILOGUE) ? 1 : 0;
+                            if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                                ok = false;
+                                break;
+                            }
+                            __threadfence();
+                        }
+                    }
+                }
+                (void)sums;
+                (void)sflags;
+
                 constexpr bool FAST = (EPI == EPI_STORE || EPI == EPI_STORE_W || EPI == EPI_STORE_ADD_W) && OP == OP_BF16;
                 if (FAST && !(C::ADD && pr.res)) {
                     // Plain bf16 stores: all of this warp's chunks of the slot into registers as
@@ -1087,31 +1115,6 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     // stores.  A 256 x 512 tile's next mainloop waits for its slots' release.
                     constexpr int NCH = C::CHUNKS / GROUPS;
                     uint32_t pk[NCH][16];
-                    // piece of a split tile: 1 = arrived first, writes its fp32 sums; 2 = adds them
-                    int split_role = 0;
-                    float4* sums = nullptr;
-                    int* sflags = nullptr;
-                    if constexpr (SPLIT) {
-                        if (sid >= 0) {
-                            const int unit = ((sid * 2 + (int)rank) * SPLIT_WARPS + (warp - EPI_WARP0)) * 2 + sl;
-                            sflags = args.split_flags + 2 * unit;
-                            sums = reinterpret_cast<float4*>(args.split_sums) + (size_t)unit * (SPLIT_UNIT_FLOATS / 4);
-                            int old = 0;
-                            if (lane == 0) old = atomicAdd(sflags, 1);
-                            split_role = __shfl_sync(0xffffffffu, old, 0) == 0 ? 1 : 2;
-                            if (split_role == 2) {
-                                // the other piece arrived first and is writing its sums
-                                int ready = 1;
-                                if (lane == 0)
-                                    ready = wait_flag_bounded(sflags + 1, tmo, err, abort_flag, ERR_EPILOGUE) ? 1 : 0;
-                                if (!__shfl_sync(0xffffffffu, ready, 0)) {
-                                    ok = false;
-                                    break;
-                                }
-                                __threadfence();
-                            }
-                        }
-                    }
 #pragma unroll
                     for (int i = 0; i < NCH; ++i) {
                         uint32_t acc[32];
@@ -1196,6 +1199,26 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                             else ptx::mbar_arrive(tempty_bar(ab));
                         }
                     }
+                    if constexpr (SPLIT) {
+                        // a piece of a split tile (residual store): the sums as in the plain store
+                        const int i = (c - grp) / GROUPS;
+                        if (split_role == 1) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                __stcg(sums + (i * 8 + q) * 32 + lane,
+                                       make_float4(__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
+                                                   __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3])));
+                        } else if (split_role == 2) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 v = __ldcg(sums + (i * 8 + q) * 32 + lane);
+                                acc[4 * q] = __float_as_uint(__uint_as_float(acc[4 * q]) + v.x);
+                                acc[4 * q + 1] = __float_as_uint(__uint_as_float(acc[4 * q + 1]) + v.y);
+                                acc[4 * q + 2] = __float_as_uint(__uint_as_float(acc[4 * q + 2]) + v.z);
+                                acc[4 * q + 3] = __float_as_uint(__uint_as_float(acc[4 * q + 3]) + v.w);
+                            }
+                        }
+                    }
 
                     // epilogue input of the residual store: the residual's 32 columns
                     uint32_t lft[16];
@@ -1219,6 +1242,9 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive(ein_empty_bar(slot));
                     }
+                    // the first piece of a split tile takes its residual chunk off the ring and
+                    // leaves the tile to the other piece
+                    if (SPLIT && split_role == 1) continue;
                     // outputs for this chunk, packed bf16 pairs (the FP8 forward's h: 4 codes a word)
                     uint32_t o0[16], o1[16], o2[16];
                     if (OP == OP_E4M3) {
@@ -1308,6 +1334,14 @@ __global__ void __launch_bounds__(Cfg<EPI, CG>::THREADS, 1)
                     if (lane == 0) ptx::bulk_commit_group();
                     ob = (ob + 1) % C::OUT_BUFS;
                 }
+                }
+                if constexpr (SPLIT) {
+                    if (split_role == 1) {
+                        // sums written: release them to the other piece
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) ptx::st_release_gpu(sflags + 1, 1);
+                    }
                 }
                 if (C::ADD && pr.res) ++res_slots;
             }

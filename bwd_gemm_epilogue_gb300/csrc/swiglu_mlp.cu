@@ -793,9 +793,11 @@ int plan_split(ScheduledArgs& a, int units) {
     return n_split;
 }
 
-// One K-major GEMM in 256 x 512 tiles with split tiles at the end of the launch (plan_split),
-// the split tiles' counters and sums in split_ws (split_ws_bytes of them).  Returns
-// SWIGLU_ERR_UNSUPPORTED_SHAPE, having enqueued nothing, where the plan does not apply.
+// One K-major GEMM in 256 x 512 tiles (EPI_STORE_W, or EPI_STORE_ADD_W with g's residual)
+// with split tiles at the end of the launch (plan_split), the split tiles' counters and sums
+// in split_ws (split_ws_bytes of them).  Returns SWIGLU_ERR_UNSUPPORTED_SHAPE, having
+// enqueued nothing, where the plan does not apply.
+template <int EPI>
 swiglu_status launch_split(DeviceState* st, int kind, const GemmSpec& g, void* split_ws, cudaStream_t s) {
     static thread_local ScheduledArgs a;
     std::memset(static_cast<KernelArgs*>(&a), 0, sizeof(KernelArgs));
@@ -803,7 +805,7 @@ swiglu_status launch_split(DeviceState* st, int kind, const GemmSpec& g, void* s
     a.num_problems = 1;
     a.prob[0].tile_begin = 0;
     a.num_tiles = a.prob[0].tiles_m * a.prob[0].tiles_n;
-    const int slots = cluster_slots<EPI_STORE_W, 2, SRC_PARAMS>(st);
+    const int slots = cluster_slots<EPI, 2, SRC_PARAMS>(st);
     if (slots <= 0) return fail(SWIGLU_ERR_LAUNCH, "cudaOccupancyMaxActiveClusters");
     const int units = a.num_tiles < slots ? a.num_tiles : slots;
     const int n_split = plan_split(a, units);
@@ -817,7 +819,7 @@ swiglu_status launch_split(DeviceState* st, int kind, const GemmSpec& g, void* s
         const cudaError_t e = cudaMemsetAsync(a.split_flags, 0, (size_t)n_split * SPLIT_UNITS * 2 * sizeof(int), s);
         if (e != cudaSuccess) return fail(SWIGLU_ERR_CUDA, "cudaMemsetAsync(split counters)", e);
     }
-    return launch_grid<EPI_STORE_W, 2, SRC_PARAMS>(st, kind, a, units, s);
+    return launch_grid<EPI, 2, SRC_PARAMS>(st, kind, a, units, s);
 }
 
 // One plain GEMM, optionally with a residual added in its epilogue.  split_ws: room for
@@ -830,12 +832,14 @@ swiglu_status run_gemm(DeviceState* st, int kind, const void* A, const void* B, 
     std::memset(&a, 0, sizeof a);
     GemmSpec g{A, B, Cp, M, N, K, a_mn, b_mn};
     g.R = R;
-    bool wide = !R && cg == 2 && wide_pays(st, &g, 1, WIDE_LONG_K);
-    if (wide && split_ws && !a_mn && split_ws_bytes(M, N, K) > 0 &&
+    const bool wide_ok = cg == 2 && wide_pays(st, &g, 1, WIDE_LONG_K);
+    if (wide_ok && split_ws && !a_mn && split_ws_bytes(M, N, K) > 0 &&
         !(g_debug_flags.load() & (DEBUG_NO_SPLIT | DEBUG_WIDE_TILES))) {
-        const swiglu_status rc = launch_split(st, kind, g, split_ws, s);
+        const swiglu_status rc = R ? launch_split<EPI_STORE_ADD_W>(st, kind, g, split_ws, s)
+                                   : launch_split<EPI_STORE_W>(st, kind, g, split_ws, s);
         if (rc != SWIGLU_ERR_UNSUPPORTED_SHAPE) return rc;
     }
+    bool wide = !R && wide_ok;
     const int64_t rows = wide && !a_mn && !(g_debug_flags.load() & DEBUG_WIDE_TILES) ? wide_rows(st, M, N, K) : M;
     if (rows == 0) wide = false;
     if (wide && rows < M) {

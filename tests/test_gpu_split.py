@@ -51,10 +51,10 @@ def tile_rows(M, seed):
     return np.unique(np.asarray(out, dtype=np.int64))
 
 
-def forward(b, x, W1, W2, flags=0):
+def forward(b, x, W1, W2, flags=0, residual=False):
     b.swiglu_mlp_set_debug_flags(flags)
     try:
-        _, y = b.swiglu_mlp_fwd(x, W1, W2)
+        _, y = b.swiglu_mlp_fwd(x, W1, W2, residual=residual)
         ok_status(b)
     finally:
         b.swiglu_mlp_set_debug_flags(0)
@@ -87,15 +87,32 @@ def test_split_tiles_match_oracle(b, s):
     close_to_unsplit(y, forward(b, xd, W1d, W2d, NO_SPLIT))
 
 
-@pytest.mark.parametrize("name", ["target"])
-def test_split_tiles_full_size_against_unsplit_and_reproducible(b, name):
-    s, x, W1, W2, _ = workloads.make_block(name)
+@pytest.mark.parametrize("residual", [False, True], ids=["plain", "residual"])
+def test_split_tiles_full_size_against_unsplit_and_reproducible(b, residual):
+    s, x, W1, W2, _ = workloads.make_block("target")
     assert b.swiglu_mlp_split_plan(s.M, s.Dout, s.H, 76) is not None
     xd, W1d, W2d = dev(x), dev(W1), dev(W2)
-    y1 = forward(b, xd, W1d, W2d)
-    y2 = forward(b, xd, W1d, W2d)
+    y1 = forward(b, xd, W1d, W2d, residual=residual)
+    y2 = forward(b, xd, W1d, W2d, residual=residual)
     assert torch.equal(y1, y2)   # which piece of a split tile arrives first does not matter
-    close_to_unsplit(y1, forward(b, xd, W1d, W2d, NO_SPLIT))
+    close_to_unsplit(y1, forward(b, xd, W1d, W2d, NO_SPLIT, residual=residual))
+
+
+def test_split_tiles_residual_block_matches_oracle(b):
+    # y = x + h @ W2^T with the residual added once, in fp32, by the piece that stores the tile
+    s = Shape(5120, 4096, 6400, 4096)
+    assert b.swiglu_mlp_split_plan(s.M, s.Dout, s.H, 76) is not None
+    _, x, W1, W2, _ = workloads.make_block(s, seed=64)
+    xd, W1d, W2d = dev(x), dev(W1), dev(W2)
+    y = forward(b, xd, W1d, W2d, residual=True)
+    rows = tile_rows(s.M, 65)
+    _, _, y_ref = oracle.fwd(x, W1, W2, rows=rows, residual=True)
+    parity(y[rows], y_ref, "y[rows] (residual)")
+    for t in np.unique(rows // 256):
+        r = rows[rows // 256 == t]
+        k = np.searchsorted(rows, r)
+        parity(y[r], y_ref[k], f"residual y rows of M-tile {t}", rel_fro=TILE_REL_FRO)
+    close_to_unsplit(y, forward(b, xd, W1d, W2d, NO_SPLIT, residual=True))
 
 
 def test_split_launch_times_out_and_recovers(b):
