@@ -130,3 +130,45 @@ def test_split_launch_times_out_and_recovers(b):
         b.swiglu_mlp_set_wait_timeout_ns(4_000_000_000)
     assert b.swiglu_mlp_device_status() == 0
     assert torch.equal(forward(b, xd, W1d, W2d), ref)
+
+
+def test_split_forward_in_a_cuda_graph_and_on_two_streams(b):
+    # the split launch enqueues a memset of its counters and the kernel on the caller's
+    # stream: a CUDA graph replays it with the direct call's bits, and forwards on two
+    # streams with their own workspaces (their own counters and sums) do not interfere
+    s = SHAPES[0]
+    _, x, W1, W2, _ = workloads.make_block(s, seed=66)
+    xd, W1d, W2d = dev(x), dev(W1), dev(W2)
+    x2 = dev(workloads.make_block(s, seed=67)[1])
+    ref = forward(b, xd, W1d, W2d)
+    ref2 = forward(b, x2, W1d, W2d)
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    preact, y = torch.empty(s.M, 2 * s.H, **bf), torch.empty(s.M, s.Dout, **bf)
+    ws = torch.empty(b.swiglu_mlp_fwd_workspace_size(s.M, s.D, s.H, s.Dout), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        b.swiglu_mlp_fwd(xd, W1d, W2d, preact, y, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        b.swiglu_mlp_fwd(xd, W1d, W2d, preact, y, ws)
+    y.zero_()
+    g.replay()
+    g.replay()
+    ok_status(b)
+    assert torch.equal(y, ref)
+
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        outs = []
+        for st, xi in zip(streams, (xd, x2)):
+            with torch.cuda.stream(st):
+                outs.append(b.swiglu_mlp_fwd(xi, W1d, W2d)[1])
+        for st in streams:
+            torch.cuda.current_stream().wait_stream(st)
+        ok_status(b)
+        assert torch.equal(outs[0], ref) and torch.equal(outs[1], ref2)
