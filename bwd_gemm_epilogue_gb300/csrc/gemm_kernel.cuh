@@ -142,7 +142,8 @@ struct KernelArgs {
 constexpr int MAX_CLUSTERS = 128;
 constexpr int MAX_SCHED = 12288;
 
-// Split tiles (one GEMM in 256 x 512 tiles, EPI_STORE_W with a host list).  The last
+// Split tiles (one GEMM in 256 x 512 tiles with a host list: EPI_STORE_W, or EPI_STORE_ADD_W,
+// whose split tiles add the residual once, in the piece that stores the tile).  The last
 // tiles of such a launch may each be shared by two CTA pairs, one summing the tile's first
 // k-blocks (its prefix piece), the other the rest (its suffix piece), so that every pair
 // gets the same number of k-blocks.  A list entry with SCHED_PIECE set is such a piece: its
@@ -154,7 +155,7 @@ constexpr int MAX_SCHED = 12288;
 // does not depend on which piece arrives first.
 constexpr int MAX_SPLIT = 80;
 constexpr int SCHED_TILE_MASK = 0x3FFF, SCHED_PIECE_PREFIX = 0x4000, SCHED_PIECE = 0x8000;
-constexpr int SPLIT_WARPS = 8, SPLIT_COLS = 128;   // epilogue warps of EPI_STORE_W; columns per warp and slot
+constexpr int SPLIT_WARPS = 8, SPLIT_COLS = 128;   // epilogue warps of the 256 x 512 stores; columns per warp and slot
 constexpr int SPLIT_UNITS = 2 * SPLIT_WARPS * 2;  // (CTA, epilogue warp, slot) blocks of one split tile
 constexpr int SPLIT_UNIT_FLOATS = 32 * SPLIT_COLS;
 struct SplitPiece {
