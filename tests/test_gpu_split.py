@@ -20,8 +20,9 @@ pytestmark = pytest.mark.gpu
 NO_SPLIT, SKIP_PRODUCER = 128, 1
 
 # 160 tiles (one whole round, then 84 tiles' k-blocks shared, 100 k-blocks per tile);
-# ragged rows (the last row tile ends inside a CTA pair) with 24 x 10 tiles
-SHAPES = [Shape(5120, 256, 6400, 4096), Shape(6000, 512, 7168, 5120)]
+# ragged rows (the last row tile ends inside a CTA pair) with 24 x 10 tiles; 16 x 16 tiles
+# (four raster bands of column tiles, the tail crossing bands)
+SHAPES = [Shape(5120, 256, 6400, 4096), Shape(6000, 512, 7168, 5120), Shape(4096, 512, 8192, 8192)]
 
 
 @pytest.fixture(scope="module")
